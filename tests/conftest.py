@@ -1,0 +1,12 @@
+"""Shared pytest setup: the repository root on sys.path and the ``gpu`` marker."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA device (runs on the GB300 box)")
+    config.addinivalue_line("markers", "slow: long-running CPU test")

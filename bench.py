@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of split-KV MLA decode (partial + LSE combine) on GB300.
+
+Default workload: dense MLA decode, batch 1, H=16, d_c=512 + d_r=64, context
+T=8192, bf16 N(0,1) inputs, scale 1/sqrt(576).  One *step* is one pass of the
+hot path over every cache copy: the copies (distinct caches, as the layers of
+a model would be) together exceed 3x the L2, so every call reads its cache
+from HBM.  The calls of one step are captured as one CUDA graph and replayed.
+
+Prints ONE JSON line: metric/value (achieved HBM GB/s of the whole call,
+algorithmic bytes / time per call), us_per_call, the roofline of the partial
+kernel (live CUDA-event timing), the end-to-end number through the C ABI with
+host buffers, the oracle timed on the host cores, and the SM clocks seen during
+the timed region.  ``--impl reference`` times the fp64 CPU oracle instead.
+``--details PATH`` also writes every workload and a context sweep to PATH.
+
+Multi-GPU: replicas only (each rank runs its own copy of the workload; no
+collective on the data path; max time over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MLA decode µs/call and achieved HBM GB/s (fraction of roofline) on 1 GB300"
+ROW_BYTES = 1152
+FLOP_PER_ROW_HEAD = 2 * (576 + 512)
+
+
+# --------------------------------------------------------------------------- utils
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for fn in ("mla_partial_mma.cu", "device_utils.cuh", "mla_internal.h"):
+        with open(os.path.join(ROOT, "decode_attention_mla_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel, workload):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None
+    if the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_sha256") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workloads
+class DenseBench:
+    """Dense decode over `copies` distinct caches of T rows (B=1)."""
+
+    def __init__(self, T, H, copies, splits, pdl, seed=0):
+        import decode_attention_mla_gb300 as mla
+        self.mla = mla
+        d = torch.device("cuda")
+        self.T, self.H, self.copies = T, H, copies
+        x = workloads.dense(1, H, T, seed=seed)
+        self.host = x
+        # copy 0 is the seeded workload; the others are shifted versions (distinct bytes, same distribution)
+        self.kv = [x.kv.to(d)]
+        for c in range(1, copies):
+            self.kv.append(torch.roll(self.kv[0], shifts=c * 37, dims=0))
+        self.q = [x.q.to(d) for _ in range(copies)]
+        self.d_pos = x.d_pos.to(d)
+        self.out = [torch.empty(1, H, 512, device=d) for _ in range(copies)]
+        self.lse = [torch.empty(1, H, device=d) for _ in range(copies)]
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=T, scale=x.scale, splits=splits, pdl=pdl)
+        self.scratch = mla.alloc_scratch(self.plan)
+        self.args = [mla.make_args(self.q[c], self.kv[c], self.out[c], self.lse[c], d_pos=self.d_pos)
+                     for c in range(copies)]
+        self.alg_bytes = T * ROW_BYTES + H * 576 * 2 + 4 + H * 512 * 4 + H * 4
+        self.flops = T * H * FLOP_PER_ROW_HEAD
+
+    def call(self, c, stream=None):
+        self.mla.forward_args(self.plan, self.args[c], self.scratch, stream)
+
+    def partial(self, c, stream=None):
+        self.mla.run(self.plan, self.args[c], self.scratch, stream)
+
+
+class SparseBench:
+    """Sparse decode; `copies` distinct caches when one cache is below 3x L2."""
+
+    def __init__(self, name, copies, splits, pdl, seed=0):
+        import decode_attention_mla_gb300 as mla
+        self.mla = mla
+        d = torch.device("cuda")
+        x = workloads.make(name, seed=seed)
+        self.host = x
+        B, H, _ = x.q.shape
+        topk = x.indices.shape[1]
+        self.copies = copies
+        self.kv = [x.kv.to(d)]
+        for c in range(1, copies):
+            self.kv.append(torch.roll(self.kv[0], shifts=c * 37, dims=0))
+        self.q = x.q.to(d)
+        self.idx = x.indices.to(d)
+        self.len = x.cache_len.to(d)
+        self.off = x.row_offset.to(d)
+        self.out = [torch.empty(B, H, 512, device=d) for _ in range(copies)]
+        self.lse = [torch.empty(B, H, device=d) for _ in range(copies)]
+        self.plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl)
+        self.scratch = mla.alloc_scratch(self.plan)
+        self.args = [mla.make_args(self.q, self.kv[c], self.out[c], self.lse[c], indices=self.idx,
+                                   cache_len=self.len, row_offset=self.off) for c in range(copies)]
+        valid = int(((x.indices >= 0) & (x.indices < x.cache_len[:, None])).sum())
+        self.alg_bytes = valid * ROW_BYTES + B * H * 576 * 2 + B * topk * 4 + B * 12 + B * H * 512 * 4 + B * H * 4
+        self.flops = valid * H * FLOP_PER_ROW_HEAD
+
+    def call(self, c, stream=None):
+        self.mla.forward_args(self.plan, self.args[c], self.scratch, stream)
+
+    def partial(self, c, stream=None):
+        self.mla.run(self.plan, self.args[c], self.scratch, stream)
+
+
+def capture(fn, n):
+    """CUDA graph of fn(0..n-1) on a side stream (warmed up eagerly first)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for c in range(n):
+            fn(c)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in range(n):
+            fn(c)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, reps, warmup):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3          # seconds
+
+
+def per_rep_times(g, reps):
+    """Individual replay times (seconds), for the spread."""
+    st = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    evs[0].record(st)
+    for r in range(reps):
+        g.replay()
+        evs[r + 1].record(st)
+    torch.cuda.synchronize()
+    return [evs[r].elapsed_time(evs[r + 1]) / 1e3 for r in range(reps)]
+
+
+def l2_bytes():
+    return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20))
+
+
+def copies_for(bytes_per_cache):
+    return max(1, math.ceil(3 * l2_bytes() / bytes_per_cache))
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_time_dense(x, budget_s, threads=0):
+    import oracle
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode(x.q, x.kv, scale=x.scale, d_pos=x.d_pos, n_threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / n, n
+
+
+def cpu_baseline(bench, budget_s):
+    import oracle
+    threads = oracle.hardware_threads()
+    per_call, n = oracle_time_dense(bench.host, budget_s, threads)
+    return {"value": bench.alg_bytes / per_call / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full calls of the dense T={bench.T} H={bench.H} workload (fp64 oracle, "
+                      f"{threads} threads), {per_call * 1e3:.1f} ms/call"}
+
+
+# --------------------------------------------------------------------------- e2e
+def e2e_dense(bench, calls):
+    """Through the public C ABI with host buffers: per call, H2D of q and d_pos
+    from pinned memory, partial + combine, D2H of out and lse, synchronise."""
+    mla = bench.mla
+    H = bench.H
+    q_h = bench.host.q.pin_memory()
+    dpos_h = bench.host.d_pos.pin_memory()
+    out_h = torch.empty(1, H, 512).pin_memory()
+    lse_h = torch.empty(1, H).pin_memory()
+    q_d = torch.empty_like(bench.q[0])
+    dpos_d = torch.empty_like(bench.d_pos)
+    out_d = torch.empty(1, H, 512, device="cuda")
+    lse_d = torch.empty(1, H, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def one(c):
+        q_d.copy_(q_h, non_blocking=True)
+        dpos_d.copy_(dpos_h, non_blocking=True)
+        mla.forward(bench.plan, q_d, bench.kv[c % bench.copies], out_d, lse_d, bench.scratch, d_pos=dpos_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+        st.synchronize()
+
+    for c in range(20):
+        one(c)
+    t0 = time.perf_counter()
+    for c in range(calls):
+        one(c)
+    el = time.perf_counter() - t0
+    per = el / calls
+    h2d = q_h.numel() * 2 + 4
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    return {"value": bench.alg_bytes / per / 1e9, "unit": "GB/s", "us_per_call": per * 1e6,
+            "h2d_bytes_per_step": h2d * bench.copies, "d2h_bytes_per_step": d2h * bench.copies,
+            "calls": calls}
+
+
+# --------------------------------------------------------------------------- main arms
+def run_ours(args, rank, world):
+    import decode_attention_mla_gb300 as mla
+    from decode_attention_mla_gb300 import build as mla_build
+    mla_build.build()
+    dev_index = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev_index)
+    P = peaks()
+    T = 8192
+    H = 16
+    copies = copies_for(T * ROW_BYTES)
+    bench = DenseBench(T, H, copies, args.splits, bool(args.pdl))
+    g = capture(bench.call, copies)
+    gp = capture(bench.partial, copies)
+    # choose K for ~2 s of timed work unless given
+    t_one = time_graph(g, 20, 3) / 20
+    steps = args.steps if args.steps > 0 else max(10, int(2.0 / max(t_one, 1e-6)))
+    warm = max(3, args.warmup)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        elapsed = time_graph(g, steps, warm)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    calls = steps * copies
+    us_call = elapsed / calls * 1e6
+    value = world * bench.alg_bytes * calls / elapsed / 1e9
+
+    # dominant kernel (split partial): live CUDA-event time per launch, same copies
+    t_part = time_graph(gp, max(10, steps // 2), warm) / (max(10, steps // 2) * copies)
+    part_bytes = T * ROW_BYTES + H * 576 * 2 + 4      # KV rows + q + d_pos read by the partial kernel
+    achieved = part_bytes / t_part / 1e9
+    traffic = ncu_traffic("mla_partial_mma_kernel", "dense_t8192")
+    reps = per_rep_times(g, 20)
+    per_call_reps = [r / copies * 1e6 for r in reps]
+    clocks = clk.summary()
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": round(elapsed / steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "dense_t8192", "batch": 1, "heads": H, "d_latent": 512, "d_rope": 64,
+                   "context": T, "splits": bench.plan.splits, "pdl": bool(args.pdl),
+                   "calls_per_step": copies,
+                   "l2": f"inputs larger than L2: {copies} distinct caches x {T * ROW_BYTES / 1e6:.2f} MB "
+                         f"= {copies * T * ROW_BYTES / 1e6:.0f} MB (> 3x L2 {l2_bytes() / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": round(us_call, 4),
+        "us_per_call_reps": [round(x, 4) for x in per_call_reps],
+        "us_per_call_sd": round(statistics.pstdev(per_call_reps), 4),
+        "roofline_us": round(bench.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, 4),
+        "frac_of_roofline": round(bench.alg_bytes / (P["hbm_gbs"] * 1e9) / (us_call * 1e-6), 4),
+        "frac_of_roofline_8tbs": round(bench.alg_bytes / 8e12 / (us_call * 1e-6), 4),
+        "alg_bytes_per_call": bench.alg_bytes,
+        "roofline": {"kernel": "mla_partial_mma_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": P["hbm_gbs"], "peak_source": P["source"] + " (burst copy)", "unit": "GB/s",
+                     "frac": round(achieved / P["hbm_gbs"], 4), "traffic": traffic,
+                     "alg_bytes_per_launch": part_bytes, "us_per_launch": round(t_part * 1e6, 4)},
+        "gpu_launches": 2 * calls,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        result["e2e"] = e2e_dense(bench, calls=2000)
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(bench, args.cpu_seconds)
+        if args.details:
+            result["details_file"] = args.details
+            write_details(args, P)
+    return result
+
+
+def run_reference(args):
+    import oracle
+    T, H = 8192, 16
+    x = workloads.dense(1, H, T, seed=0)
+    alg = T * ROW_BYTES + H * 576 * 2 + 4 + H * 512 * 4 + H * 4
+    threads = oracle.hardware_threads()
+    steps = args.steps if args.steps > 0 else 10
+    for _ in range(max(1, min(args.warmup, 3))):
+        oracle.decode(x.q, x.kv, scale=x.scale, d_pos=x.d_pos, n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.decode(x.q, x.kv, scale=x.scale, d_pos=x.d_pos, n_threads=threads)
+    el = time.perf_counter() - t0
+    value = alg * steps / el / 1e9
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "dense_t8192", "batch": 1, "heads": H, "context": T, "calls_per_step": 1},
+            "us_per_call": round(el / steps * 1e6, 1),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{steps} full calls of dense T={T} H={H}"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------- details (all workloads)
+def time_bench(bench, reps=200, warm=5):
+    g = capture(bench.call, bench.copies)
+    gp = capture(bench.partial, bench.copies)
+    el = time_graph(g, reps, warm)
+    elp = time_graph(gp, reps, warm)
+    rep_list = per_rep_times(g, 20)
+    us = el / (reps * bench.copies) * 1e6
+    return us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list]
+
+
+def write_details(args, P):
+    rows = []
+
+    def entry(name, bench, us, us_part, reps, extra=None):
+        r = {"workload": name, "splits": bench.plan.splits, "copies": bench.copies, "us_per_call": us,
+             "us_partial": us_part, "sd_us": statistics.pstdev(reps), "alg_bytes": bench.alg_bytes,
+             "gbs": bench.alg_bytes / (us * 1e-6) / 1e9,
+             "frac_hbm": bench.alg_bytes / (P["hbm_gbs"] * 1e9) / (us * 1e-6),
+             "frac_8tbs": bench.alg_bytes / 8e12 / (us * 1e-6),
+             "tflops": bench.flops / (us * 1e-6) / 1e12}
+        r.update(extra or {})
+        rows.append(r)
+        log(json.dumps(r))
+
+    for T in (256, 8192, 16384, 32768, 65536, 131072):
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl))
+        us, usp, reps = time_bench(b)
+        entry(f"dense_h16_t{T}", b, us, usp, reps)
+        del b
+    for s in (1, 2, 4, 8, 16, 32, 64, 128):
+        b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), s, bool(args.pdl))
+        us, usp, reps = time_bench(b)
+        entry("dense_t8192_split_sweep", b, us, usp, reps)
+        del b
+    # a call touches only its gathered rows: enough distinct caches that those exceed 3x L2
+    b = SparseBench("sparse_k2048", copies_for(2048 * ROW_BYTES), args.splits, bool(args.pdl))
+    us, usp, reps = time_bench(b)
+    entry("sparse_k2048", b, us, usp, reps)
+    del b
+    torch.cuda.empty_cache()
+    b = SparseBench("sparse_b64", copies_for(64 * 2048 * ROW_BYTES), args.splits, bool(args.pdl))
+    us, usp, reps = time_bench(b, reps=50)
+    entry("sparse_b64", b, us, usp, reps)
+    del b
+    torch.cuda.empty_cache()
+    with open(args.details, "w") as f:
+        json.dump({"peaks": P, "rows": rows}, f, indent=1)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0 = about 2 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=int(os.environ.get("MLA_DECODE_SPLITS", "0")))
+    ap.add_argument("--pdl", type=int, default=int(os.environ.get("MLA_DECODE_PDL", "1")))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--details", default=None)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,312 @@
+// mla_decode_api.cu -- the C ABI declared in include/mla_decode.h: the
+// planner, argument checks and kernel launches.  Host code only.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+constexpr int kPlanMagic = 0x4d4c4131;       // "MLA1"
+constexpr int kMaxDevices = 64;
+// Resident-CTA target of the split derivation: two partial CTAs per SM, so
+// one CTA's copies overlap the other's math ("Launch Geometry", Lecture 04,
+// s.4: kMlaBlocksPerSm = 2, named beside the derivation it drives).
+constexpr int kCtasPerSmTarget = 2;
+// A slice must read at least this many times the bytes its partials write.
+constexpr int kSliceBytesOverPartialBytes = 2;
+constexpr size_t kScratchAlign = 256;
+
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_prepared[kMaxDevices];
+std::mutex g_prepare_mutex;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ECUDA;
+    }
+    if (*dev < 0 || *dev >= kMaxDevices) return MLA_ECUDA;
+    return MLA_OK;
+}
+
+int device_sm_count(int dev, int* sms) {
+    int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (cached == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            return MLA_ECUDA;
+        }
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+        cached = v;
+    }
+    *sms = cached;
+    return MLA_OK;
+}
+
+// Kernel attributes are set once per device, outside any capture
+// ("Graph-resident decode", Lecture 08, s.3: lazy initialisation inside a
+// capture breaks it, so it is done up front).
+int prepare_device(int dev) {
+    if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
+    std::lock_guard<std::mutex> lock(g_prepare_mutex);
+    if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
+    if (mla::partial_mma_prepare(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ECUDA;
+    }
+    g_prepared[dev].store(1, std::memory_order_release);
+    return MLA_OK;
+}
+
+int ensure_prepared(cudaStream_t stream) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc != MLA_OK) return rc;
+    if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ECUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return MLA_ENOTREADY;
+    return prepare_device(dev);
+}
+
+int check_shape(const mla_decode_shape* s) {
+    if (!s) return MLA_EINVAL;
+    if (s->batch < 1 || s->batch > 65535) return MLA_EINVAL;
+    if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
+    if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
+    if (s->variant < 0 || s->variant > 1) return MLA_EINVAL;
+    if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
+    if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
+    if (!s->sparse && s->max_ctx < 1) return MLA_EINVAL;
+    if (s->sparse && s->topk < 1) return MLA_EINVAL;
+    if (s->d_latent != MLA_D_LATENT || s->d_rope != MLA_D_ROPE) return MLA_EUNSUPPORTED;
+    if (s->heads != 16 && s->heads != 32 && s->heads != 64 && s->heads != 128) return MLA_EUNSUPPORTED;
+    return MLA_OK;
+}
+
+int check_plan(const mla_decode_plan_t* pl) {
+    if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
+    if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
+    if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
+    if (pl->head_group != mla::kHeadGroup || pl->n_head_groups * pl->head_group != pl->shape.heads) return MLA_EINVAL;
+    if (pl->grid_x != pl->n_head_groups || pl->grid_y != pl->splits || pl->grid_z != pl->shape.batch)
+        return MLA_EINVAL;
+    return MLA_OK;
+}
+
+int check_args(const mla_decode_plan_t* pl, const mla_decode_args* a) {
+    if (!a || !a->q || !a->kv || !a->out || !a->lse) return MLA_EINVAL;
+    if (a->kv_rows < 1 || a->row_stride < MLA_D_ROW) return MLA_EINVAL;
+    if (a->row_stride % 8 != 0) return MLA_EALIGN;
+    if (misaligned(a->q, 16) || misaligned(a->kv, 16) || misaligned(a->out, 16) || misaligned(a->lse, 4))
+        return MLA_EALIGN;
+    if (a->row_offset && misaligned(a->row_offset, 8)) return MLA_EALIGN;
+    if (!pl->shape.sparse) {
+        if (!a->d_pos) return MLA_EINVAL;
+        if (misaligned(a->d_pos, 4)) return MLA_EALIGN;
+        if (pl->shape.batch > 1 && !a->row_offset) return MLA_EINVAL;
+    } else {
+        if (!a->indices || !a->cache_len || !a->row_offset) return MLA_EINVAL;
+        if (misaligned(a->indices, 4) || misaligned(a->cache_len, 4)) return MLA_EALIGN;
+    }
+    return MLA_OK;
+}
+
+int check_scratch(const mla_decode_plan_t* pl, const void* scratch, size_t bytes) {
+    if (!scratch || misaligned(scratch, kScratchAlign) || bytes < pl->scratch_bytes) return MLA_ESCRATCH;
+    return MLA_OK;
+}
+
+int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return MLA_OK;
+    cudaGetLastError();
+    return MLA_ECUDA;
+}
+
+int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch, size_t bytes, void* stream) {
+    int rc = check_plan(pl);
+    if (rc == MLA_OK) rc = check_args(pl, a);
+    if (rc == MLA_OK) rc = check_scratch(pl, scratch, bytes);
+    if (rc != MLA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = ensure_prepared(st);
+    if (rc != MLA_OK) return rc;
+    char* base = static_cast<char*>(scratch);
+    mla::PartialParams p{};
+    p.q = static_cast<const uint16_t*>(a->q);
+    p.kv = static_cast<const uint16_t*>(a->kv);
+    p.kv_rows = a->kv_rows;
+    p.row_stride = a->row_stride;
+    p.d_pos = a->d_pos;
+    p.row_offset = a->row_offset;
+    p.cache_len = a->cache_len;
+    p.indices = a->indices;
+    p.batch = pl->shape.batch;
+    p.heads = pl->shape.heads;
+    p.topk = pl->shape.topk;
+    p.splits = pl->splits;
+    p.sparse = pl->shape.sparse;
+    p.scale_log2 = pl->shape.scale * 1.4426950408889634f;
+    p.o_part = reinterpret_cast<float*>(base + pl->o_part_offset);
+    p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
+    p.status = reinterpret_cast<int*>(base + pl->status_offset);
+    return launch_status(mla::launch_partial_mma(p, dim3(pl->grid_x, pl->grid_y, pl->grid_z), pl->shape.pdl != 0, st));
+}
+
+int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void* scratch, size_t bytes,
+               void* stream) {
+    int rc = check_plan(pl);
+    if (rc == MLA_OK) rc = check_args(pl, a);
+    if (rc == MLA_OK) rc = check_scratch(pl, scratch, bytes);
+    if (rc != MLA_OK) return rc;
+    const char* base = static_cast<const char*>(scratch);
+    mla::CombineParams c{};
+    c.o_part = reinterpret_cast<const float*>(base + pl->o_part_offset);
+    c.lse_part = reinterpret_cast<const float*>(base + pl->lse_part_offset);
+    c.status = reinterpret_cast<const int*>(base + pl->status_offset);
+    c.out = a->out;
+    c.lse = a->lse;
+    c.batch = pl->shape.batch;
+    c.heads = pl->shape.heads;
+    c.splits = pl->splits;
+    return launch_status(mla::launch_combine(c, dim3(pl->combine_grid_x, pl->combine_grid_y, 1), pl->combine_block,
+                                             pl->shape.pdl != 0, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_abi_version(void) { return MLA_DECODE_ABI_VERSION; }
+
+int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
+    if (!plan) return MLA_EINVAL;
+    int rc = check_shape(shape);
+    if (rc != MLA_OK) return rc;
+    const mla_decode_shape s = *shape;
+    int sms = s.num_sms;
+    if (sms == 0) {
+        int dev = 0;
+        rc = current_device(&dev);
+        if (rc == MLA_OK) rc = device_sm_count(dev, &sms);
+        if (rc == MLA_OK) rc = prepare_device(dev);
+        if (rc != MLA_OK) return rc;
+    }
+    mla_decode_plan_t pl{};
+    pl.shape = s;
+    pl.magic = kPlanMagic;
+    pl.variant = 1;
+    pl.head_group = mla::kHeadGroup;
+    pl.n_head_groups = s.heads / mla::kHeadGroup;
+    pl.ctas_per_sm = kCtasPerSmTarget;
+    pl.num_sms = sms;
+
+    // Split count derived from the shape ("Launch Geometry", Lecture 04, s.4):
+    // enough CTAs for ctas_per_sm per SM, but no slice so short that its
+    // partial write (heads x (512 + 1) fp32) outweighs half its KV bytes.
+    const long long rows = s.sparse ? s.topk : s.max_ctx;
+    const long long partial_bytes = static_cast<long long>(s.heads) * (MLA_D_LATENT + 1) * 4;
+    long long min_rows = ceil_div(kSliceBytesOverPartialBytes * partial_bytes, mla::kRowBytes);
+    min_rows = ceil_div(min_rows, mla::kStageRows) * mla::kStageRows;
+    const long long cap = ceil_div(rows, min_rows);
+    long long S = ceil_div(static_cast<long long>(kCtasPerSmTarget) * sms,
+                           static_cast<long long>(s.batch) * pl.n_head_groups);
+    if (S > cap) S = cap;
+    if (S > MLA_MAX_SPLITS) S = MLA_MAX_SPLITS;
+    if (S < 1) S = 1;
+    if (s.splits_override > 0) S = s.splits_override;
+    pl.splits = static_cast<int>(S);
+    long long per = ceil_div(rows, S);
+    pl.entries_per_split = static_cast<int>(ceil_div(per, mla::kStageRows) * mla::kStageRows);
+
+    pl.grid_x = pl.n_head_groups;
+    pl.grid_y = pl.splits;
+    pl.grid_z = s.batch;
+    pl.block = mla::partial_mma_block_threads();
+    pl.smem_bytes = static_cast<int>(mla::partial_mma_smem_bytes());
+    pl.combine_grid_x = s.batch * s.heads;
+    pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
+    pl.combine_block = 32;
+
+    const size_t bh = static_cast<size_t>(s.batch) * s.heads;
+    pl.status_offset = 0;
+    pl.o_part_offset = kScratchAlign;
+    pl.lse_part_offset = align_up(pl.o_part_offset + bh * pl.splits * MLA_D_LATENT * sizeof(float), kScratchAlign);
+    pl.scratch_bytes = align_up(pl.lse_part_offset + bh * pl.splits * sizeof(float), kScratchAlign);
+    *plan = pl;
+    return MLA_OK;
+}
+
+int mla_decode_run(const mla_decode_plan_t* plan, const mla_decode_args* args, void* scratch, size_t scratch_bytes,
+                   void* stream) {
+    return do_run(plan, args, scratch, scratch_bytes, stream);
+}
+
+int mla_decode_combine(const mla_decode_plan_t* plan, const mla_decode_args* args, const void* scratch,
+                       size_t scratch_bytes, void* stream) {
+    return do_combine(plan, args, scratch, scratch_bytes, stream);
+}
+
+int mla_decode_forward(const mla_decode_plan_t* plan, const mla_decode_args* args, void* scratch,
+                       size_t scratch_bytes, void* stream) {
+    int rc = do_run(plan, args, scratch, scratch_bytes, stream);
+    if (rc != MLA_OK) return rc;
+    return do_combine(plan, args, scratch, scratch_bytes, stream);
+}
+
+int mla_decode_append(void* kv, long long kv_rows, long long row_stride, const void* new_rows, const int* d_pos,
+                      const long long* row_offset, int batch, void* stream) {
+    if (!kv || !new_rows || !d_pos || batch < 1 || kv_rows < 1 || row_stride < MLA_D_ROW) return MLA_EINVAL;
+    if (batch > 1 && !row_offset) return MLA_EINVAL;
+    if (row_stride % 8 != 0 || misaligned(kv, 16) || misaligned(new_rows, 16) || misaligned(d_pos, 4) ||
+        (row_offset && misaligned(row_offset, 8)))
+        return MLA_EALIGN;
+    mla::AppendParams p{};
+    p.kv = static_cast<uint16_t*>(kv);
+    p.kv_rows = kv_rows;
+    p.row_stride = row_stride;
+    p.new_rows = static_cast<const uint16_t*>(new_rows);
+    p.d_pos = d_pos;
+    p.row_offset = row_offset;
+    p.batch = batch;
+    return launch_status(mla::launch_append(p, false, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_advance(int* d_pos, int batch, void* stream) {
+    if (!d_pos || batch < 1) return MLA_EINVAL;
+    if (misaligned(d_pos, 4)) return MLA_EALIGN;
+    return launch_status(mla::launch_advance(d_pos, batch, false, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_scratch_init(void* scratch, size_t scratch_bytes, void* stream) {
+    if (!scratch || scratch_bytes == 0) return MLA_EINVAL;
+    return launch_status(cudaMemsetAsync(scratch, 0, scratch_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+const char* mla_decode_strerror(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_EINVAL: return "invalid argument (null pointer, bad shape, size or plan)";
+        case MLA_EUNSUPPORTED: return "unsupported shape (needs d_latent 512, d_rope 64, heads 16/32/64/128)";
+        case MLA_ESCRATCH: return "scratch missing, not 256-byte aligned, or smaller than plan scratch_bytes";
+        case MLA_EALIGN: return "misaligned pointer or row stride";
+        case MLA_ECUDA: return "CUDA runtime error";
+        case MLA_EDEVICE: return "a kernel wait ran out of time (device status word set)";
+        case MLA_ENOTREADY: return "kernels not prepared on this device; call mla_decode_plan before capture";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// mla_internal.h -- parameters shared between the C-ABI host code and the
+// kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kDLatent = 512;
+constexpr int kDRope = 64;
+constexpr int kDRow = kDLatent + kDRope;       // 576 bf16 per cache row
+constexpr int kRowBytes = kDRow * 2;           // 1152
+constexpr int kStageRows = 32;                 // rows per pipeline stage (partial kernel)
+constexpr int kHeadGroup = 16;                 // heads per CTA of the warp-MMA kernel
+constexpr int kCombineChunk = 128;             // features per combine CTA
+
+// Everything the split partial kernel needs; passed by value.
+struct PartialParams {
+    const uint16_t* q;          // bf16 [B][H][576]
+    const uint16_t* kv;         // bf16 rows
+    long long kv_rows;
+    long long row_stride;       // elements
+    const int* d_pos;           // dense [B]
+    const long long* row_offset;// [B] or null (dense, B == 1)
+    const int* cache_len;       // sparse [B]
+    const int* indices;         // sparse [B][topk]
+    int batch, heads, topk, splits, sparse;
+    float scale_log2;           // scale * log2(e): scores are kept in base-2 units
+    float* o_part;              // [B][H][S][512]
+    float* lse_part;            // [B][H][S]
+    int* status;                // status word
+};
+
+struct CombineParams {
+    const float* o_part;
+    const float* lse_part;
+    const int* status;
+    float* out;                 // [B][H][512]
+    float* lse;                 // [B][H]
+    int batch, heads, splits;
+};
+
+struct AppendParams {
+    uint16_t* kv;
+    long long kv_rows;
+    long long row_stride;
+    const uint16_t* new_rows;   // [B][576]
+    const int* d_pos;
+    const long long* row_offset;
+    int batch;
+};
+
+// Launch helpers (each returns the cudaError_t of the launch).
+cudaError_t partial_mma_prepare(int device);
+size_t partial_mma_smem_bytes();
+int partial_mma_block_threads();
+cudaError_t partial_mma_occupancy(int* ctas_per_sm);
+cudaError_t launch_partial_mma(const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t stream);
+cudaError_t launch_advance(int* d_pos, int batch, bool pdl, cudaStream_t stream);
+
+}  // namespace mla

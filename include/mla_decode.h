@@ -1,0 +1,192 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: split-KV multi-head latent
+ * attention (MLA) decode on one GB300 (sm_103a).
+ *
+ * One query token per request attends over a latent KV cache whose rows are
+ * [c (512 bf16) | k_rope (64 bf16)] = 576 bf16 = 1152 bytes.  For request b
+ * and head h over the attended rows R_b:
+ *
+ *     s_t    = (q_lat[h] . c_t + q_rope[h] . k_rope_t) * scale
+ *     lse    = ln sum_t exp(s_t)                           (natural log)
+ *     out[f] = sum_t exp(s_t - lse) * c_t[f]               (normalised latent)
+ *
+ * Dense : R_b = rows base_b + 0 .. base_b + d_pos[b]; the context bound
+ *         n_ctx = d_pos[b] + 1 is read from device memory by the kernels
+ *         ("Graph-resident decode", Lecture 08, s.2: the MLA kernels read
+ *         *d_pos + 1 as their loop bound, so a captured graph stays valid as
+ *         the position advances).
+ * Sparse: R_b = rows base_b + indices[b][j] for each list entry j with
+ *         0 <= indices[b][j] < cache_len[b] ("The Commit That Changed
+ *         Direction": split-KV sparse MLA decode gathers scattered rows of a
+ *         large cache).  Out-of-range entries are skipped.
+ *
+ * The context (or index list) is cut into `splits` slices; a partial kernel
+ * computes each (head group, slice) online-softmax partial and a separate
+ * combine kernel merges them with a log-sum-exp weighting, slices summed in
+ * ascending order ("Graph-resident decode", Lecture 08, s.6; "Launch
+ * Geometry", Lecture 04, s.8).  The split count and the grid are derived from
+ * the SM count and the context length by mla_decode_plan ("Launch Geometry",
+ * Lecture 04, s.4: derive the slice floor, name the blocks-per-SM target).
+ *
+ * Conventions for every call:
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or synchronises, and keeps no state
+ *     other than a per-device cache of the SM count and of kernel attributes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Launches are
+ *     asynchronous and legal inside stream capture once mla_decode_plan has
+ *     been called on the device (it prepares the kernels; "Graph-resident
+ *     decode", Lecture 08, s.3: pre-warm lazy initialisation before capture).
+ *   - Every call returns an mla_status; arguments are checked on the host
+ *     before anything is launched.  Nothing throws across the ABI.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_DECODE_ABI_VERSION 1
+#define MLA_D_LATENT 512
+#define MLA_D_ROPE 64
+#define MLA_D_ROW 576        /* elements per cache row */
+#define MLA_MAX_SPLITS 128   /* largest split count a plan may hold */
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_EINVAL = -1,        /* null pointer, bad shape, size or plan */
+    MLA_EUNSUPPORTED = -2,  /* shape the kernels do not implement (d_c != 512, d_r != 64, H) */
+    MLA_ESCRATCH = -3,      /* scratch missing, misaligned or smaller than plan->scratch_bytes */
+    MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 */
+    MLA_ECUDA = -5,         /* the CUDA runtime reported an error for a launch or query */
+    MLA_EDEVICE = -6,       /* a kernel's bounded wait ran out (see the scratch status word) */
+    MLA_ENOTREADY = -7      /* kernels not prepared on this device and the stream is capturing */
+} mla_status;
+
+/* Problem description given to the planner. */
+typedef struct {
+    int batch;            /* B >= 1 requests, one query token each */
+    int heads;            /* H in {16, 32, 64, 128} */
+    int d_latent;         /* must be 512 */
+    int d_rope;           /* must be 64 */
+    int sparse;           /* 0 = dense context, 1 = top-k index gather */
+    int max_ctx;          /* dense: largest n_ctx = d_pos + 1 any request reaches (>= 1) */
+    int topk;             /* sparse: index-list length per request (>= 1) */
+    float scale;          /* softmax scale, finite and > 0 (1/sqrt(576) for these shapes) */
+    int num_sms;          /* SMs to plan for; 0 = query the current device */
+    int splits_override;  /* 0 = derive; 1..MLA_MAX_SPLITS = force this split count */
+    int variant;          /* 0 = auto; 1 = head-group-16 warp-MMA kernel */
+    int pdl;              /* 1 = launch with programmatic dependent launch */
+} mla_decode_shape;
+
+/* Launch plan (plain data; copy freely).  The plan is the capture key of a
+ * graph: a graph stays valid as long as the plan it was captured with does
+ * ("Graph-resident decode", Lecture 08, s.2: splits sizes the grid, so it is
+ * decided on the host by the same function the launcher uses). */
+typedef struct {
+    mla_decode_shape shape;
+    int magic;                 /* set by mla_decode_plan; checked by every launch */
+    int variant;               /* kernel chosen */
+    int splits;                /* S: slices per (request, head group) */
+    int entries_per_split;     /* rows (dense) or list entries (sparse) per slice at max_ctx / topk */
+    int head_group;            /* heads per CTA */
+    int n_head_groups;         /* H / head_group */
+    int ctas_per_sm;           /* resident-CTA target the split count aims at */
+    int num_sms;               /* SM count planned for */
+    int grid_x, grid_y, grid_z, block, smem_bytes;          /* partial kernel launch */
+    int combine_grid_x, combine_grid_y, combine_block;      /* combine kernel launch */
+    size_t scratch_bytes;      /* bytes of caller scratch needed by run + combine */
+    size_t o_part_offset;      /* fp32 [B][H][S][512] normalised slice outputs */
+    size_t lse_part_offset;    /* fp32 [B][H][S] slice log-sum-exp (-inf for an empty slice) */
+    size_t status_offset;      /* int32 status word: 0 healthy, else an mla_status */
+} mla_decode_plan_t;
+
+/* Per-call tensors. */
+typedef struct {
+    const void *q;               /* (device) bf16 [B][H][576] = [q_lat | q_rope], 16-byte aligned */
+    const void *kv;              /* (device) bf16 cache rows, row r at kv + r * row_stride, 16-byte aligned */
+    long long kv_rows;           /* rows addressable in kv (bounds for every row the kernels read) */
+    long long row_stride;        /* elements between rows: >= 576 and a multiple of 8 */
+    const int *d_pos;            /* (device) dense: int32 [B]; n_ctx of request b = d_pos[b] + 1 */
+    const long long *row_offset; /* (device) int64 [B]: first row of request b's segment;
+                                    may be NULL for a dense batch of 1 (segment starts at row 0) */
+    const int *cache_len;        /* (device) sparse: int32 [B] rows in request b's segment */
+    const int *indices;          /* (device) sparse: int32 [B][topk] request-local row ids */
+    float *out;                  /* (device) fp32 [B][H][512], 16-byte aligned */
+    float *lse;                  /* (device) fp32 [B][H], natural log; -inf if no row is attended */
+} mla_decode_args;
+
+/* Version of this ABI (MLA_DECODE_ABI_VERSION). */
+MLA_API int mla_decode_abi_version(void);
+
+/* Plan a decode: validates the shape, derives the split count
+ *   S = clamp(ceil(ctas_per_sm * num_sms / (B * n_head_groups)), 1,
+ *             min(MLA_MAX_SPLITS, ceil(rows / min_rows)))
+ * where min_rows keeps each slice's KV bytes at least twice the bytes of the
+ * partials it writes, rounded up to the kernel's 32-row stage, and fills the
+ * launch geometry and scratch layout.  With num_sms == 0 it queries the
+ * current device and prepares the kernels there (call it before capturing a
+ * graph).  Host only; the plan does not depend on any device pointer.
+ * ("Launch Geometry", Lecture 04, s.1 and s.4; "Graph-resident decode",
+ * Lecture 08, s.2.)  Errors: MLA_EINVAL (null or bad field),
+ * MLA_EUNSUPPORTED (shape), MLA_ECUDA (device query failed). */
+MLA_API int mla_decode_plan(const mla_decode_shape *shape, mla_decode_plan_t *plan);
+
+/* Launch the split partial kernel: each CTA computes one (request, head group,
+ * slice) online-softmax partial into scratch (o_part normalised, lse_part).
+ * `scratch` (device) must be 256-byte aligned and at least
+ * plan->scratch_bytes long; the caller zeroes it once before first use (see
+ * mla_decode_scratch_init) and must not reuse it for an overlapping call.
+ * Errors: MLA_EINVAL, MLA_EALIGN, MLA_ESCRATCH, MLA_ENOTREADY, MLA_ECUDA. */
+MLA_API int mla_decode_run(const mla_decode_plan_t *plan, const mla_decode_args *args, void *scratch,
+                   size_t scratch_bytes, void *stream);
+
+/* Launch the log-sum-exp combine: M = max_s lse_s, lse = M + ln sum_s
+ * exp(lse_s - M), out = sum_s exp(lse_s - lse) * o_s with s ascending, for
+ * every (request, head), over a (B*H, 512/128) grid ("Graph-resident decode",
+ * Lecture 08, s.6: a merge grid wider than n_head, no serial prologue).
+ * Must follow mla_decode_run on the same stream with the same plan and
+ * scratch.  Errors as mla_decode_run. */
+MLA_API int mla_decode_combine(const mla_decode_plan_t *plan, const mla_decode_args *args, const void *scratch,
+                       size_t scratch_bytes, void *stream);
+
+/* mla_decode_run followed by mla_decode_combine (two launches). */
+MLA_API int mla_decode_forward(const mla_decode_plan_t *plan, const mla_decode_args *args, void *scratch,
+                       size_t scratch_bytes, void *stream);
+
+/* Write the new token's cache row from device memory: for each request b,
+ * copy new_rows[b] (bf16 [576]) to row base_b + d_pos[b] of kv, where base_b
+ * = row_offset[b] (row_offset may be NULL for batch 1).  The destination is
+ * computed on the device so a captured graph writes a new row on every replay
+ * ("Graph-resident decode", Lecture 08, s.2: the K-cache row write derives
+ * the row from a device-resident d_pos and moves the same bytes).  Rows
+ * outside [0, kv_rows) are not written.  kv and new_rows 16-byte aligned.
+ * Errors: MLA_EINVAL, MLA_EALIGN, MLA_ECUDA. */
+MLA_API int mla_decode_append(void *kv, long long kv_rows, long long row_stride, const void *new_rows,
+                      const int *d_pos, const long long *row_offset, int batch, void *stream);
+
+/* d_pos[b] += 1 for b < batch, on the device ("Graph-resident decode",
+ * Lecture 08, s.2: the position increment runs inside the captured region).
+ * Errors: MLA_EINVAL, MLA_ECUDA. */
+MLA_API int mla_decode_advance(int *d_pos, int batch, void *stream);
+
+/* Zero the scratch region (async memset on `stream`), clearing the status
+ * word.  Errors: MLA_EINVAL, MLA_ECUDA. */
+MLA_API int mla_decode_scratch_init(void *scratch, size_t scratch_bytes, void *stream);
+
+/* Static description of a status code. */
+MLA_API const char *mla_decode_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

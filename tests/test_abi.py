@@ -1,0 +1,189 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+declared symbol, plans deterministically, and rejects bad arguments before any
+CUDA call (every case here fails validation, so nothing is launched)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import decode_attention_mla_gb300 as mla
+from decode_attention_mla_gb300 import build as mla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SCALE = 1.0 / math.sqrt(576)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mla_build.build()
+    yield
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_symbols()
+    assert names, "no declarations found"
+    assert set(mla.EXPORTED) <= names
+    L = ctypes.CDLL(mla.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared but not exported"
+    assert mla.abi_version() == 1
+    assert "scratch" in mla.strerror(mla.ESCRATCH)
+
+
+def _plan(**kw):
+    base = dict(batch=1, heads=16, scale=SCALE, num_sms=152)
+    base.update(kw)
+    return mla.plan(**base)
+
+
+@pytest.mark.parametrize("kw,splits,entries", [
+    (dict(max_ctx=256), 4, 64),
+    (dict(max_ctx=8192), 128, 64),
+    (dict(sparse=True, topk=2048), 32, 64),
+    (dict(batch=64, sparse=True, topk=2048), 5, 416),
+    (dict(heads=128, max_ctx=32768 + 64), 38, 864),
+])
+def test_plan_derivation_for_the_workloads(kw, splits, entries):
+    p = _plan(**kw)
+    assert (p.splits, p.entries_per_split) == (splits, entries)
+    rows = kw.get("topk") or kw.get("max_ctx")
+    assert p.splits * p.entries_per_split >= rows
+    assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
+    assert p.grid_x == p.n_head_groups == kw.get("heads", 16) // 16
+    assert p.grid_y == p.splits and p.grid_z == kw.get("batch", 1)
+    assert p.combine_grid_x == kw.get("batch", 1) * kw.get("heads", 16) and p.combine_grid_y == 4
+    # scratch layout: status word, then o_part, then lse_part, 256-byte aligned
+    bh = kw.get("batch", 1) * kw.get("heads", 16)
+    assert p.status_offset == 0 and p.o_part_offset % 256 == 0 and p.lse_part_offset % 256 == 0
+    assert p.lse_part_offset >= p.o_part_offset + bh * p.splits * 512 * 4
+    assert p.scratch_bytes >= p.lse_part_offset + bh * p.splits * 4 and p.scratch_bytes % 256 == 0
+
+
+def test_plan_scales_with_sm_count_and_is_deterministic():
+    a = _plan(max_ctx=131072, num_sms=132)
+    b = _plan(max_ctx=131072, num_sms=132)
+    assert a.as_dict() == b.as_dict()
+    assert a.splits == 128                     # capped by MLA_MAX_SPLITS
+    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == 66   # ceil(2*132/4)
+    assert _plan(max_ctx=131072, batch=4, num_sms=160).splits == 80
+    # the floor, not the SM count, binds for short contexts
+    assert _plan(max_ctx=100, num_sms=152).splits == 2
+
+
+def test_plan_override():
+    for s in (1, 2, 7, 64, 128):
+        p = _plan(max_ctx=8192, splits=s)
+        assert p.splits == s and p.grid_y == s
+        assert p.entries_per_split == -(-(-(-8192 // s)) // 32) * 32
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(heads=8, max_ctx=16), mla.EUNSUPPORTED),
+    (dict(heads=48, max_ctx=16), mla.EUNSUPPORTED),
+    (dict(batch=0, max_ctx=16), mla.EINVAL),
+    (dict(max_ctx=0), mla.EINVAL),
+    (dict(sparse=True, topk=0), mla.EINVAL),
+    (dict(max_ctx=16, scale=0.0), mla.EINVAL),
+    (dict(max_ctx=16, scale=float("nan")), mla.EINVAL),
+    (dict(max_ctx=16, scale=float("inf")), mla.EINVAL),
+    (dict(max_ctx=16, splits=129), mla.EINVAL),
+    (dict(max_ctx=16, splits=-1), mla.EINVAL),
+    (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
+    (dict(max_ctx=16, variant=7), mla.EINVAL),
+])
+def test_plan_rejects(kw, status):
+    with pytest.raises(mla.MLADecodeError) as e:
+        _plan(**kw)
+    assert e.value.status == status
+
+
+def test_plan_rejects_bad_dims():
+    L = mla.lib()
+    s = mla.Shape(batch=1, heads=16, d_latent=256, d_rope=64, sparse=0, max_ctx=16, topk=0, scale=SCALE,
+                  num_sms=152, splits_override=0, variant=0, pdl=0)
+    p = mla.Plan()
+    assert L.mla_decode_plan(ctypes.byref(s), ctypes.byref(p)) == mla.EUNSUPPORTED
+    s.d_latent, s.d_rope = 512, 32
+    assert L.mla_decode_plan(ctypes.byref(s), ctypes.byref(p)) == mla.EUNSUPPORTED
+    assert L.mla_decode_plan(None, ctypes.byref(p)) == mla.EINVAL
+    assert L.mla_decode_plan(ctypes.byref(s), None) == mla.EINVAL
+
+
+def _args(**kw):
+    base = dict(q=0x10000, kv=0x20000, kv_rows=100, row_stride=576, d_pos=0x30000, row_offset=None,
+                cache_len=None, indices=None, out=0x40000, lse=0x50000)
+    base.update(kw)
+    return mla.Args(**base)
+
+
+def _call(fn, p, a, scratch=0x100000, nbytes=None):
+    L = mla.lib()
+    nbytes = (p.scratch_bytes if p is not None else 1 << 20) if nbytes is None else nbytes
+    return getattr(L, fn)(ctypes.byref(p) if p is not None else None, ctypes.byref(a) if a is not None else None,
+                          ctypes.c_void_p(scratch) if scratch else None, nbytes, None)
+
+
+@pytest.mark.parametrize("fn", ["mla_decode_run", "mla_decode_combine", "mla_decode_forward"])
+def test_launch_argument_checks(fn):
+    p = _plan(max_ctx=64)
+    assert _call(fn, None, _args()) == mla.EINVAL
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.magic = 0
+    assert _call(fn, bad, _args()) == mla.EINVAL
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.splits = 0
+    assert _call(fn, bad, _args()) == mla.EINVAL
+    assert _call(fn, p, None) == mla.EINVAL
+    assert _call(fn, p, _args(q=None)) == mla.EINVAL
+    assert _call(fn, p, _args(kv=None)) == mla.EINVAL
+    assert _call(fn, p, _args(out=None)) == mla.EINVAL
+    assert _call(fn, p, _args(lse=None)) == mla.EINVAL
+    assert _call(fn, p, _args(d_pos=None)) == mla.EINVAL
+    assert _call(fn, p, _args(kv_rows=0)) == mla.EINVAL
+    assert _call(fn, p, _args(row_stride=512)) == mla.EINVAL
+    assert _call(fn, p, _args(row_stride=580)) == mla.EALIGN
+    assert _call(fn, p, _args(q=0x10002)) == mla.EALIGN
+    assert _call(fn, p, _args(kv=0x20008)) == mla.EALIGN
+    assert _call(fn, p, _args(out=0x40004)) == mla.EALIGN
+    assert _call(fn, p, _args(lse=0x50002)) == mla.EALIGN
+    assert _call(fn, p, _args(d_pos=0x30002)) == mla.EALIGN
+    assert _call(fn, p, _args(row_offset=0x60004)) == mla.EALIGN
+    # scratch checks come after the argument checks and still before any launch
+    assert _call(fn, p, _args(), scratch=0) == mla.ESCRATCH
+    assert _call(fn, p, _args(), scratch=0x100080) == mla.ESCRATCH
+    assert _call(fn, p, _args(), nbytes=p.scratch_bytes - 1) == mla.ESCRATCH
+    # dense batches > 1 need row offsets; sparse needs indices, lengths and offsets
+    p2 = _plan(max_ctx=64, batch=2)
+    assert _call(fn, p2, _args()) == mla.EINVAL
+    ps = _plan(sparse=True, topk=64)
+    assert _call(fn, ps, _args()) == mla.EINVAL
+    assert _call(fn, ps, _args(indices=0x70000, cache_len=0x71000)) == mla.EINVAL
+    assert _call(fn, ps, _args(indices=0x70002, cache_len=0x71000, row_offset=0x72000)) == mla.EALIGN
+
+
+def test_append_advance_argument_checks():
+    L = mla.lib()
+    assert L.mla_decode_append(None, 10, 576, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), None, 1, None) == mla.EINVAL
+    assert L.mla_decode_append(ctypes.c_void_p(0x1000), 0, 576, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000),
+                               None, 1, None) == mla.EINVAL
+    assert L.mla_decode_append(ctypes.c_void_p(0x1000), 10, 576, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000),
+                               None, 2, None) == mla.EINVAL
+    assert L.mla_decode_append(ctypes.c_void_p(0x1008), 10, 576, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000),
+                               None, 1, None) == mla.EALIGN
+    assert L.mla_decode_append(ctypes.c_void_p(0x1000), 10, 578, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000),
+                               None, 1, None) == mla.EALIGN
+    assert L.mla_decode_advance(None, 1, None) == mla.EINVAL
+    assert L.mla_decode_advance(ctypes.c_void_p(0x1000), 0, None) == mla.EINVAL
+    assert L.mla_decode_advance(ctypes.c_void_p(0x1002), 1, None) == mla.EALIGN
+    assert L.mla_decode_scratch_init(None, 16, None) == mla.EINVAL

@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Bar: max|out - oracle| <= 2e-3 and relative LSE error
+<= 1e-4; byte identity across runs at a fixed split count."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import decode_attention_mla_gb300 as mla
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from __graft_entry__ import build
+    build()
+    torch.cuda.set_device(0)
+    yield
+
+
+# ---- dense, small shapes: several stages, ragged tails, many split counts ----
+@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 100, 256, 1000, 2049])
+@pytest.mark.parametrize("splits", [0, 1, 3, 8])
+def test_dense_small(T, splits):
+    x = workloads.dense(1, 16, T, seed=T)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=splits)
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"dense T={T} S={plan.splits}")
+    assert mla.status_word(plan, scratch) == 0
+
+
+def test_dense_t256_workload():
+    x = workloads.make("dense_t256")
+    out, lse, plan, _ = _gpu.run_dense(x)
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, "dense_t256")
+
+
+def test_dense_t8192_split_sweep():
+    x = workloads.make("dense_t8192")
+    ro, rl = _gpu.oracle_dense(x)
+    results = {}
+    for s in (1, 2, 4, 8, 16, 32, 64, 128, 0):
+        out, lse, plan, _ = _gpu.run_dense(x, splits=s)
+        _gpu.assert_parity(out, lse, ro, rl, f"dense_t8192 S={plan.splits}")
+        results[plan.splits] = (out.double().cpu().numpy(), lse.double().cpu().numpy())
+    keys = sorted(results)
+    for a in keys:
+        for b in keys:
+            assert np.abs(results[a][0] - results[b][0]).max() <= 2 * _gpu.OUT_ATOL
+            assert (np.abs(results[a][1] - results[b][1]) / np.maximum(np.abs(rl), 1)).max() <= 2 * _gpu.LSE_RTOL
+
+
+def test_dense_partials_match_oracle_split_emulation():
+    """The partial kernel's scratch (o_s, lse_s) against the oracle's fp64 emulation
+    of the same slices (32-row granule, as the plan cuts them)."""
+    x = workloads.dense(1, 16, 1000, seed=3)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=5)
+    S = plan.splits
+    _, _, op, lp = oracle.decode_split(x.q, x.kv, scale=x.scale, splits=S, granule=32, d_pos=x.d_pos,
+                                       return_partials=True)
+    o_off, l_off = plan.o_part_offset, plan.lse_part_offset
+    o_gpu = scratch[o_off:o_off + 16 * S * 512 * 4].view(torch.float32).view(1, 16, S, 512).double().cpu().numpy()
+    l_gpu = scratch[l_off:l_off + 16 * S * 4].view(torch.float32).view(1, 16, S).double().cpu().numpy()
+    assert np.abs(o_gpu - op).max() <= _gpu.OUT_ATOL
+    fin = np.isfinite(lp)
+    assert np.array_equal(np.isfinite(l_gpu), fin)
+    assert (np.abs(l_gpu[fin] - lp[fin]) / np.maximum(np.abs(lp[fin]), 1)).max() <= _gpu.LSE_RTOL
+
+
+def test_dense_batch_ragged():
+    B, H, cap = 3, 16, 1500
+    x = workloads.dense(B, H, cap, seed=21)
+    x.d_pos = torch.tensor([1499, 17, 640], dtype=torch.int32)
+    out, lse, plan, _ = _gpu.run_dense(x, max_ctx=cap)
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, "dense batch 3 ragged")
+
+
+@pytest.mark.parametrize("H", [32, 64, 128])
+def test_dense_more_heads(H):
+    x = workloads.dense(1, H, 2000, seed=H)
+    out, lse, plan, _ = _gpu.run_dense(x)
+    assert plan.n_head_groups == H // 16
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"dense H={H}")
+
+
+def test_dense_row_stride_and_capacity():
+    """Rows padded to a 640-element stride; d_pos beyond the cache is clamped."""
+    T = 700
+    x = workloads.dense(1, 16, T, seed=5)
+    d = _gpu.dev()
+    padded = torch.zeros(T, 640, dtype=torch.bfloat16)
+    padded[:, :576] = x.kv
+    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale)
+    scratch = mla.alloc_scratch(plan)
+    out = torch.empty(1, 16, 512, device=d)
+    lse = torch.empty(1, 16, device=d)
+    mla.forward(plan, x.q.to(d), padded.to(d), out, lse, scratch, d_pos=x.d_pos.to(d))
+    torch.cuda.synchronize()
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, "row stride 640")
+    # d_pos past the last row: only the rows that exist are attended
+    big = torch.tensor([T + 50], dtype=torch.int32)
+    mla.forward(plan, x.q.to(d), x.kv.to(d), out, lse, scratch, d_pos=big.to(d))
+    torch.cuda.synchronize()
+    _gpu.assert_parity(out, lse, ro, rl, "d_pos clamped to the cache")
+
+
+def test_uniform_scores_closed_form():
+    """q = 0: every score is 0, so out = mean of the attended latent rows and lse = ln n."""
+    T = 777
+    x = workloads.dense(1, 16, T, seed=9)
+    x.q = torch.zeros_like(x.q)
+    out, lse, _, _ = _gpu.run_dense(x, splits=6)
+    mean = x.kv[:, :512].double().mean(0).numpy()
+    assert np.abs(out.double().cpu().numpy() - mean[None, None]).max() <= _gpu.OUT_ATOL
+    assert np.abs(lse.double().cpu().numpy() - math.log(T)).max() <= _gpu.LSE_RTOL * math.log(T)
+
+
+# ---- sparse ------------------------------------------------------------------
+def test_sparse_k2048_workload():
+    x = workloads.make("sparse_k2048")
+    ro, rl = _gpu.oracle_sparse(x)
+    for s in (0, 1, 7, 64):
+        out, lse, plan, _ = _gpu.run_sparse(x, splits=s)
+        _gpu.assert_parity(out, lse, ro, rl, f"sparse_k2048 S={plan.splits}")
+
+
+@pytest.mark.parametrize("topk", [1, 17, 64, 300])
+def test_sparse_small(topk):
+    x = workloads.sparse(2, 16, [5000, 300], topk, seed=topk)
+    out, lse, plan, _ = _gpu.run_sparse(x)
+    ro, rl = _gpu.oracle_sparse(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"sparse k={topk}")
+
+
+def test_sparse_masking_out_of_range_ids():
+    x = workloads.sparse(2, 16, [4000, 900], 256, seed=31)
+    idx = x.indices.clone()
+    idx[0, 3] = -1
+    idx[0, 100] = 4000          # == cache_len: masked
+    idx[1, 0] = 900
+    idx[1, 7] = 2 ** 31 - 1
+    idx[1, 255] = -(2 ** 31)
+    x.indices = idx
+    out, lse, plan, _ = _gpu.run_sparse(x, splits=3)
+    ro, rl = _gpu.oracle_sparse(x)
+    _gpu.assert_parity(out, lse, ro, rl, "sparse masked ids")
+
+
+def test_sparse_all_masked_is_empty():
+    x = workloads.sparse(1, 16, 100, 40, seed=32)
+    x.indices = torch.full_like(x.indices, -7)
+    out, lse, _, _ = _gpu.run_sparse(x, splits=2)
+    assert torch.isneginf(lse).all()
+    assert (out == 0).all()
+
+
+def test_sparse_equals_dense_on_permutation():
+    T = 3000
+    xd = workloads.dense(1, 16, T, seed=33)
+    perm = workloads.unique_indices(T, T, seed=33, stream=9).view(1, -1)
+    xs = workloads.SparseInputs(q=xd.q, kv=xd.kv, indices=perm, cache_len=torch.tensor([T], dtype=torch.int32),
+                                row_offset=torch.tensor([0], dtype=torch.int64))
+    od, ld, _, _ = _gpu.run_dense(xd)
+    os_, ls, _, _ = _gpu.run_sparse(xs)
+    assert (od - os_).abs().max().item() <= 2 * _gpu.OUT_ATOL
+    assert ((ld - ls).abs() / ld.abs().clamp(min=1)).max().item() <= 2 * _gpu.LSE_RTOL
+
+
+def test_sparse_b64_workload_sampled():
+    """Full-size ragged batch (~5 GB cache) on the GPU; the oracle checks a sample of requests."""
+    x = workloads.make("sparse_b64")
+    d = _gpu.dev()
+    kv_dev = x.kv.to(d)
+    out, lse, plan, scratch = _gpu.run_sparse(x, kv_dev=kv_dev)
+    assert mla.status_word(plan, scratch) == 0
+    sample = [0, 1, 17, 31, 42, 63]
+    sub = workloads.SparseInputs(q=x.q[sample], kv=x.kv, indices=x.indices[sample], cache_len=x.cache_len[sample],
+                                 row_offset=x.row_offset[sample])
+    ro, rl = _gpu.oracle_sparse(sub)
+    _gpu.assert_parity(out[sample], lse[sample], ro, rl, "sparse_b64 sample")
+    del kv_dev
+
+
+# ---- determinism, A/A, PDL, guards -------------------------------------------
+def test_fixed_split_is_bit_identical_across_runs():
+    x = workloads.dense(1, 16, 8192, seed=41)
+    ref = None
+    for _ in range(10):
+        out, lse, plan, _ = _gpu.run_dense(x, splits=32)
+        cur = (_gpu.bits(out).clone(), _gpu.bits(lse).clone())
+        if ref is None:
+            ref = cur
+        else:
+            assert torch.equal(cur[0], ref[0]) and torch.equal(cur[1], ref[1])
+
+
+def test_aa_control_sparse():
+    """Two independent runs of the same arm (fresh scratch each) must match byte for byte."""
+    x = workloads.sparse(4, 16, [9000, 7000, 12000, 4096], 512, seed=42)
+    a = _gpu.run_sparse(x, splits=4)
+    b = _gpu.run_sparse(x, splits=4)
+    assert torch.equal(_gpu.bits(a[0]), _gpu.bits(b[0])) and torch.equal(_gpu.bits(a[1]), _gpu.bits(b[1]))
+
+
+def test_pdl_on_off_bit_identical():
+    x = workloads.dense(1, 16, 4096, seed=43)
+    a = _gpu.run_dense(x, splits=16, pdl=False)
+    b = _gpu.run_dense(x, splits=16, pdl=True)
+    assert torch.equal(_gpu.bits(a[0]), _gpu.bits(b[0])) and torch.equal(_gpu.bits(a[1]), _gpu.bits(b[1]))
+
+
+def test_guard_regions_untouched():
+    """out, lse and scratch live inside larger buffers; the bytes around them must not change."""
+    x = workloads.dense(1, 16, 2000, seed=44)
+    d = _gpu.dev()
+    plan = mla.plan(batch=1, heads=16, max_ctx=2000, scale=x.scale, splits=9)
+    G = 1024
+    sbuf = torch.full((plan.scratch_bytes + 2 * G * 4,), 0xA5, dtype=torch.uint8, device=d)
+    scratch = sbuf[G * 4:G * 4 + plan.scratch_bytes]
+    mla.scratch_init(scratch)
+    obuf = torch.full((16 * 512 + 2 * G,), 7.0, device=d)
+    lbuf = torch.full((16 + 2 * G,), 7.0, device=d)
+    out = obuf[G:G + 16 * 512].view(1, 16, 512)
+    lse = lbuf[G:G + 16].view(1, 16)
+    mla.forward(plan, x.q.to(d), x.kv.to(d), out, lse, scratch, d_pos=x.d_pos.to(d))
+    torch.cuda.synchronize()
+    assert (sbuf[:G * 4] == 0xA5).all() and (sbuf[G * 4 + plan.scratch_bytes:] == 0xA5).all()
+    assert (obuf[:G] == 7.0).all() and (obuf[G + 16 * 512:] == 7.0).all()
+    assert (lbuf[:G] == 7.0).all() and (lbuf[G + 16:] == 7.0).all()
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, "guarded buffers")
+
+
+def test_plan_on_device_matches_occupancy_target():
+    p = mla.plan(batch=1, heads=16, max_ctx=8192, scale=workloads.SCALE)
+    assert p.num_sms == torch.cuda.get_device_properties(0).multi_processor_count
+    assert p.ctas_per_sm == 2

@@ -204,6 +204,47 @@ class SparseBench:
         self.mla.run(self.plan, self.args[c], self.scratch, stream)
 
 
+class GraphBench:
+    """Multi-step dense decode, H=128, start context T0, `steps` steps per graph.
+    `layers` distinct caches (as the layers of a model) share one d_pos: each
+    step appends a row to every layer's cache, runs partial + combine per layer,
+    then advances d_pos once.  The layers together exceed 3x L2."""
+
+    def __init__(self, H, T0, steps, layers, splits, pdl, seed=0):
+        import decode_attention_mla_gb300 as mla
+        self.mla = mla
+        d = torch.device("cuda")
+        g = workloads.graph(H, T0, steps, seed=seed)
+        self.g, self.H, self.T0, self.steps, self.copies = g, H, T0, steps, layers
+        base = g.kv.to(d)
+        self.kv = [base] + [torch.roll(base, shifts=c * 37, dims=0) for c in range(1, layers)]
+        self.kv_init = [k.clone() for k in self.kv] if layers * base.numel() * 2 < (8 << 30) else None
+        rows = g.new_rows.to(d)
+        self.new_rows = [rows] + [torch.roll(rows, shifts=c, dims=0) for c in range(1, layers)]
+        self.q = g.q_steps.to(d)
+        self.d_pos = torch.tensor([T0], dtype=torch.int32, device=d)
+        self.d_pos0 = self.d_pos.clone()
+        self.out = [torch.empty(steps, 1, H, 512, device=d) for _ in range(layers)]
+        self.lse = [torch.empty(steps, 1, H, device=d) for _ in range(layers)]
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=T0 + steps, scale=g.scale, splits=splits, pdl=pdl)
+        self.scratch = mla.alloc_scratch(self.plan)
+        self.args = [[mla.make_args(self.q[k], self.kv[l], self.out[l][k], self.lse[l][k], d_pos=self.d_pos)
+                      for k in range(steps)] for l in range(layers)]
+        mean_rows = T0 + 1 + (steps - 1) / 2.0
+        self.alg_bytes = mean_rows * ROW_BYTES + H * 576 * 2 + H * 512 * 4 + H * 4 + 2 * ROW_BYTES + 8
+        self.flops = mean_rows * H * FLOP_PER_ROW_HEAD
+        self.calls = steps * layers
+
+    def loop(self, _c=0, stream=None):
+        mla = self.mla
+        self.d_pos.copy_(self.d_pos0)
+        for k in range(self.steps):
+            for l in range(self.copies):
+                mla.append(self.kv[l], self.new_rows[l][k], self.d_pos)
+                mla.forward_args(self.plan, self.args[l][k], self.scratch)
+            mla.advance(self.d_pos)
+
+
 def capture(fn, n):
     """CUDA graph of fn(0..n-1) on a side stream (warmed up eagerly first)."""
     s = torch.cuda.Stream()
@@ -430,6 +471,14 @@ def time_bench(bench, reps=200, warm=5):
     return us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list]
 
 
+def time_graph_bench(gb, reps=10, warm=3):
+    g = capture(gb.loop, 1)
+    el = time_graph(g, reps, warm)
+    rep_list = per_rep_times(g, 5)
+    us = el / (reps * gb.calls) * 1e6
+    return us, None, [r / gb.calls * 1e6 for r in rep_list]
+
+
 def write_details(args, P):
     rows = []
 
@@ -465,8 +514,34 @@ def write_details(args, P):
     entry("sparse_b64", b, us, usp, reps)
     del b
     torch.cuda.empty_cache()
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, bool(args.pdl))
+    us, _, reps = time_graph_bench(gb)
+    tensor_us = gb.flops / (P["bf16_tflops_sustained"] * 1e12) * 1e6
+    entry("graph_h128", gb, us, None, reps,
+          {"per": "decode step per layer", "layers": gb.copies,
+           "roofline_us_hbm": gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, "roofline_us_tensor": tensor_us,
+           "frac_roofline": max(gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, tensor_us) / us})
+    del gb
+    torch.cuda.empty_cache()
     with open(args.details, "w") as f:
         json.dump({"peaks": P, "rows": rows}, f, indent=1)
+
+
+def ncu_case(args):
+    """A few eager calls on distinct caches (together larger than L2), for ncu."""
+    from decode_attention_mla_gb300 import build as mla_build
+    mla_build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    if args.ncu_case == "dense_t8192":
+        b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), args.splits, bool(args.pdl))
+    elif args.ncu_case == "sparse_k2048":
+        b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl))
+    else:
+        b = SparseBench("sparse_b64", 1, args.splits, bool(args.pdl))
+    for c in range(args.calls):
+        b.call(c % b.copies)
+    torch.cuda.synchronize()
+    log(f"ncu case {args.ncu_case}: {args.calls} calls, splits {b.plan.splits}, copies {b.copies}")
 
 
 def main():
@@ -480,8 +555,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--details", default=None)
+    ap.add_argument("--ncu-case", default=None, choices=["dense_t8192", "sparse_k2048", "sparse_b64"],
+                    help="profiling helper: run --calls eager calls of one workload and exit (no JSON)")
+    ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.ncu_case:
+        ncu_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -125,5 +125,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits), .y = hi
     return *reinterpret_cast<uint32_t*>(&v);
 }
+// (a, b) -> bf16x2 hi = RN(a), RN(b) and bf16x2 lo = RN(a - hi_a), RN(b - hi_b):
+// hi + lo carries ~16 significant bits (the differences are exact in fp32).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float ra = a - __bfloat162float(h.x);
+    const float rb = b - __bfloat162float(h.y);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 
 }  // namespace mla

@@ -1,15 +1,17 @@
 // mla_combine.cu -- log-sum-exp merge of the split partials.
 //
 // For every (request, head):  M = max_s lse_s,  lse = M + ln sum_s exp(lse_s - M),
-// out = sum_s exp(lse_s - lse) * o_s, slices added in ascending order
+// out = sum_s exp(lse_s - lse) * o_s
 // ("Graph-resident decode", Lecture 08, s.6: the merge is its own kernel with
-// a grid wider than n_head, the slice sum runs in ascending slice order and
-// there is no serial thread-0 prologue; here every lane of the warp computes
-// the weights of its own slices and a fixed butterfly forms the normaliser).
+// a grid wider than n_head and no serial thread-0 prologue).
 //
-// Grid (B*H, 512/128), one warp per CTA; each lane owns 4 consecutive output
-// features (float4 loads of the partials, which stay in L2 between the two
-// kernels).  An all-empty row set gives lse = -inf and out = 0.
+// Grid (B*H, 512/128): a CTA merges 128 output features of one (request,
+// head).  Its 8 warps take contiguous runs of slices; each lane owns 4
+// consecutive features and first loads all of its run's partials into
+// registers, so those loads are in flight together with the lse loads.  Each
+// warp adds its run in ascending slice order and the 8 run sums are added in
+// warp order: a fixed association, so the result is reproducible bit for bit.
+// An all-empty row set gives lse = -inf and out = 0.
 #include <cmath>
 
 #include "device_utils.cuh"
@@ -19,48 +21,91 @@
 namespace mla {
 namespace {
 
-__global__ void __launch_bounds__(32) mla_combine_kernel(const CombineParams p) {
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxRun = (MLA_MAX_SPLITS + kWarps - 1) / kWarps;   // slices per warp at most
+static_assert(MLA_MAX_SPLITS <= kThreads, "one lse per thread");
+
+__global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombineParams p) {
     __shared__ float weight[MLA_MAX_SPLITS];
+    __shared__ float red_max[kWarps];
+    __shared__ float red_sum[kWarps];
+    __shared__ float4 part[kWarps][32];
     grid_dependency_wait();          // the partials come from the preceding kernel
     allow_dependent_launch();
     const int bh = blockIdx.x;
     const int chunk = blockIdx.y;
-    const int lane = threadIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int S = p.splits;
-    const float* lp = p.lse_part + static_cast<long long>(bh) * S;
+    const int run = (S + kWarps - 1) / kWarps;
+    const int s0 = warp * run;
+    const int s1 = min(S, s0 + run);
 
-    float mx = -INFINITY;
-    for (int i = lane; i < S; i += 32) mx = fmaxf(mx, lp[i]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-
-    float sum = 0.f;
-    if (mx != -INFINITY) {
-        for (int i = lane; i < S; i += 32) sum += expf(lp[i] - mx);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float total = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-    for (int i = lane; i < S; i += 32) weight[i] = (mx == -INFINITY) ? 0.f : expf(lp[i] - total);
-    __syncwarp();
-
+    // partials of this warp's run, loaded up front
     const float4* src = reinterpret_cast<const float4*>(p.o_part + static_cast<long long>(bh) * S * kDLatent) +
                         chunk * (kCombineChunk / 4) + lane;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int i = 0; i < S; ++i) {
-        const float w = weight[i];
-        const float4 v = src[static_cast<long long>(i) * (kDLatent / 4)];
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+    float4 v[kMaxRun];
+#pragma unroll
+    for (int i = 0; i < kMaxRun; ++i) {
+        const int s = s0 + i;
+        v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    reinterpret_cast<float4*>(p.out + static_cast<long long>(bh) * kDLatent)[chunk * (kCombineChunk / 4) + lane] = acc;
-    if (chunk == 0 && lane == 0) p.lse[bh] = total;
+
+    // slice weights exp(lse_s - lse)
+    const float ls = (threadIdx.x < S) ? p.lse_part[static_cast<long long>(bh) * S + threadIdx.x] : -INFINITY;
+    float mx = ls;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red_max[warp] = mx;
+    __syncthreads();
+    mx = red_max[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w]);
+    float e = (mx == -INFINITY || threadIdx.x >= S) ? 0.f : expf(ls - mx);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+    if (lane == 0) red_sum[warp] = e;
+    __syncthreads();
+    float sum = red_sum[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) sum += red_sum[w];
+    const float total = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+    if (threadIdx.x < S) weight[threadIdx.x] = (mx == -INFINITY) ? 0.f : expf(ls - total);
+    __syncthreads();
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kMaxRun; ++i) {
+        const int s = s0 + i;
+        if (s < s1) {
+            const float w = weight[s];
+            acc.x += w * v[i].x;
+            acc.y += w * v[i].y;
+            acc.z += w * v[i].z;
+            acc.w += w * v[i].w;
+        }
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float4 o = part[0][lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) {
+            const float4 q = part[w][lane];
+            o.x += q.x;
+            o.y += q.y;
+            o.z += q.z;
+            o.w += q.w;
+        }
+        reinterpret_cast<float4*>(p.out + static_cast<long long>(bh) * kDLatent)[chunk * (kCombineChunk / 4) + lane] = o;
+        if (chunk == 0 && lane == 0) p.lse[bh] = total;
+    }
 }
 
 }  // namespace
+
+int combine_block_threads() { return kThreads; }
 
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};

@@ -238,7 +238,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.smem_bytes = static_cast<int>(mla::partial_mma_smem_bytes());
     pl.combine_grid_x = s.batch * s.heads;
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
-    pl.combine_block = 32;
+    pl.combine_block = mla::combine_block_threads();
 
     const size_t bh = static_cast<size_t>(s.batch) * s.heads;
     pl.status_offset = 0;

@@ -27,6 +27,8 @@ struct PartialParams {
     const int* cache_len;       // sparse [B]
     const int* indices;         // sparse [B][topk]
     int batch, heads, topk, splits, sparse;
+    int n_groups;               // heads / kHeadGroup
+    int n_items;                // batch * n_groups * splits work items, walked round-robin by the CTAs
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units
     float* o_part;              // [B][H][S][512]
     float* lse_part;            // [B][H][S]
@@ -40,6 +42,10 @@ struct CombineParams {
     float* out;                 // [B][H][512]
     float* lse;                 // [B][H]
     int batch, heads, splits;
+    int sparse, topk;           // with d_pos / row_offset / kv_rows: which slices hold entries
+    const int* d_pos;
+    const long long* row_offset;
+    long long kv_rows;
 };
 
 struct AppendParams {
@@ -58,6 +64,7 @@ size_t partial_mma_smem_bytes();
 int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
 cudaError_t launch_partial_mma(const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
+int combine_block_threads();
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_advance(int* d_pos, int batch, bool pdl, cudaStream_t stream);

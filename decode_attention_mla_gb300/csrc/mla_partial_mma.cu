@@ -21,7 +21,8 @@
 //                   Every warp then applies the same online-softmax update
 //                   (base-2 exponent, quad shuffles for row max / row sum)
 //                   and accumulates O[16 x 128 features of its own] += P . V
-//                   with P rounded to bf16 and V = the latent c rows.
+//                   with V = the latent c rows and P as a bf16 hi + lo pair
+//                   (two MMAs), so P keeps ~16 significant bits.
 // Epilogue: o_part = O / l (normalised) and lse_part = ln(sum exp(s)), or
 // (0, -inf) for an empty slice.  No floating-point atomics: the result is a
 // pure function of the inputs and the split count.
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2) mla_partial_mma_kernel(const Part
             if (e < e1) {
                 if (!p.sparse) {
                     row = base + e;
-                    valid = true;
+                    valid = (row >= 0 && row < p.kv_rows);
                 } else {
                     const int id = p.indices[static_cast<long long>(b) * p.topk + e];
                     if (id >= 0 && id < seg_len) {
@@ -294,14 +295,17 @@ __global__ void __launch_bounds__(kThreads, 2) mla_partial_mma_kernel(const Part
             o[i][3] *= alpha1;
         }
 
-        // ---- P (bf16) as the A operand of P . V ---------------------------
-        uint32_t pa[kPSteps][4];
+        // ---- P as the A operand of P . V, split P = P_hi + P_lo -------------
+        // A single bf16 rounding of P (relative error up to 2^-8) moves the
+        // output by ~3e-3 when a handful of rows carry the weight; the hi/lo
+        // pair keeps ~16 significant bits of P at the cost of a second MMA.
+        uint32_t pa_hi[kPSteps][4], pa_lo[kPSteps][4];
 #pragma unroll
         for (int kp = 0; kp < kPSteps; ++kp) {
-            pa[kp][0] = pack_bf16x2(sc[2 * kp][0], sc[2 * kp][1]);
-            pa[kp][1] = pack_bf16x2(sc[2 * kp][2], sc[2 * kp][3]);
-            pa[kp][2] = pack_bf16x2(sc[2 * kp + 1][0], sc[2 * kp + 1][1]);
-            pa[kp][3] = pack_bf16x2(sc[2 * kp + 1][2], sc[2 * kp + 1][3]);
+            split_bf16x2(sc[2 * kp][0], sc[2 * kp][1], pa_hi[kp][0], pa_lo[kp][0]);
+            split_bf16x2(sc[2 * kp][2], sc[2 * kp][3], pa_hi[kp][1], pa_lo[kp][1]);
+            split_bf16x2(sc[2 * kp + 1][0], sc[2 * kp + 1][1], pa_hi[kp][2], pa_lo[kp][2]);
+            split_bf16x2(sc[2 * kp + 1][2], sc[2 * kp + 1][3], pa_hi[kp][3], pa_lo[kp][3]);
         }
         // ---- O[:, own 128 features] += P . V --------------------------------
 #pragma unroll
@@ -312,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 2) mla_partial_mma_kernel(const Part
                 const int fbytes = (f_base + 8 * nt + ((lmat >> 1) << 3)) * 2;
                 uint32_t vb[4];
                 ldmatrix_x4_trans(vb, kv_base + row * kSmemRow + fbytes);
-                mma_bf16_16816(o[nt], pa[kp], vb[0], vb[1]);
-                mma_bf16_16816(o[nt + 1], pa[kp], vb[2], vb[3]);
+                mma_bf16_16816(o[nt], pa_lo[kp], vb[0], vb[1]);
+                mma_bf16_16816(o[nt + 1], pa_lo[kp], vb[2], vb[3]);
+                mma_bf16_16816(o[nt], pa_hi[kp], vb[0], vb[1]);
+                mma_bf16_16816(o[nt + 1], pa_hi[kp], vb[2], vb[3]);
             }
         }
         __syncwarp();

@@ -151,7 +151,7 @@ MLA_API int mla_decode_run(const mla_decode_plan_t *plan, const mla_decode_args 
 
 /* Launch the log-sum-exp combine: M = max_s lse_s, lse = M + ln sum_s
  * exp(lse_s - M), out = sum_s exp(lse_s - lse) * o_s with s ascending, for
- * every (request, head), over a (B*H, 512/128) grid ("Graph-resident decode",
+ * every (request, head), over a (B*H, 512/128) grid of 256-thread CTAs ("Graph-resident decode",
  * Lecture 08, s.6: a merge grid wider than n_head, no serial prologue).
  * Must follow mla_decode_run on the same stream with the same plan and
  * scratch.  Errors as mla_decode_run. */

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
 D_LATENT = 512
 D_ROPE = 64
 D_ROW = 576
-MAX_SPLITS = 128
+MAX_SPLITS = 256
 
 OK, EINVAL, EUNSUPPORTED, ESCRATCH, EALIGN, ECUDA, EDEVICE, ENOTREADY = 0, -1, -2, -3, -4, -5, -6, -7
 

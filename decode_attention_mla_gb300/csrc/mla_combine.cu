@@ -6,25 +6,28 @@
 // a grid wider than n_head and no serial thread-0 prologue).
 //
 // Grid (B*H, 512/128): a CTA merges 128 output features of one (request,
-// head).  Its 8 warps take contiguous runs of slices; each lane owns 4
-// consecutive features and first loads all of its run's partials into
-// registers, so those loads are in flight together with the lse loads.  Each
-// warp adds its run in ascending slice order and the 8 run sums are added in
-// warp order: a fixed association, so the result is reproducible bit for bit.
-// An all-empty row set gives lse = -inf and out = 0.
+// head).  Only the slices that hold entries are read (the same slicing as the
+// partial kernel).  The 8 warps take contiguous runs of those slices; each
+// lane owns 4 consecutive features and loads its run's partials (16 at a time)
+// before the weights are known, so those loads are in flight together with
+// the lse loads.  Each warp adds its run in ascending slice order and the 8
+// run sums are added in warp order: a fixed association, so the result is
+// reproducible bit for bit.  An all-empty row set gives lse = -inf, out = 0.
 #include <cmath>
 
 #include "device_utils.cuh"
 #include "mla_decode.h"
 #include "mla_internal.h"
+#include "slicing.cuh"
 
 namespace mla {
 namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxRun = (MLA_MAX_SPLITS + kWarps - 1) / kWarps;   // slices per warp at most
+constexpr int kBatch = 16;                                       // partials a lane loads at once
 static_assert(MLA_MAX_SPLITS <= kThreads, "one lse per thread");
+static_assert(MLA_MAX_SPLITS <= kWarps * 2 * kBatch, "a warp's run fits two load batches");
 
 __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombineParams p) {
     __shared__ float weight[MLA_MAX_SPLITS];
@@ -34,26 +37,33 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     grid_dependency_wait();          // the partials come from the preceding kernel
     allow_dependent_launch();
     const int bh = blockIdx.x;
+    const int b = bh / p.heads;
     const int chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.splits;
-    const int run = (S + kWarps - 1) / kWarps;
+    // only the slices that hold entries were written by the partial kernel
+    long long base;
+    const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, b, &base);
+    const long long per = slice_entries(n, S);
+    const int S_used = per > 0 ? static_cast<int>(min(static_cast<long long>(S), (n + per - 1) / per)) : 0;
+    const int run = (S_used + kWarps - 1) / kWarps;
     const int s0 = warp * run;
-    const int s1 = min(S, s0 + run);
+    const int s1 = min(S_used, s0 + run);
 
-    // partials of this warp's run, loaded up front
+    // the first batch of this warp's partials, loaded before the weights are known
     const float4* src = reinterpret_cast<const float4*>(p.o_part + static_cast<long long>(bh) * S * kDLatent) +
                         chunk * (kCombineChunk / 4) + lane;
-    float4 v[kMaxRun];
+    float4 v[kBatch];
 #pragma unroll
-    for (int i = 0; i < kMaxRun; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
         const int s = s0 + i;
         v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     // slice weights exp(lse_s - lse)
-    const float ls = (threadIdx.x < S) ? p.lse_part[static_cast<long long>(bh) * S + threadIdx.x] : -INFINITY;
+    const int t = threadIdx.x;
+    const float ls = (t < S_used) ? p.lse_part[static_cast<long long>(bh) * S + t] : -INFINITY;
     float mx = ls;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -62,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     mx = red_max[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w]);
-    float e = (mx == -INFINITY || threadIdx.x >= S) ? 0.f : expf(ls - mx);
+    float e = (mx == -INFINITY || t >= S_used) ? 0.f : expf(ls - mx);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
     if (lane == 0) red_sum[warp] = e;
@@ -71,12 +81,13 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) sum += red_sum[w];
     const float total = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-    if (threadIdx.x < S) weight[threadIdx.x] = (mx == -INFINITY) ? 0.f : expf(ls - total);
+    if (t < S_used) weight[t] = (mx == -INFINITY) ? 0.f : expf(ls - total);
     __syncthreads();
 
+    // this warp's run, ascending slice order
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kMaxRun; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
         const int s = s0 + i;
         if (s < s1) {
             const float w = weight[s];
@@ -84,6 +95,24 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
             acc.y += w * v[i].y;
             acc.z += w * v[i].z;
             acc.w += w * v[i].w;
+        }
+    }
+    if (s0 + kBatch < s1) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int s = s0 + kBatch + i;
+            v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int s = s0 + kBatch + i;
+            if (s < s1) {
+                const float w = weight[s];
+                acc.x += w * v[i].x;
+                acc.y += w * v[i].y;
+                acc.z += w * v[i].z;
+                acc.w += w * v[i].w;
+            }
         }
     }
     part[warp][lane] = acc;

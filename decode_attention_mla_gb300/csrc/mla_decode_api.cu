@@ -1,5 +1,6 @@
 // mla_decode_api.cu -- the C ABI declared in include/mla_decode.h: the
 // planner, argument checks and kernel launches.  Host code only.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -7,17 +8,18 @@
 
 #include "mla_decode.h"
 #include "mla_internal.h"
+#include "slicing.cuh"
 
 namespace {
 
 constexpr int kPlanMagic = 0x4d4c4131;       // "MLA1"
 constexpr int kMaxDevices = 64;
-// Resident-CTA target of the split derivation: two partial CTAs per SM, so
-// one CTA's copies overlap the other's math ("Launch Geometry", Lecture 04,
-// s.4: kMlaBlocksPerSm = 2, named beside the derivation it drives).
-constexpr int kCtasPerSmTarget = 2;
-// A slice must read at least this many times the bytes its partials write.
-constexpr int kSliceBytesOverPartialBytes = 2;
+// The partial kernel is persistent with one CTA per SM: its 5-stage ring of
+// cache rows fills the shared memory.  The two-CTAs-per-SM target named in
+// "Launch Geometry" (Lecture 04, s.4: kMlaBlocksPerSm = 2) was there so one
+// CTA's loads overlap another's math; here the producer warp and the MMA warps
+// of one CTA overlap them through the ring instead.
+constexpr int kCtasPerSm = 1;
 constexpr size_t kScratchAlign = 256;
 
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -101,8 +103,9 @@ int check_plan(const mla_decode_plan_t* pl) {
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
     if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (pl->head_group != mla::kHeadGroup || pl->n_head_groups * pl->head_group != pl->shape.heads) return MLA_EINVAL;
-    if (pl->grid_x != pl->n_head_groups || pl->grid_y != pl->splits || pl->grid_z != pl->shape.batch)
-        return MLA_EINVAL;
+    const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
+    if (pl->grid_x < 1 || pl->grid_x > items || pl->grid_y != 1 || pl->grid_z != 1) return MLA_EINVAL;
+    if (items > 0x7fffffffLL) return MLA_EINVAL;
     return MLA_OK;
 }
 
@@ -158,6 +161,8 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.topk = pl->shape.topk;
     p.splits = pl->splits;
     p.sparse = pl->shape.sparse;
+    p.n_groups = pl->n_head_groups;
+    p.n_items = pl->shape.batch * pl->n_head_groups * pl->splits;
     p.scale_log2 = pl->shape.scale * 1.4426950408889634f;
     p.o_part = reinterpret_cast<float*>(base + pl->o_part_offset);
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
@@ -181,6 +186,11 @@ int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void
     c.batch = pl->shape.batch;
     c.heads = pl->shape.heads;
     c.splits = pl->splits;
+    c.sparse = pl->shape.sparse;
+    c.topk = pl->shape.topk;
+    c.d_pos = a->d_pos;
+    c.row_offset = a->row_offset;
+    c.kv_rows = a->kv_rows;
     return launch_status(mla::launch_combine(c, dim3(pl->combine_grid_x, pl->combine_grid_y, 1), pl->combine_block,
                                              pl->shape.pdl != 0, static_cast<cudaStream_t>(stream)));
 }
@@ -210,30 +220,37 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.variant = 1;
     pl.head_group = mla::kHeadGroup;
     pl.n_head_groups = s.heads / mla::kHeadGroup;
-    pl.ctas_per_sm = kCtasPerSmTarget;
+    pl.ctas_per_sm = kCtasPerSm;
     pl.num_sms = sms;
 
-    // Split count derived from the shape ("Launch Geometry", Lecture 04, s.4):
-    // enough CTAs for ctas_per_sm per SM, but no slice so short that its
-    // partial write (heads x (512 + 1) fp32) outweighs half its KV bytes.
+    // Split count derived from the shape ("Launch Geometry", Lecture 04, s.4:
+    // derive it, do not pin it): minimise the modelled partial-kernel time
+    //   waves(S) * (stages per slice(S) + 1),  waves = ceil(items / grid),
+    // over S, where a slice is ceil(rows / S) rounded up to whole 32-row
+    // stages and only non-empty slices are items.
     const long long rows = s.sparse ? s.topk : s.max_ctx;
-    const long long partial_bytes = static_cast<long long>(s.heads) * (MLA_D_LATENT + 1) * 4;
-    long long min_rows = ceil_div(kSliceBytesOverPartialBytes * partial_bytes, mla::kRowBytes);
-    min_rows = ceil_div(min_rows, mla::kStageRows) * mla::kStageRows;
-    const long long cap = ceil_div(rows, min_rows);
-    long long S = ceil_div(static_cast<long long>(kCtasPerSmTarget) * sms,
-                           static_cast<long long>(s.batch) * pl.n_head_groups);
-    if (S > cap) S = cap;
-    if (S > MLA_MAX_SPLITS) S = MLA_MAX_SPLITS;
-    if (S < 1) S = 1;
+    const long long pairs = static_cast<long long>(s.batch) * pl.n_head_groups;
+    const long long grid_cap = static_cast<long long>(kCtasPerSm) * sms;
+    long long best_s = 1, best_cost = -1;
+    const long long s_hi = std::min<long long>(MLA_MAX_SPLITS, ceil_div(rows, mla::kStageRows));
+    for (long long S = 1; S <= s_hi; ++S) {
+        const long long per = mla::slice_entries(rows, static_cast<int>(S));
+        const long long items = pairs * ceil_div(rows, per);
+        const long long waves = ceil_div(items, std::min(items, grid_cap));
+        const long long cost = waves * (per / mla::kStageRows + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_s = S;
+        }
+    }
+    long long S = best_s;
     if (s.splits_override > 0) S = s.splits_override;
     pl.splits = static_cast<int>(S);
-    long long per = ceil_div(rows, S);
-    pl.entries_per_split = static_cast<int>(ceil_div(per, mla::kStageRows) * mla::kStageRows);
-
-    pl.grid_x = pl.n_head_groups;
-    pl.grid_y = pl.splits;
-    pl.grid_z = s.batch;
+    pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits));
+    const long long items = pairs * pl.splits;
+    pl.grid_x = static_cast<int>(std::min(items, grid_cap));
+    pl.grid_y = 1;
+    pl.grid_z = 1;
     pl.block = mla::partial_mma_block_threads();
     pl.smem_bytes = static_cast<int>(mla::partial_mma_smem_bytes());
     pl.combine_grid_x = s.batch * s.heads;

@@ -58,7 +58,7 @@ extern "C" {
 #define MLA_D_LATENT 512
 #define MLA_D_ROPE 64
 #define MLA_D_ROW 576        /* elements per cache row */
-#define MLA_MAX_SPLITS 128   /* largest split count a plan may hold */
+#define MLA_MAX_SPLITS 256   /* largest split count a plan may hold */
 
 typedef enum {
     MLA_OK = 0,
@@ -95,11 +95,11 @@ typedef struct {
     mla_decode_shape shape;
     int magic;                 /* set by mla_decode_plan; checked by every launch */
     int variant;               /* kernel chosen */
-    int splits;                /* S: slices per (request, head group) */
+    int splits;                /* S: slices per (request, head group) = work items per pair */
     int entries_per_split;     /* rows (dense) or list entries (sparse) per slice at max_ctx / topk */
     int head_group;            /* heads per CTA */
     int n_head_groups;         /* H / head_group */
-    int ctas_per_sm;           /* resident-CTA target the split count aims at */
+    int ctas_per_sm;           /* resident CTAs per SM of the partial kernel (persistent: 1) */
     int num_sms;               /* SM count planned for */
     int grid_x, grid_y, grid_z, block, smem_bytes;          /* partial kernel launch */
     int combine_grid_x, combine_grid_y, combine_block;      /* combine kernel launch */
@@ -127,12 +127,13 @@ typedef struct {
 /* Version of this ABI (MLA_DECODE_ABI_VERSION). */
 MLA_API int mla_decode_abi_version(void);
 
-/* Plan a decode: validates the shape, derives the split count
- *   S = clamp(ceil(ctas_per_sm * num_sms / (B * n_head_groups)), 1,
- *             min(MLA_MAX_SPLITS, ceil(rows / min_rows)))
- * where min_rows keeps each slice's KV bytes at least twice the bytes of the
- * partials it writes, rounded up to the kernel's 32-row stage, and fills the
- * launch geometry and scratch layout.  With num_sms == 0 it queries the
+/* Plan a decode: validates the shape, derives the split count and fills the
+ * launch geometry and scratch layout.  The partial kernel runs a persistent
+ * grid of min(items, num_sms) CTAs (one per SM) that walk the
+ * B * n_head_groups * S work items round-robin; S is the split count that
+ * minimises the modelled time ceil(items / grid) * (stages per slice + 1),
+ * one stage being 32 rows and the +1 the item's partial write, the smallest
+ * such S on ties (S <= MLA_MAX_SPLITS and no slice shorter than a stage).  With num_sms == 0 it queries the
  * current device and prepares the kernels there (call it before capturing a
  * graph).  Host only; the plan does not depend on any device pointer.
  * ("Launch Geometry", Lecture 04, s.1 and s.4; "Graph-resident decode",

@@ -47,44 +47,69 @@ def _plan(**kw):
     return mla.plan(**base)
 
 
+def _model_split(rows, pairs, sms, max_splits=256):
+    """The planner's split rule, evaluated independently: minimise
+    ceil(items / grid) * (stages per slice + 1), smallest S on ties."""
+    best = None
+    for S in range(1, min(max_splits, -(-rows // 32)) + 1):
+        per = -(-(-(-rows // S)) // 32) * 32
+        items = pairs * -(-rows // per)
+        waves = -(-items // min(items, sms))
+        cost = waves * (per // 32 + 1)
+        if best is None or cost < best[0]:
+            best = (cost, S)
+    return best[1]
+
+
 @pytest.mark.parametrize("kw,splits,entries", [
-    (dict(max_ctx=256), 4, 64),
+    (dict(max_ctx=256), 8, 32),
     (dict(max_ctx=8192), 128, 64),
-    (dict(sparse=True, topk=2048), 32, 64),
-    (dict(batch=64, sparse=True, topk=2048), 5, 416),
-    (dict(heads=128, max_ctx=32768 + 64), 38, 864),
+    (dict(sparse=True, topk=2048), 64, 32),
+    (dict(batch=64, sparse=True, topk=2048), 2, 1024),
+    (dict(heads=128, max_ctx=32768 + 64), 19, 1728),
 ])
 def test_plan_derivation_for_the_workloads(kw, splits, entries):
     p = _plan(**kw)
     assert (p.splits, p.entries_per_split) == (splits, entries)
     rows = kw.get("topk") or kw.get("max_ctx")
+    B, H = kw.get("batch", 1), kw.get("heads", 16)
     assert p.splits * p.entries_per_split >= rows
     assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
-    assert p.grid_x == p.n_head_groups == kw.get("heads", 16) // 16
-    assert p.grid_y == p.splits and p.grid_z == kw.get("batch", 1)
-    assert p.combine_grid_x == kw.get("batch", 1) * kw.get("heads", 16) and p.combine_grid_y == 4
+    assert p.n_head_groups == H // 16 and p.ctas_per_sm == 1
+    assert p.grid_x == min(B * p.n_head_groups * p.splits, 152) and p.grid_y == 1 and p.grid_z == 1
+    assert p.combine_grid_x == B * H and p.combine_grid_y == 4
     # scratch layout: status word, then o_part, then lse_part, 256-byte aligned
-    bh = kw.get("batch", 1) * kw.get("heads", 16)
+    bh = B * H
     assert p.status_offset == 0 and p.o_part_offset % 256 == 0 and p.lse_part_offset % 256 == 0
     assert p.lse_part_offset >= p.o_part_offset + bh * p.splits * 512 * 4
     assert p.scratch_bytes >= p.lse_part_offset + bh * p.splits * 4 and p.scratch_bytes % 256 == 0
+
+
+@pytest.mark.parametrize("rows", [1, 31, 32, 33, 100, 256, 1000, 8192, 20000, 131072])
+@pytest.mark.parametrize("batch,heads,sms", [(1, 16, 152), (1, 16, 132), (4, 16, 152), (64, 16, 152),
+                                             (1, 128, 152), (3, 64, 148)])
+def test_plan_split_rule_matches_model(rows, batch, heads, sms):
+    p = _plan(max_ctx=rows, batch=batch, heads=heads, num_sms=sms)
+    assert p.splits == _model_split(rows, batch * heads // 16, sms)
+    ps = _plan(sparse=True, topk=rows, batch=batch, heads=heads, num_sms=sms)
+    assert ps.splits == p.splits
 
 
 def test_plan_scales_with_sm_count_and_is_deterministic():
     a = _plan(max_ctx=131072, num_sms=132)
     b = _plan(max_ctx=131072, num_sms=132)
     assert a.as_dict() == b.as_dict()
-    assert a.splits == 128                     # capped by MLA_MAX_SPLITS
-    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == 66   # ceil(2*132/4)
-    assert _plan(max_ctx=131072, batch=4, num_sms=160).splits == 80
-    # the floor, not the SM count, binds for short contexts
-    assert _plan(max_ctx=100, num_sms=152).splits == 2
+    assert a.splits == 128 and a.grid_x == 128
+    assert _plan(max_ctx=131072, num_sms=152).splits == 152
+    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == 33
+    # short contexts: one stage per slice
+    assert _plan(max_ctx=100, num_sms=152).splits == 4
 
 
 def test_plan_override():
-    for s in (1, 2, 7, 64, 128):
+    for s in (1, 2, 7, 64, 128, 256):
         p = _plan(max_ctx=8192, splits=s)
-        assert p.splits == s and p.grid_y == s
+        assert p.splits == s and p.grid_x == min(s, 152)
         assert p.entries_per_split == -(-(-(-8192 // s)) // 32) * 32
 
 
@@ -97,7 +122,7 @@ def test_plan_override():
     (dict(max_ctx=16, scale=0.0), mla.EINVAL),
     (dict(max_ctx=16, scale=float("nan")), mla.EINVAL),
     (dict(max_ctx=16, scale=float("inf")), mla.EINVAL),
-    (dict(max_ctx=16, splits=129), mla.EINVAL),
+    (dict(max_ctx=16, splits=257), mla.EINVAL),
     (dict(max_ctx=16, splits=-1), mla.EINVAL),
     (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
     (dict(max_ctx=16, variant=7), mla.EINVAL),

@@ -243,6 +243,17 @@ def test_guard_regions_untouched():
 
 
 def test_plan_on_device_matches_occupancy_target():
-    p = mla.plan(batch=1, heads=16, max_ctx=8192, scale=workloads.SCALE)
-    assert p.num_sms == torch.cuda.get_device_properties(0).multi_processor_count
-    assert p.ctas_per_sm == 2
+    p = mla.plan(batch=1, heads=16, max_ctx=131072, scale=workloads.SCALE)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p.num_sms == sms
+    assert p.ctas_per_sm == 1 and p.grid_x == min(p.splits, sms)
+
+
+def test_persistent_grid_walks_many_items():
+    """Forced split counts far above the SM count: each CTA walks several items."""
+    x = workloads.dense(2, 32, 3000, seed=45)
+    ro, rl = _gpu.oracle_dense(x)
+    for s in (150, 256):
+        out, lse, plan, _ = _gpu.run_dense(x, splits=s)
+        assert plan.grid_x < 2 * 2 * s
+        _gpu.assert_parity(out, lse, ro, rl, f"dense B=2 H=32 S={s}")

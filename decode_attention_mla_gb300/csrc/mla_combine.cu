@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     // only the slices that hold entries were written by the partial kernel
     long long base;
     const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, b, &base);
-    const long long per = slice_entries(n, S);
+    const long long per = slice_entries(n, S, p.granule);
     const int S_used = per > 0 ? static_cast<int>(min(static_cast<long long>(S), (n + per - 1) / per)) : 0;
     const int run = (S_used + kWarps - 1) / kWarps;
     const int s0 = warp * run;

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "mla_decode.h"
 #include "mla_internal.h"
 #include "slicing.cuh"
@@ -21,6 +23,43 @@ constexpr int kMaxDevices = 64;
 // of one CTA overlap them through the ring instead.
 constexpr int kCtasPerSm = 1;
 constexpr size_t kScratchAlign = 256;
+constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 32-row stages
+constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
+
+int variant_tile_rows(int v) { return v == kVariantTc ? mla::kTcTileRows : mla::kStageRows; }
+int variant_granule(int v) { return v == kVariantTc ? 16 : mla::kStageRows; }
+
+// cuTensorMapEncodeTiled, reached through the runtime (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult qr{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+int encode_bf16_rows(CUtensorMap* map, const void* base, long long rows, long long row_stride_elems,
+                     uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return MLA_ECUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLA_D_ROW), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_elems) * 2u};
+    const cuuint32_t box[2] = {64u, box_rows};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                           elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
+}
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_prepared[kMaxDevices];
@@ -61,7 +100,7 @@ int prepare_device(int dev) {
     if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
     std::lock_guard<std::mutex> lock(g_prepare_mutex);
     if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
-    if (mla::partial_mma_prepare(dev) != cudaSuccess) {
+    if (mla::partial_mma_prepare(dev) != cudaSuccess || mla::partial_tc_prepare(dev) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ECUDA;
     }
@@ -88,7 +127,7 @@ int check_shape(const mla_decode_shape* s) {
     if (s->batch < 1 || s->batch > 65535) return MLA_EINVAL;
     if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
-    if (s->variant < 0 || s->variant > 1) return MLA_EINVAL;
+    if (s->variant < 0 || s->variant > 2) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
     if (!s->sparse && s->max_ctx < 1) return MLA_EINVAL;
@@ -102,6 +141,7 @@ int check_plan(const mla_decode_plan_t* pl) {
     if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
     if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
+    if (pl->variant != kVariantWarpMma && pl->variant != kVariantTc) return MLA_EINVAL;
     if (pl->head_group != mla::kHeadGroup || pl->n_head_groups * pl->head_group != pl->shape.heads) return MLA_EINVAL;
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
     if (pl->grid_x < 1 || pl->grid_x > items || pl->grid_y != 1 || pl->grid_z != 1) return MLA_EINVAL;
@@ -163,11 +203,24 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.sparse = pl->shape.sparse;
     p.n_groups = pl->n_head_groups;
     p.n_items = pl->shape.batch * pl->n_head_groups * pl->splits;
+    p.granule = variant_granule(pl->variant);
     p.scale_log2 = pl->shape.scale * 1.4426950408889634f;
     p.o_part = reinterpret_cast<float*>(base + pl->o_part_offset);
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
-    return launch_status(mla::launch_partial_mma(p, dim3(pl->grid_x, pl->grid_y, pl->grid_z), pl->shape.pdl != 0, st));
+    const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
+    if (pl->variant == kVariantTc) {
+        // TMA coordinates are 32-bit: the cache must be addressable by them
+        if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
+        mla::TcMaps maps;
+        rc = encode_bf16_rows(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kTcTileRows);
+        if (rc == MLA_OK)
+            rc = encode_bf16_rows(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads, MLA_D_ROW,
+                                  mla::kHeadGroup);
+        if (rc != MLA_OK) return rc;
+        return launch_status(mla::launch_partial_tc(maps, p, grid, pl->shape.pdl != 0, st));
+    }
+    return launch_status(mla::launch_partial_mma(p, grid, pl->shape.pdl != 0, st));
 }
 
 int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void* scratch, size_t bytes,
@@ -191,6 +244,7 @@ int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void
     c.d_pos = a->d_pos;
     c.row_offset = a->row_offset;
     c.kv_rows = a->kv_rows;
+    c.granule = variant_granule(pl->variant);
     return launch_status(mla::launch_combine(c, dim3(pl->combine_grid_x, pl->combine_grid_y, 1), pl->combine_block,
                                              pl->shape.pdl != 0, static_cast<cudaStream_t>(stream)));
 }
@@ -217,7 +271,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     mla_decode_plan_t pl{};
     pl.shape = s;
     pl.magic = kPlanMagic;
-    pl.variant = 1;
+    pl.variant = s.variant == 0 ? kVariantTc : s.variant;
     pl.head_group = mla::kHeadGroup;
     pl.n_head_groups = s.heads / mla::kHeadGroup;
     pl.ctas_per_sm = kCtasPerSm;
@@ -231,13 +285,15 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     const long long rows = s.sparse ? s.topk : s.max_ctx;
     const long long pairs = static_cast<long long>(s.batch) * pl.n_head_groups;
     const long long grid_cap = static_cast<long long>(kCtasPerSm) * sms;
+    const int tile = variant_tile_rows(pl.variant);
+    const int granule = variant_granule(pl.variant);
     long long best_s = 1, best_cost = -1;
-    const long long s_hi = std::min<long long>(MLA_MAX_SPLITS, ceil_div(rows, mla::kStageRows));
+    const long long s_hi = std::min<long long>(MLA_MAX_SPLITS, ceil_div(rows, granule));
     for (long long S = 1; S <= s_hi; ++S) {
-        const long long per = mla::slice_entries(rows, static_cast<int>(S));
+        const long long per = mla::slice_entries(rows, static_cast<int>(S), granule);
         const long long items = pairs * ceil_div(rows, per);
         const long long waves = ceil_div(items, std::min(items, grid_cap));
-        const long long cost = waves * (per / mla::kStageRows + 1);
+        const long long cost = waves * (ceil_div(per, tile) + 1);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best_s = S;
@@ -246,13 +302,14 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     long long S = best_s;
     if (s.splits_override > 0) S = s.splits_override;
     pl.splits = static_cast<int>(S);
-    pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits));
+    pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits, granule));
     const long long items = pairs * pl.splits;
     pl.grid_x = static_cast<int>(std::min(items, grid_cap));
     pl.grid_y = 1;
     pl.grid_z = 1;
-    pl.block = mla::partial_mma_block_threads();
-    pl.smem_bytes = static_cast<int>(mla::partial_mma_smem_bytes());
+    pl.block = pl.variant == kVariantTc ? mla::partial_tc_block_threads() : mla::partial_mma_block_threads();
+    pl.smem_bytes = static_cast<int>(pl.variant == kVariantTc ? mla::partial_tc_smem_bytes()
+                                                              : mla::partial_mma_smem_bytes());
     pl.combine_grid_x = s.batch * s.heads;
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
     pl.combine_block = mla::combine_block_threads();

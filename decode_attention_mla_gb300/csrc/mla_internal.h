@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mla {
@@ -12,7 +13,8 @@ constexpr int kDLatent = 512;
 constexpr int kDRope = 64;
 constexpr int kDRow = kDLatent + kDRope;       // 576 bf16 per cache row
 constexpr int kRowBytes = kDRow * 2;           // 1152
-constexpr int kStageRows = 32;                 // rows per pipeline stage (partial kernel)
+constexpr int kStageRows = 32;                 // rows per pipeline stage (warp-MMA partial kernel)
+constexpr int kTcTileRows = 80;                // rows per tile (tcgen05 partial kernel)
 constexpr int kHeadGroup = 16;                 // heads per CTA of the warp-MMA kernel
 constexpr int kCombineChunk = 128;             // features per combine CTA
 
@@ -28,6 +30,7 @@ struct PartialParams {
     const int* indices;         // sparse [B][topk]
     int batch, heads, topk, splits, sparse;
     int n_groups;               // heads / kHeadGroup
+    int granule;                // slices are whole multiples of this many entries
     int n_items;                // batch * n_groups * splits work items, walked round-robin by the CTAs
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units
     float* o_part;              // [B][H][S][512]
@@ -43,6 +46,7 @@ struct CombineParams {
     float* lse;                 // [B][H]
     int batch, heads, splits;
     int sparse, topk;           // with d_pos / row_offset / kv_rows: which slices hold entries
+    int granule;
     const int* d_pos;
     const long long* row_offset;
     long long kv_rows;
@@ -58,12 +62,24 @@ struct AppendParams {
     int batch;
 };
 
+// TMA descriptors of the tcgen05 kernel: the cache rows [kv_rows x 576] in
+// boxes of 64 x 80 and the queries [B*H x 576] in boxes of 64 x 16, both
+// with the 128-byte swizzle.
+struct TcMaps {
+    CUtensorMap kv;
+    CUtensorMap q;
+};
+
 // Launch helpers (each returns the cudaError_t of the launch).
 cudaError_t partial_mma_prepare(int device);
 size_t partial_mma_smem_bytes();
 int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
 cudaError_t launch_partial_mma(const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
+cudaError_t partial_tc_prepare(int device);
+size_t partial_tc_smem_bytes();
+int partial_tc_block_threads();
+cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
 int combine_block_threads();
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t stream);

@@ -91,7 +91,7 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     it.s = rest % p.splits;
     it.b = rest / p.splits;
     const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base);
-    const long long per = slice_entries(n, p.splits);
+    const long long per = slice_entries(n, p.splits, p.granule);
     long long e0 = static_cast<long long>(it.s) * per;
     long long e1 = e0 + per;
     if (e1 > n) e1 = n;

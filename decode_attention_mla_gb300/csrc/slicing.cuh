@@ -22,10 +22,11 @@ __device__ __forceinline__ long long request_entries(int sparse, int topk, const
     return n;
 }
 
-// Entries per slice: ceil(n / S) rounded up to whole 32-row stages.
-__host__ __device__ __forceinline__ long long slice_entries(long long n, int splits) {
+// Entries per slice: ceil(n / S) rounded up to a whole number of granules
+// (the kernel's row step: 32 for the warp-MMA kernel, 16 for tcgen05).
+__host__ __device__ __forceinline__ long long slice_entries(long long n, int splits, int granule) {
     long long per = (n + splits - 1) / splits;
-    return (per + kStageRows - 1) / kStageRows * kStageRows;
+    return (per + granule - 1) / granule * granule;
 }
 
 }  // namespace mla

@@ -63,7 +63,8 @@ extern "C" {
 typedef enum {
     MLA_OK = 0,
     MLA_EINVAL = -1,        /* null pointer, bad shape, size or plan */
-    MLA_EUNSUPPORTED = -2,  /* shape the kernels do not implement (d_c != 512, d_r != 64, H) */
+    MLA_EUNSUPPORTED = -2,  /* shape the kernels do not implement (d_c != 512, d_r != 64, H,
+                               or a cache of 2^31 rows or more for the tcgen05 kernel) */
     MLA_ESCRATCH = -3,      /* scratch missing, misaligned or smaller than plan->scratch_bytes */
     MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 */
     MLA_ECUDA = -5,         /* the CUDA runtime reported an error for a launch or query */
@@ -83,7 +84,8 @@ typedef struct {
     float scale;          /* softmax scale, finite and > 0 (1/sqrt(576) for these shapes) */
     int num_sms;          /* SMs to plan for; 0 = query the current device */
     int splits_override;  /* 0 = derive; 1..MLA_MAX_SPLITS = force this split count */
-    int variant;          /* 0 = auto; 1 = head-group-16 warp-MMA kernel */
+    int variant;          /* 0 = auto (2); 1 = warp-MMA (mma.sync) kernel, 32-row stages;
+                             2 = tcgen05/TMEM kernel, 80-row TMA tiles (both: 16 heads per CTA) */
     int pdl;              /* 1 = launch with programmatic dependent launch */
 } mla_decode_shape;
 
@@ -131,9 +133,11 @@ MLA_API int mla_decode_abi_version(void);
  * launch geometry and scratch layout.  The partial kernel runs a persistent
  * grid of min(items, num_sms) CTAs (one per SM) that walk the
  * B * n_head_groups * S work items round-robin; S is the split count that
- * minimises the modelled time ceil(items / grid) * (stages per slice + 1),
- * one stage being 32 rows and the +1 the item's partial write, the smallest
- * such S on ties (S <= MLA_MAX_SPLITS and no slice shorter than a stage).  With num_sms == 0 it queries the
+ * minimises the modelled time ceil(items / grid) * (tiles per slice + 1),
+ * a tile being the kernel's row step (80 rows for tcgen05, 32 for warp-MMA)
+ * and the +1 the item's partial write, the smallest such S on ties; slices
+ * are whole multiples of 16 (tcgen05) or 32 (warp-MMA) rows and
+ * S <= MLA_MAX_SPLITS.  With num_sms == 0 it queries the
  * current device and prepares the kernels there (call it before capturing a
  * graph).  Host only; the plan does not depend on any device pointer.
  * ("Launch Geometry", Lecture 04, s.1 and s.4; "Graph-resident decode",

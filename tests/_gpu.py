@@ -17,13 +17,18 @@ def dev():
     return torch.device("cuda:0")
 
 
-def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, plan=None, max_ctx=None):
+VARIANTS = [1, 2]      # warp-MMA kernel, tcgen05 kernel
+GRANULE = {1: 32, 2: 16}
+
+
+def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, plan=None, max_ctx=None, variant=0):
     """Dense decode of workloads.DenseInputs on the GPU; returns (out, lse, plan, scratch)."""
     d = dev()
     B, H, _ = x.q.shape
     if plan is None:
         mc = max_ctx or int(x.d_pos.max()) + 1
-        plan = mla.plan(batch=B, heads=H, max_ctx=mc, scale=x.scale, splits=splits, pdl=pdl, num_sms=num_sms)
+        plan = mla.plan(batch=B, heads=H, max_ctx=mc, scale=x.scale, splits=splits, pdl=pdl, num_sms=num_sms,
+                        variant=variant)
     if scratch is None:
         scratch = mla.alloc_scratch(plan)
     out = torch.full((B, H, 512), float("nan"), device=d)
@@ -34,12 +39,13 @@ def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, pl
     return out, lse, plan, scratch
 
 
-def run_sparse(x, *, splits=0, pdl=False, scratch=None, plan=None, kv_dev=None):
+def run_sparse(x, *, splits=0, pdl=False, scratch=None, plan=None, kv_dev=None, variant=0):
     d = dev()
     B, H, _ = x.q.shape
     topk = x.indices.shape[1]
     if plan is None:
-        plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl)
+        plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl,
+                        variant=variant)
     if scratch is None:
         scratch = mla.alloc_scratch(plan)
     out = torch.full((B, H, 512), float("nan"), device=d)

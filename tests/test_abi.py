@@ -47,30 +47,38 @@ def _plan(**kw):
     return mla.plan(**base)
 
 
-def _model_split(rows, pairs, sms, max_splits=256):
+TILE = {1: 32, 2: 80}        # rows per kernel step: warp-MMA stage, tcgen05 tile
+GRANULE = {1: 32, 2: 16}     # slices are whole multiples of this
+
+
+def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     """The planner's split rule, evaluated independently: minimise
-    ceil(items / grid) * (stages per slice + 1), smallest S on ties."""
+    ceil(items / grid) * (tiles per slice + 1), smallest S on ties."""
+    tile, gran = TILE[variant], GRANULE[variant]
     best = None
-    for S in range(1, min(max_splits, -(-rows // 32)) + 1):
-        per = -(-(-(-rows // S)) // 32) * 32
+    for S in range(1, min(max_splits, -(-rows // gran)) + 1):
+        per = -(-(-(-rows // S)) // gran) * gran
         items = pairs * -(-rows // per)
         waves = -(-items // min(items, sms))
-        cost = waves * (per // 32 + 1)
+        cost = waves * (-(-per // tile) + 1)
         if best is None or cost < best[0]:
             best = (cost, S)
     return best[1]
 
 
 @pytest.mark.parametrize("kw,splits,entries", [
-    (dict(max_ctx=256), 8, 32),
-    (dict(max_ctx=8192), 128, 64),
-    (dict(sparse=True, topk=2048), 64, 32),
+    (dict(max_ctx=256), 4, 64),
+    (dict(max_ctx=8192), 103, 80),
+    (dict(sparse=True, topk=2048), 26, 80),
     (dict(batch=64, sparse=True, topk=2048), 2, 1024),
     (dict(heads=128, max_ctx=32768 + 64), 19, 1728),
+    (dict(max_ctx=8192, variant=1), 128, 64),
+    (dict(sparse=True, topk=2048, variant=1), 64, 32),
 ])
 def test_plan_derivation_for_the_workloads(kw, splits, entries):
     p = _plan(**kw)
     assert (p.splits, p.entries_per_split) == (splits, entries)
+    assert p.variant == (kw.get("variant") or 2)
     rows = kw.get("topk") or kw.get("max_ctx")
     B, H = kw.get("batch", 1), kw.get("heads", 16)
     assert p.splits * p.entries_per_split >= rows
@@ -85,13 +93,14 @@ def test_plan_derivation_for_the_workloads(kw, splits, entries):
     assert p.scratch_bytes >= p.lse_part_offset + bh * p.splits * 4 and p.scratch_bytes % 256 == 0
 
 
+@pytest.mark.parametrize("variant", [1, 2])
 @pytest.mark.parametrize("rows", [1, 31, 32, 33, 100, 256, 1000, 8192, 20000, 131072])
 @pytest.mark.parametrize("batch,heads,sms", [(1, 16, 152), (1, 16, 132), (4, 16, 152), (64, 16, 152),
                                              (1, 128, 152), (3, 64, 148)])
-def test_plan_split_rule_matches_model(rows, batch, heads, sms):
-    p = _plan(max_ctx=rows, batch=batch, heads=heads, num_sms=sms)
-    assert p.splits == _model_split(rows, batch * heads // 16, sms)
-    ps = _plan(sparse=True, topk=rows, batch=batch, heads=heads, num_sms=sms)
+def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
+    p = _plan(max_ctx=rows, batch=batch, heads=heads, num_sms=sms, variant=variant)
+    assert p.splits == _model_split(rows, batch * heads // 16, sms, variant)
+    ps = _plan(sparse=True, topk=rows, batch=batch, heads=heads, num_sms=sms, variant=variant)
     assert ps.splits == p.splits
 
 
@@ -99,18 +108,19 @@ def test_plan_scales_with_sm_count_and_is_deterministic():
     a = _plan(max_ctx=131072, num_sms=132)
     b = _plan(max_ctx=131072, num_sms=132)
     assert a.as_dict() == b.as_dict()
-    assert a.splits == 128 and a.grid_x == 128
-    assert _plan(max_ctx=131072, num_sms=152).splits == 152
-    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == 33
-    # short contexts: one stage per slice
-    assert _plan(max_ctx=100, num_sms=152).splits == 4
+    assert a.splits == _model_split(131072, 1, 132) and a.grid_x <= 132
+    assert _plan(max_ctx=131072, num_sms=152).splits == _model_split(131072, 1, 152)
+    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == _model_split(131072, 4, 132)
+    # short contexts: one tile per slice
+    assert _plan(max_ctx=100, num_sms=152).entries_per_split <= 80
 
 
 def test_plan_override():
     for s in (1, 2, 7, 64, 128, 256):
-        p = _plan(max_ctx=8192, splits=s)
-        assert p.splits == s and p.grid_x == min(s, 152)
-        assert p.entries_per_split == -(-(-(-8192 // s)) // 32) * 32
+        for v in (1, 2):
+            p = _plan(max_ctx=8192, splits=s, variant=v)
+            assert p.splits == s and p.grid_x == min(s, 152)
+            assert p.entries_per_split == -(-(-(-8192 // s)) // GRANULE[v]) * GRANULE[v]
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -126,6 +136,7 @@ def test_plan_override():
     (dict(max_ctx=16, splits=-1), mla.EINVAL),
     (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
     (dict(max_ctx=16, variant=7), mla.EINVAL),
+    (dict(max_ctx=16, variant=3), mla.EINVAL),
 ])
 def test_plan_rejects(kw, status):
     with pytest.raises(mla.MLADecodeError) as e:

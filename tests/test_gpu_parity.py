@@ -26,11 +26,12 @@ def _setup():
 
 
 # ---- dense, small shapes: several stages, ragged tails, many split counts ----
-@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 100, 256, 1000, 2049])
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 79, 80, 81, 100, 160, 256, 1000, 2049])
 @pytest.mark.parametrize("splits", [0, 1, 3, 8])
-def test_dense_small(T, splits):
+def test_dense_small(T, splits, variant):
     x = workloads.dense(1, 16, T, seed=T)
-    out, lse, plan, scratch = _gpu.run_dense(x, splits=splits)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=splits, variant=variant)
     ro, rl = _gpu.oracle_dense(x)
     _gpu.assert_parity(out, lse, ro, rl, f"dense T={T} S={plan.splits}")
     assert mla.status_word(plan, scratch) == 0
@@ -43,12 +44,13 @@ def test_dense_t256_workload():
     _gpu.assert_parity(out, lse, ro, rl, "dense_t256")
 
 
-def test_dense_t8192_split_sweep():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_dense_t8192_split_sweep(variant):
     x = workloads.make("dense_t8192")
     ro, rl = _gpu.oracle_dense(x)
     results = {}
     for s in (1, 2, 4, 8, 16, 32, 64, 128, 0):
-        out, lse, plan, _ = _gpu.run_dense(x, splits=s)
+        out, lse, plan, _ = _gpu.run_dense(x, splits=s, variant=variant)
         _gpu.assert_parity(out, lse, ro, rl, f"dense_t8192 S={plan.splits}")
         results[plan.splits] = (out.double().cpu().numpy(), lse.double().cpu().numpy())
     keys = sorted(results)
@@ -58,14 +60,15 @@ def test_dense_t8192_split_sweep():
             assert (np.abs(results[a][1] - results[b][1]) / np.maximum(np.abs(rl), 1)).max() <= 2 * _gpu.LSE_RTOL
 
 
-def test_dense_partials_match_oracle_split_emulation():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_dense_partials_match_oracle_split_emulation(variant):
     """The partial kernel's scratch (o_s, lse_s) against the oracle's fp64 emulation
-    of the same slices (32-row granule, as the plan cuts them)."""
+    of the same slices (cut at the kernel's granule, as the plan cuts them)."""
     x = workloads.dense(1, 16, 1000, seed=3)
-    out, lse, plan, scratch = _gpu.run_dense(x, splits=5)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=5, variant=variant)
     S = plan.splits
-    _, _, op, lp = oracle.decode_split(x.q, x.kv, scale=x.scale, splits=S, granule=32, d_pos=x.d_pos,
-                                       return_partials=True)
+    _, _, op, lp = oracle.decode_split(x.q, x.kv, scale=x.scale, splits=S, granule=_gpu.GRANULE[variant],
+                                       d_pos=x.d_pos, return_partials=True)
     o_off, l_off = plan.o_part_offset, plan.lse_part_offset
     o_gpu = scratch[o_off:o_off + 16 * S * 512 * 4].view(torch.float32).view(1, 16, S, 512).double().cpu().numpy()
     l_gpu = scratch[l_off:l_off + 16 * S * 4].view(torch.float32).view(1, 16, S).double().cpu().numpy()
@@ -75,32 +78,35 @@ def test_dense_partials_match_oracle_split_emulation():
     assert (np.abs(l_gpu[fin] - lp[fin]) / np.maximum(np.abs(lp[fin]), 1)).max() <= _gpu.LSE_RTOL
 
 
-def test_dense_batch_ragged():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_dense_batch_ragged(variant):
     B, H, cap = 3, 16, 1500
     x = workloads.dense(B, H, cap, seed=21)
     x.d_pos = torch.tensor([1499, 17, 640], dtype=torch.int32)
-    out, lse, plan, _ = _gpu.run_dense(x, max_ctx=cap)
+    out, lse, plan, _ = _gpu.run_dense(x, max_ctx=cap, variant=variant)
     ro, rl = _gpu.oracle_dense(x)
     _gpu.assert_parity(out, lse, ro, rl, "dense batch 3 ragged")
 
 
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
 @pytest.mark.parametrize("H", [32, 64, 128])
-def test_dense_more_heads(H):
+def test_dense_more_heads(H, variant):
     x = workloads.dense(1, H, 2000, seed=H)
-    out, lse, plan, _ = _gpu.run_dense(x)
+    out, lse, plan, _ = _gpu.run_dense(x, variant=variant)
     assert plan.n_head_groups == H // 16
     ro, rl = _gpu.oracle_dense(x)
     _gpu.assert_parity(out, lse, ro, rl, f"dense H={H}")
 
 
-def test_dense_row_stride_and_capacity():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_dense_row_stride_and_capacity(variant):
     """Rows padded to a 640-element stride; d_pos beyond the cache is clamped."""
     T = 700
     x = workloads.dense(1, 16, T, seed=5)
     d = _gpu.dev()
     padded = torch.zeros(T, 640, dtype=torch.bfloat16)
     padded[:, :576] = x.kv
-    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale)
+    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, variant=variant)
     scratch = mla.alloc_scratch(plan)
     out = torch.empty(1, 16, 512, device=d)
     lse = torch.empty(1, 16, device=d)
@@ -115,35 +121,39 @@ def test_dense_row_stride_and_capacity():
     _gpu.assert_parity(out, lse, ro, rl, "d_pos clamped to the cache")
 
 
-def test_uniform_scores_closed_form():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_uniform_scores_closed_form(variant):
     """q = 0: every score is 0, so out = mean of the attended latent rows and lse = ln n."""
     T = 777
     x = workloads.dense(1, 16, T, seed=9)
     x.q = torch.zeros_like(x.q)
-    out, lse, _, _ = _gpu.run_dense(x, splits=6)
+    out, lse, _, _ = _gpu.run_dense(x, splits=6, variant=variant)
     mean = x.kv[:, :512].double().mean(0).numpy()
     assert np.abs(out.double().cpu().numpy() - mean[None, None]).max() <= _gpu.OUT_ATOL
     assert np.abs(lse.double().cpu().numpy() - math.log(T)).max() <= _gpu.LSE_RTOL * math.log(T)
 
 
 # ---- sparse ------------------------------------------------------------------
-def test_sparse_k2048_workload():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_sparse_k2048_workload(variant):
     x = workloads.make("sparse_k2048")
     ro, rl = _gpu.oracle_sparse(x)
     for s in (0, 1, 7, 64):
-        out, lse, plan, _ = _gpu.run_sparse(x, splits=s)
+        out, lse, plan, _ = _gpu.run_sparse(x, splits=s, variant=variant)
         _gpu.assert_parity(out, lse, ro, rl, f"sparse_k2048 S={plan.splits}")
 
 
-@pytest.mark.parametrize("topk", [1, 17, 64, 300])
-def test_sparse_small(topk):
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("topk", [1, 17, 64, 80, 81, 300])
+def test_sparse_small(topk, variant):
     x = workloads.sparse(2, 16, [5000, 300], topk, seed=topk)
-    out, lse, plan, _ = _gpu.run_sparse(x)
+    out, lse, plan, _ = _gpu.run_sparse(x, variant=variant)
     ro, rl = _gpu.oracle_sparse(x)
     _gpu.assert_parity(out, lse, ro, rl, f"sparse k={topk}")
 
 
-def test_sparse_masking_out_of_range_ids():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_sparse_masking_out_of_range_ids(variant):
     x = workloads.sparse(2, 16, [4000, 900], 256, seed=31)
     idx = x.indices.clone()
     idx[0, 3] = -1
@@ -152,15 +162,16 @@ def test_sparse_masking_out_of_range_ids():
     idx[1, 7] = 2 ** 31 - 1
     idx[1, 255] = -(2 ** 31)
     x.indices = idx
-    out, lse, plan, _ = _gpu.run_sparse(x, splits=3)
+    out, lse, plan, _ = _gpu.run_sparse(x, splits=3, variant=variant)
     ro, rl = _gpu.oracle_sparse(x)
     _gpu.assert_parity(out, lse, ro, rl, "sparse masked ids")
 
 
-def test_sparse_all_masked_is_empty():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_sparse_all_masked_is_empty(variant):
     x = workloads.sparse(1, 16, 100, 40, seed=32)
     x.indices = torch.full_like(x.indices, -7)
-    out, lse, _, _ = _gpu.run_sparse(x, splits=2)
+    out, lse, _, _ = _gpu.run_sparse(x, splits=2, variant=variant)
     assert torch.isneginf(lse).all()
     assert (out == 0).all()
 
@@ -182,22 +193,24 @@ def test_sparse_b64_workload_sampled():
     x = workloads.make("sparse_b64")
     d = _gpu.dev()
     kv_dev = x.kv.to(d)
-    out, lse, plan, scratch = _gpu.run_sparse(x, kv_dev=kv_dev)
-    assert mla.status_word(plan, scratch) == 0
     sample = [0, 1, 17, 31, 42, 63]
     sub = workloads.SparseInputs(q=x.q[sample], kv=x.kv, indices=x.indices[sample], cache_len=x.cache_len[sample],
                                  row_offset=x.row_offset[sample])
     ro, rl = _gpu.oracle_sparse(sub)
-    _gpu.assert_parity(out[sample], lse[sample], ro, rl, "sparse_b64 sample")
+    for variant in _gpu.VARIANTS:
+        out, lse, plan, scratch = _gpu.run_sparse(x, kv_dev=kv_dev, variant=variant)
+        assert mla.status_word(plan, scratch) == 0
+        _gpu.assert_parity(out[sample], lse[sample], ro, rl, f"sparse_b64 sample, variant {variant}")
     del kv_dev
 
 
 # ---- determinism, A/A, PDL, guards -------------------------------------------
-def test_fixed_split_is_bit_identical_across_runs():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_fixed_split_is_bit_identical_across_runs(variant):
     x = workloads.dense(1, 16, 8192, seed=41)
     ref = None
     for _ in range(10):
-        out, lse, plan, _ = _gpu.run_dense(x, splits=32)
+        out, lse, plan, _ = _gpu.run_dense(x, splits=32, variant=variant)
         cur = (_gpu.bits(out).clone(), _gpu.bits(lse).clone())
         if ref is None:
             ref = cur
@@ -205,18 +218,20 @@ def test_fixed_split_is_bit_identical_across_runs():
             assert torch.equal(cur[0], ref[0]) and torch.equal(cur[1], ref[1])
 
 
-def test_aa_control_sparse():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_aa_control_sparse(variant):
     """Two independent runs of the same arm (fresh scratch each) must match byte for byte."""
     x = workloads.sparse(4, 16, [9000, 7000, 12000, 4096], 512, seed=42)
-    a = _gpu.run_sparse(x, splits=4)
-    b = _gpu.run_sparse(x, splits=4)
+    a = _gpu.run_sparse(x, splits=4, variant=variant)
+    b = _gpu.run_sparse(x, splits=4, variant=variant)
     assert torch.equal(_gpu.bits(a[0]), _gpu.bits(b[0])) and torch.equal(_gpu.bits(a[1]), _gpu.bits(b[1]))
 
 
-def test_pdl_on_off_bit_identical():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_pdl_on_off_bit_identical(variant):
     x = workloads.dense(1, 16, 4096, seed=43)
-    a = _gpu.run_dense(x, splits=16, pdl=False)
-    b = _gpu.run_dense(x, splits=16, pdl=True)
+    a = _gpu.run_dense(x, splits=16, pdl=False, variant=variant)
+    b = _gpu.run_dense(x, splits=16, pdl=True, variant=variant)
     assert torch.equal(_gpu.bits(a[0]), _gpu.bits(b[0])) and torch.equal(_gpu.bits(a[1]), _gpu.bits(b[1]))
 
 
@@ -249,11 +264,38 @@ def test_plan_on_device_matches_occupancy_target():
     assert p.ctas_per_sm == 1 and p.grid_x == min(p.splits, sms)
 
 
-def test_persistent_grid_walks_many_items():
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+def test_persistent_grid_walks_many_items(variant):
     """Forced split counts far above the SM count: each CTA walks several items."""
     x = workloads.dense(2, 32, 3000, seed=45)
     ro, rl = _gpu.oracle_dense(x)
     for s in (150, 256):
-        out, lse, plan, _ = _gpu.run_dense(x, splits=s)
+        out, lse, plan, _ = _gpu.run_dense(x, splits=s, variant=variant)
         assert plan.grid_x < 2 * 2 * s
         _gpu.assert_parity(out, lse, ro, rl, f"dense B=2 H=32 S={s}")
+
+
+def test_variants_agree():
+    """The warp-MMA and tcgen05 kernels on the same inputs: both within the bar of the
+    oracle, and within twice the bar of each other."""
+    x = workloads.dense(1, 16, 5000, seed=46)
+    a = _gpu.run_dense(x, variant=1)
+    b = _gpu.run_dense(x, variant=2)
+    assert (a[0] - b[0]).abs().max().item() <= 2 * _gpu.OUT_ATOL
+    assert ((a[1] - b[1]).abs() / a[1].abs().clamp(min=1)).max().item() <= 2 * _gpu.LSE_RTOL
+
+
+def test_tcgen05_rescale_path():
+    """Scores that keep growing along the context force the softmax reference to
+    move (and O to be rescaled in tensor memory) many times within one slice."""
+    T = 4000
+    x = workloads.dense(1, 16, T, seed=47)
+    ramp = torch.linspace(0.0, 12.0, T).unsqueeze(1)
+    kv = x.kv.float()
+    kv[:, :512] = kv[:, :512] + ramp * x.q[0, 0, :512].float().sign().unsqueeze(0) * 0.05
+    x.kv = kv.to(torch.bfloat16)
+    x.q = (x.q.float() * 4.0).to(torch.bfloat16)
+    ro, rl = _gpu.oracle_dense(x)
+    for variant in _gpu.VARIANTS:
+        out, lse, plan, _ = _gpu.run_dense(x, splits=1, variant=variant)
+        _gpu.assert_parity(out, lse, ro, rl, f"growing scores, variant {variant}")

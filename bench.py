@@ -60,7 +60,8 @@ def peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for fn in ("mla_partial_mma.cu", "device_utils.cuh", "mla_internal.h"):
+    for fn in ("mla_partial_tc.cu", "mla_partial_mma.cu", "tc_utils.cuh", "device_utils.cuh", "mla_internal.h",
+               "slicing.cuh"):
         with open(os.path.join(ROOT, "decode_attention_mla_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -139,7 +140,7 @@ class ClockSampler:
 class DenseBench:
     """Dense decode over `copies` distinct caches of T rows (B=1)."""
 
-    def __init__(self, T, H, copies, splits, pdl, seed=0):
+    def __init__(self, T, H, copies, splits, pdl, seed=0, variant=0):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
         d = torch.device("cuda")
@@ -154,7 +155,7 @@ class DenseBench:
         self.d_pos = x.d_pos.to(d)
         self.out = [torch.empty(1, H, 512, device=d) for _ in range(copies)]
         self.lse = [torch.empty(1, H, device=d) for _ in range(copies)]
-        self.plan = mla.plan(batch=1, heads=H, max_ctx=T, scale=x.scale, splits=splits, pdl=pdl)
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=T, scale=x.scale, splits=splits, pdl=pdl, variant=variant)
         self.scratch = mla.alloc_scratch(self.plan)
         self.args = [mla.make_args(self.q[c], self.kv[c], self.out[c], self.lse[c], d_pos=self.d_pos)
                      for c in range(copies)]
@@ -171,7 +172,7 @@ class DenseBench:
 class SparseBench:
     """Sparse decode; `copies` distinct caches when one cache is below 3x L2."""
 
-    def __init__(self, name, copies, splits, pdl, seed=0):
+    def __init__(self, name, copies, splits, pdl, seed=0, variant=0):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
         d = torch.device("cuda")
@@ -189,7 +190,8 @@ class SparseBench:
         self.off = x.row_offset.to(d)
         self.out = [torch.empty(B, H, 512, device=d) for _ in range(copies)]
         self.lse = [torch.empty(B, H, device=d) for _ in range(copies)]
-        self.plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl)
+        self.plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl,
+                             variant=variant)
         self.scratch = mla.alloc_scratch(self.plan)
         self.args = [mla.make_args(self.q, self.kv[c], self.out[c], self.lse[c], indices=self.idx,
                                    cache_len=self.len, row_offset=self.off) for c in range(copies)]
@@ -210,7 +212,7 @@ class GraphBench:
     step appends a row to every layer's cache, runs partial + combine per layer,
     then advances d_pos once.  The layers together exceed 3x L2."""
 
-    def __init__(self, H, T0, steps, layers, splits, pdl, seed=0):
+    def __init__(self, H, T0, steps, layers, splits, pdl, seed=0, variant=0):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
         d = torch.device("cuda")
@@ -226,7 +228,8 @@ class GraphBench:
         self.d_pos0 = self.d_pos.clone()
         self.out = [torch.empty(steps, 1, H, 512, device=d) for _ in range(layers)]
         self.lse = [torch.empty(steps, 1, H, device=d) for _ in range(layers)]
-        self.plan = mla.plan(batch=1, heads=H, max_ctx=T0 + steps, scale=g.scale, splits=splits, pdl=pdl)
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=T0 + steps, scale=g.scale, splits=splits, pdl=pdl,
+                             variant=variant)
         self.scratch = mla.alloc_scratch(self.plan)
         self.args = [[mla.make_args(self.q[k], self.kv[l], self.out[l][k], self.lse[l][k], d_pos=self.d_pos)
                       for k in range(steps)] for l in range(layers)]
@@ -368,7 +371,7 @@ def run_ours(args, rank, world):
     T = 8192
     H = 16
     copies = copies_for(T * ROW_BYTES)
-    bench = DenseBench(T, H, copies, args.splits, bool(args.pdl))
+    bench = DenseBench(T, H, copies, args.splits, bool(args.pdl), variant=args.variant)
     g = capture(bench.call, copies)
     gp = capture(bench.partial, copies)
     # choose K for ~2 s of timed work unless given
@@ -397,7 +400,8 @@ def run_ours(args, rank, world):
     t_part = time_graph(gp, max(10, steps // 2), warm) / (max(10, steps // 2) * copies)
     part_bytes = T * ROW_BYTES + H * 576 * 2 + 4      # KV rows + q + d_pos read by the partial kernel
     achieved = part_bytes / t_part / 1e9
-    traffic = ncu_traffic("mla_partial_mma_kernel", "dense_t8192")
+    kname = "mla_partial_tc_kernel" if bench.plan.variant == 2 else "mla_partial_mma_kernel"
+    traffic = ncu_traffic(kname, "dense_t8192")
     reps = per_rep_times(g, 20)
     per_call_reps = [r / copies * 1e6 for r in reps]
     clocks = clk.summary()
@@ -408,6 +412,7 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "dense_t8192", "batch": 1, "heads": H, "d_latent": 512, "d_rope": 64,
                    "context": T, "splits": bench.plan.splits, "pdl": bool(args.pdl),
+                   "kernel": "tcgen05" if bench.plan.variant == 2 else "warp-mma",
                    "calls_per_step": copies,
                    "l2": f"inputs larger than L2: {copies} distinct caches x {T * ROW_BYTES / 1e6:.2f} MB "
                          f"= {copies * T * ROW_BYTES / 1e6:.0f} MB (> 3x L2 {l2_bytes() / 1e6:.0f} MB)",
@@ -419,7 +424,7 @@ def run_ours(args, rank, world):
         "frac_of_roofline": round(bench.alg_bytes / (P["hbm_gbs"] * 1e9) / (us_call * 1e-6), 4),
         "frac_of_roofline_8tbs": round(bench.alg_bytes / 8e12 / (us_call * 1e-6), 4),
         "alg_bytes_per_call": bench.alg_bytes,
-        "roofline": {"kernel": "mla_partial_mma_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": P["hbm_gbs"], "peak_source": P["source"] + " (burst copy)", "unit": "GB/s",
                      "frac": round(achieved / P["hbm_gbs"], 4), "traffic": traffic,
                      "alg_bytes_per_launch": part_bytes, "us_per_launch": round(t_part * 1e6, 4)},
@@ -494,27 +499,29 @@ def write_details(args, P):
         log(json.dumps(r))
 
     for T in (256, 8192, 16384, 32768, 65536, 131072):
-        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl))
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
         us, usp, reps = time_bench(b)
         entry(f"dense_h16_t{T}", b, us, usp, reps)
         del b
     for s in (1, 2, 4, 8, 16, 32, 64, 128):
-        b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), s, bool(args.pdl))
+        b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), s, bool(args.pdl), variant=args.variant)
         us, usp, reps = time_bench(b)
         entry("dense_t8192_split_sweep", b, us, usp, reps)
         del b
     # a call touches only its gathered rows: enough distinct caches that those exceed 3x L2
-    b = SparseBench("sparse_k2048", copies_for(2048 * ROW_BYTES), args.splits, bool(args.pdl))
+    b = SparseBench("sparse_k2048", copies_for(2048 * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
     us, usp, reps = time_bench(b)
     entry("sparse_k2048", b, us, usp, reps)
     del b
     torch.cuda.empty_cache()
-    b = SparseBench("sparse_b64", copies_for(64 * 2048 * ROW_BYTES), args.splits, bool(args.pdl))
+    b = SparseBench("sparse_b64", copies_for(64 * 2048 * ROW_BYTES), args.splits, bool(args.pdl),
+                    variant=args.variant)
     us, usp, reps = time_bench(b, reps=50)
     entry("sparse_b64", b, us, usp, reps)
     del b
     torch.cuda.empty_cache()
-    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, bool(args.pdl))
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, bool(args.pdl),
+                    variant=args.variant)
     us, _, reps = time_graph_bench(gb)
     tensor_us = gb.flops / (P["bf16_tflops_sustained"] * 1e12) * 1e6
     entry("graph_h128", gb, us, None, reps,
@@ -532,12 +539,14 @@ def ncu_case(args):
     from decode_attention_mla_gb300 import build as mla_build
     mla_build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    if args.ncu_case == "dense_t8192":
-        b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), args.splits, bool(args.pdl))
+    if args.ncu_case.startswith("dense_t"):
+        T = int(args.ncu_case[len("dense_t"):])
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
     elif args.ncu_case == "sparse_k2048":
-        b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl))
+        b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl),
+                        variant=args.variant)
     else:
-        b = SparseBench("sparse_b64", 1, args.splits, bool(args.pdl))
+        b = SparseBench("sparse_b64", 1, args.splits, bool(args.pdl), variant=args.variant)
     for c in range(args.calls):
         b.call(c % b.copies)
     torch.cuda.synchronize()
@@ -552,11 +561,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=int(os.environ.get("MLA_DECODE_SPLITS", "0")))
     ap.add_argument("--pdl", type=int, default=int(os.environ.get("MLA_DECODE_PDL", "1")))
+    ap.add_argument("--variant", type=int, default=int(os.environ.get("MLA_DECODE_VARIANT", "0")),
+                    help="0 = auto (tcgen05), 1 = warp-MMA kernel, 2 = tcgen05 kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--details", default=None)
-    ap.add_argument("--ncu-case", default=None, choices=["dense_t8192", "sparse_k2048", "sparse_b64"],
-                    help="profiling helper: run --calls eager calls of one workload and exit (no JSON)")
+    ap.add_argument("--ncu-case", default=None,
+                    help="profiling helper: dense_t<T> | sparse_k2048 | sparse_b64: run --calls eager calls of "
+                         "that workload and exit (no JSON)")
     ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

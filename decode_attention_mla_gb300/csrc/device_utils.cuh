@@ -11,6 +11,9 @@ namespace mla {
 // A bounded wait gives up after this long and reports MLA_EDEVICE through the
 // status word instead of spinning forever.
 constexpr unsigned long long kWaitTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2 s
+// The same bound in SM clock cycles (about 2 s at 2 GHz; longer at lower
+// clocks): waits count cycles, which are cheap to read, not the global timer.
+constexpr long long kWaitTimeoutCycles = 4000ll * 1000ll * 1000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,15 +62,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Returns false if
-// the CTA-wide abort flag is raised or the time limit passes.
+// the CTA-wide abort flag is raised or the time limit passes.  The limit is
+// checked every 256 polls against the SM cycle counter (reading the global
+// timer on every wait would put its latency on every hand-off).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
+    long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0u) {
+        if ((i & 255u) == 0u) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitTimeoutCycles) {
+                return false;
+            }
         }
     }
 }
@@ -102,6 +112,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Barrier that also ORs a predicate over the participating threads: every
+// thread gets the same answer, so they can leave a loop together.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 // ---- warp-level bf16 MMA (m16n8k16, fp32 accumulate) ---------------------
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -120,6 +144,13 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
+}
+// 2^x with the MUFU instruction (PTX ex2.approx.ftz.f32: relative error about
+// 2^-22; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
     uint32_t v;

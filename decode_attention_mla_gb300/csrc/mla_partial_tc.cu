@@ -20,7 +20,7 @@
 // side along N (~16 significant bits of P in one MMA); O = O_hi + O_lo at the
 // end.  Scores and O live in tensor memory (fp32).
 //
-// Warp roles (288 threads):
+// Warp roles (320 threads):
 //   warps 0-3  producer: TMA tiled loads of the dense tile (9 boxes of 80 rows,
 //              rows past the cache zero-filled by the TMA unit) or, for the
 //              sparse top-k gather ("The Commit That Changed Direction"),
@@ -33,7 +33,8 @@
 //              head's max grows by more than 2^8, so p <= 256); writes P as
 //              the bf16 pair; at the end of an item reads O from tensor memory
 //              and writes the partial.
-//   warp 8     MMA issue (one thread) and tensor-memory allocation.
+//   warp 8     score MMA issue and tensor-memory allocation; warp 9 P . V
+//              MMA issue.
 // Every wait is bounded (MLA_EDEVICE in the status word on a timeout); the
 // CTA drains its copies and its MMAs and frees its tensor memory before it
 // exits.  No floating-point atomics: results are a pure function of the
@@ -60,8 +61,9 @@ constexpr int kPAtomBytes = kPVHeads * 128;             // one 64-row K atom of 
 constexpr int kPBytes = 2 * kPAtomBytes;                // 80 rows need two K atoms
 constexpr int kProducerThreads = 128;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kMmaWarp = 8;
-constexpr int kThreads = 288;
+constexpr int kMmaWarp = 8;                             // QK issue + TMEM allocation
+constexpr int kPvWarp = 9;                              // P . V issue (its own warp: no divergent waits)
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns 16*buf
 constexpr uint32_t kTmemO = 32;                         // O^T block j at 32 + 32j: hi 0..15, lo 16..31
@@ -75,11 +77,12 @@ struct __align__(1024) SharedStorage {
     uint8_t kv[2][kTileBytes];            // double-buffered tile (chunk c of buffer b at kv[b] + c*kChunkBytes)
     uint8_t q[kChunks * kQChunkBytes];    // Q^T: also absorbs the M=128 over-read of the last chunk
     uint8_t p[2][kPBytes];                // [P_hi | P_lo]^T, K-major, per tile buffer
-    float red_max[2][4][16];
-    float red_sum[2][4][16];
+    alignas(16) float red_max[2][4][16];
+    alignas(16) float red_sum[2][4][16];
     int valid[2][kTileRows];
+    long long rowid[2][kTileRows];        // sparse: the tile's absolute cache rows (-1 = masked)
     uint64_t full[2], empty[2], s_full[2], p_full[2], o_done[2];
-    uint64_t q_full, q_empty, o_free, bar_max[2], bar_sum[2], mma_done;
+    uint64_t q_full, q_empty, o_free, bar_max[2], bar_sum[2], mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -130,28 +133,75 @@ __device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* statu
     if (status) atomicCAS(status, 0, static_cast<int>(MLA_EDEVICE));
 }
 
+// A cursor over this CTA's tiles in order: (item, tile k within it, global
+// tile number g).
+struct Cursor {
+    int item, k, g;
+    bool valid;
+    Item it;
+};
+
+__device__ __forceinline__ void cursor_next_item(const PartialParams& p, Cursor& c) {
+    for (int i = c.item + static_cast<int>(gridDim.x); i < p.n_items; i += gridDim.x) {
+        const Item it = decode_item(p, i);
+        if (it.n_tiles > 0) {
+            c.item = i;
+            c.it = it;
+            c.k = 0;
+            c.valid = true;
+            return;
+        }
+    }
+    c.valid = false;
+}
+__device__ __forceinline__ void cursor_init(const PartialParams& p, Cursor& c) {
+    c.item = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+    c.g = 0;
+    c.k = 0;
+    cursor_next_item(p, c);
+}
+__device__ __forceinline__ void cursor_step(const PartialParams& p, Cursor& c) {
+    ++c.g;
+    if (++c.k == c.it.n_tiles) cursor_next_item(p, c);
+}
+
 // ============================== producer ==================================
+// Dense: one thread issues every TMA (the other producer threads do nothing
+// and wait at the final barrier, so they take no issue slots from the
+// softmax warps); rows past the slice or the cache are masked by the softmax.
+// Sparse: thread 0 alone polls the barriers and a hardware barrier releases
+// the 128 gather threads; every thread reaches every hardware barrier, also
+// when a wait runs out (then all of them leave together).
 __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int t) {
+    if (!p.sparse && t != 0) return;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_normal();
+    // L2 prefetch runs two tiles ahead of the shared-memory loads: shared memory
+    // holds two tiles, L2 the next two in flight
+    Cursor pf;
+    cursor_init(p, pf);
+    for (int i = 0; i < 2 && pf.valid; ++i) cursor_step(p, pf);
     int g = 0;
     int q_loads = 0;
     int q_key = -1;
-    bool ok = true;
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+    // `stop` is uniform over the producer threads (sparse: agreed at a barrier)
+    bool stop = false;
+    for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
         const Item it = decode_item(p, item);
         if (it.n_tiles == 0) continue;
         const int key = it.b * p.n_groups + it.hg;
-        if (key != q_key) {
-            if (q_loads > 0 && !mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
+        const bool new_q = key != q_key;
+        if (new_q) {
             if (t == 0) {
-                mbar_arrive_expect_tx(&sh.q_full, kChunks * kQChunkBytes);
-                const int y = it.b * p.heads + it.hg * kHeadGroup;
+                if (q_loads > 0 && !mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
+                    raise_device_error(sh, p.status);
+                } else {
+                    mbar_arrive_expect_tx(&sh.q_full, kChunks * kQChunkBytes);
+                    const int y = it.b * p.heads + it.hg * kHeadGroup;
 #pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) tma_load_2d(sh.q + c * kQChunkBytes, &maps.q, 64 * c, y, &sh.q_full, pol_q);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_2d(sh.q + c * kQChunkBytes, &maps.q, 64 * c, y, &sh.q_full, pol_q);
+                }
             }
             q_key = key;
             ++q_loads;
@@ -159,66 +209,76 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
         const int seg_len = p.sparse ? p.cache_len[it.b] : 0;
         for (int k = 0; k < it.n_tiles; ++k, ++g) {
             const int buf = g & 1;
-            if (g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
+            if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
+                raise_device_error(sh, p.status);
             const long long r0 = it.e0 + static_cast<long long>(k) * kTileRows;
             const int rows = rows_in_tile(it, k);
             if (!p.sparse) {
-                if (t < kTileRows) {
-                    const long long row = it.base + r0 + t;
-                    sh.valid[buf][t] = (t < rows && row >= 0 && row < p.kv_rows) ? 1 : 0;
-                }
-                if (t == 0) {
-                    mbar_arrive_expect_tx(&sh.full[buf], kTileBytes);
-                    const int y = static_cast<int>(it.base + r0);
+                stop = sh.abort_flag != 0;
+                if (stop) break;
+                mbar_arrive_expect_tx(&sh.full[buf], kTileBytes);
+                const int y = static_cast<int>(it.base + r0);
 #pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_2d(sh.kv[buf] + c * kChunkBytes, &maps.kv, 64 * c, y, &sh.full[buf], pol_kv);
-                } else {
-                    mbar_arrive(&sh.full[buf]);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_2d(sh.kv[buf] + c * kChunkBytes, &maps.kv, 64 * c, y, &sh.full[buf], pol_kv);
+                if (pf.valid) {
+                    const int yp = static_cast<int>(pf.it.base + pf.it.e0 + static_cast<long long>(pf.k) * kTileRows);
+#pragma unroll 1
+                    for (int c = 0; c < kChunks; ++c) tma_prefetch_2d(&maps.kv, 64 * c, yp);
                 }
             } else {
+                // the buffer is free, or some thread saw the CTA abort
+                stop = named_barrier_or(1, kProducerThreads, sh.abort_flag != 0);
+                if (stop) break;
+                // the tile's row ids, resolved once into shared memory
                 const int* idx = p.indices + static_cast<long long>(it.b) * p.topk + r0;
                 if (t < kTileRows) {
-                    bool v = false;
+                    long long row = -1;
                     if (t < rows) {
                         const int id = idx[t];
-                        v = id >= 0 && id < seg_len && it.base + id >= 0 && it.base + id < p.kv_rows;
+                        if (id >= 0 && id < seg_len && it.base + id >= 0 && it.base + id < p.kv_rows) row = it.base + id;
                     }
-                    sh.valid[buf][t] = v ? 1 : 0;
+                    sh.rowid[buf][t] = row;
+                    sh.valid[buf][t] = row >= 0 ? 1 : 0;
                 }
+                named_barrier_sync(1, kProducerThreads);      // row ids ready
                 // rows past the tile's last k-step are never read by P . V; masked
                 // rows inside it must hold zeros (they meet p = 0)
                 const int rows_read = (rows + 15) & ~15;
                 const uint32_t dst0 = smem_u32(sh.kv[buf]);
+                const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
+                const long long stride_bytes = p.row_stride * 2;
 #pragma unroll 4
                 for (int piece = t; piece < rows_read * 72; piece += kProducerThreads) {
                     const int r = piece / 72;
                     const int u = piece - r * 72;
                     const int c = u >> 3;
                     const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
-                    bool v = false;
-                    long long row = 0;
-                    if (r < rows) {
-                        const int id = idx[r];
-                        row = it.base + id;
-                        v = id >= 0 && id < seg_len && row >= 0 && row < p.kv_rows;
-                    }
-                    if (v)
-                        cp_async_16(dst, reinterpret_cast<const uint8_t*>(p.kv + row * p.row_stride) + u * 16);
+                    const long long row = sh.rowid[buf][r];
+                    if (row >= 0)
+                        cp_async_16(dst, kvb + row * stride_bytes + u * 16);
                     else
                         st_shared_v4_zero(dst);
                 }
                 cp_async_commit();
+                if (pf.valid && t < kTileRows) {
+                    // rows of the tile two ahead into L2 while this tile's copies land
+                    const long long pr0 = pf.it.e0 + static_cast<long long>(pf.k) * kTileRows;
+                    if (t < rows_in_tile(pf.it, pf.k)) {
+                        const int id = p.indices[static_cast<long long>(pf.it.b) * p.topk + pr0 + t];
+                        const int plen = p.cache_len[pf.it.b];
+                        const long long prow = pf.it.base + id;
+                        if (id >= 0 && id < plen && prow >= 0 && prow < p.kv_rows)
+                            bulk_prefetch_l2(kvb + prow * stride_bytes, kRowBytes);
+                    }
+                }
                 cp_async_wait_group<0>();
                 fence_proxy_async_smem();
                 mbar_arrive(&sh.full[buf]);
             }
+            if (pf.valid) cursor_step(p, pf);
         }
     }
-    if (!ok && t == 0) raise_device_error(sh, p.status);
     // Never retire the CTA with copies into its shared memory in flight.
     if (t == 0) {
         volatile int never = 0;
@@ -231,53 +291,26 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
 }
 
 // ============================== MMA issue ==================================
-__device__ void mma_issuer(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
+// Two threads in two warps issue the MMAs (the tensor pipe overlaps
+// instructions from different issuers, and a waiting issuer does not stall
+// the other): the scores of each tile, and the P . V products.  QK of tile g waits for its tile and for the softmax of
+// tile g-2 (the owner of its score buffer); P . V of tile g waits for the
+// softmax of tile g, and the first one of an item for the previous item's
+// epilogue.
+__device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
     const uint32_t idesc_qk = make_idesc_bf16(128, kHeadGroup, 0, 0);
-    const uint32_t idesc_pv = make_idesc_bf16(128, kPVHeads, 1, 0);
-    const uint32_t kv0 = smem_u32(sh.kv[0]);
-    const uint32_t q0 = smem_u32(sh.q);
-    const uint32_t p0 = smem_u32(sh.p[0]);
     // K-major 128-byte-swizzled operands: 8-row groups 1024 bytes apart
-    const uint64_t kv_desc0 = make_sdesc(kv0, 16, 1024, kLayoutSw128);
-    const uint64_t q_desc0 = make_sdesc(q0, 16, 1024, kLayoutSw128);
-    const uint64_t p_desc0 = make_sdesc(p0, 16, 1024, kLayoutSw128);
-    // V^T is MN-major: 64-feature atoms one chunk apart, 8-row groups 1024 apart
-    const uint64_t v_desc0 = make_sdesc(kv0, kChunkBytes, 1024, kLayoutSw128);
-    int g = 0;
+    const uint64_t kv_desc0 = make_sdesc(smem_u32(sh.kv[0]), 16, 1024, kLayoutSw128);
+    const uint64_t q_desc0 = make_sdesc(smem_u32(sh.q), 16, 1024, kLayoutSw128);
+    Cursor qc;
+    cursor_init(p, qc);
     int q_loads = 0;
-    int items_done = 0;
     int cur_key = -1;
     bool ok = true;
-
-    auto issue_pv = [&](int gg, const Item& it, int k, bool first_of_item) -> bool {
-        const int buf = gg & 1;
-        if (!mbar_wait_bounded(&sh.p_full[buf], (gg >> 1) & 1, &sh.abort_flag)) return false;
-        if (first_of_item && items_done > 0 &&
-            !mbar_wait_bounded(&sh.o_free, (items_done - 1) & 1, &sh.abort_flag))
-            return false;
-        tc_fence_after_sync();
-        const int ksteps = (rows_in_tile(it, k) + 15) >> 4;
-        const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
-        const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * kPBytes) >> 4);
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll 1
-            for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t a = vb + ((2u * j * kChunkBytes + kk * 2048u) >> 4);
-                const uint64_t bd = pb + ((static_cast<uint32_t>(kk >> 2) * kPAtomBytes + (kk & 3) * 32u) >> 4);
-                umma_bf16(tmem + kTmemO + 32 * j, a, bd, idesc_pv, (first_of_item && kk == 0) ? 0u : 1u);
-            }
-        }
-        umma_commit(&sh.empty[buf]);
-        umma_commit(&sh.o_done[buf]);
-        return true;
-    };
-
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, item);
-        if (it.n_tiles == 0) continue;
-        const int key = it.b * p.n_groups + it.hg;
-        if (key != cur_key) {
+    while (qc.valid && ok) {
+        const int key = qc.it.b * p.n_groups + qc.it.hg;
+        const int buf = qc.g & 1;
+        if (qc.k == 0 && key != cur_key) {
             if (!mbar_wait_bounded(&sh.q_full, q_loads & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
@@ -285,48 +318,94 @@ __device__ void mma_issuer(const PartialParams& p, SharedStorage& sh, uint32_t t
             ++q_loads;
             cur_key = key;
         }
-        const int first_g = g;
-        for (int k = 0; k < it.n_tiles; ++k, ++g) {
-            const int buf = g & 1;
-            if (!mbar_wait_bounded(&sh.full[buf], (g >> 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const uint64_t kb = kv_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
-#pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t off = (c * kChunkBytes + kk * 32u) >> 4;
-                    const uint32_t qoff = (c * kQChunkBytes + kk * 32u) >> 4;
-                    umma_bf16(tmem + kTmemS + 16 * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
-                }
-            }
-            umma_commit(&sh.s_full[buf]);
-            if (k > 0 && !issue_pv(g - 1, it, k - 1, k - 1 == 0)) {
-                ok = false;
-                break;
-            }
-        }
-        if (!ok) break;
-        if (!issue_pv(g - 1, it, it.n_tiles - 1, it.n_tiles == 1)) {
+        if (!mbar_wait_bounded(&sh.full[buf], (qc.g >> 1) & 1, &sh.abort_flag) ||
+            (qc.g >= 2 && !mbar_wait_bounded(&sh.p_full[buf], ((qc.g >> 1) - 1) & 1, &sh.abort_flag))) {
             ok = false;
             break;
         }
-        (void)first_g;
-        ++items_done;
-        // release the query tile once its last user has been issued, if the
-        // next item of this CTA needs a different one
-        Item nx;
-        const int ni = next_busy_item(p, item, &nx);
-        if (ni >= 0 && nx.b * p.n_groups + nx.hg != key) umma_commit(&sh.q_empty);
+        tc_fence_after_sync();
+        const uint64_t kb = kv_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
+        // fully unrolled: every descriptor is a constant offset from kb / q_desc0,
+        // so the issuing thread keeps pace with the tensor pipe
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t off = (c * kChunkBytes + kk * 32u) >> 4;
+                const uint32_t qoff = (c * kQChunkBytes + kk * 32u) >> 4;
+                umma_bf16(tmem + kTmemS + 16 * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
+            }
+        }
+        umma_commit(&sh.s_full[buf]);
+        if (qc.k == qc.it.n_tiles - 1) {
+            // last user of this query tile: release it if the next item needs another
+            Item nx;
+            const int ni = next_busy_item(p, qc.item, &nx);
+            if (ni >= 0 && nx.b * p.n_groups + nx.hg != key) umma_commit(&sh.q_empty);
+        }
+        cursor_step(p, qc);
     }
     if (!ok) raise_device_error(sh, p.status);
-    // all MMAs complete before the CTA frees its tensor memory
-    umma_commit(&sh.mma_done);
+    umma_commit(&sh.mma_done[0]);
     volatile int never = 0;
-    if (!mbar_wait_bounded(&sh.mma_done, 0, &never)) raise_device_error(sh, p.status);
+    if (!mbar_wait_bounded(&sh.mma_done[0], 0, &never)) raise_device_error(sh, p.status);
+}
+
+__device__ void mma_issue_pv(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
+    const uint32_t idesc_pv = make_idesc_bf16(128, kPVHeads, 1, 0);
+    const uint64_t p_desc0 = make_sdesc(smem_u32(sh.p[0]), 16, 1024, kLayoutSw128);
+    // V^T is MN-major: 64-feature atoms one chunk apart, 8-row groups 1024 apart
+    const uint64_t v_desc0 = make_sdesc(smem_u32(sh.kv[0]), kChunkBytes, 1024, kLayoutSw128);
+    Cursor pc;
+    cursor_init(p, pc);
+    int items_done = 0;
+    bool ok = true;
+    while (pc.valid && ok) {
+        const int buf = pc.g & 1;
+        const bool first = pc.k == 0;
+        if (!mbar_wait_bounded(&sh.p_full[buf], (pc.g >> 1) & 1, &sh.abort_flag) ||
+            (first && items_done > 0 && !mbar_wait_bounded(&sh.o_free, (items_done - 1) & 1, &sh.abort_flag))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        const int ksteps = (rows_in_tile(pc.it, pc.k) + 15) >> 4;
+        const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
+        const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * kPBytes) >> 4);
+        const uint32_t acc0 = first ? 0u : 1u;
+        if (ksteps == kTileRows / 16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint64_t a = vb + ((2u * j * kChunkBytes + kk * 2048u) >> 4);
+                    const uint64_t bd = pb + ((static_cast<uint32_t>(kk >> 2) * kPAtomBytes + (kk & 3) * 32u) >> 4);
+                    umma_bf16(tmem + kTmemO + 32 * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    if (kk < ksteps) {
+                        const uint64_t a = vb + ((2u * j * kChunkBytes + kk * 2048u) >> 4);
+                        const uint64_t bd =
+                            pb + ((static_cast<uint32_t>(kk >> 2) * kPAtomBytes + (kk & 3) * 32u) >> 4);
+                        umma_bf16(tmem + kTmemO + 32 * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                    }
+                }
+            }
+        }
+        umma_commit(&sh.empty[buf]);
+        umma_commit(&sh.o_done[buf]);
+        if (pc.k == pc.it.n_tiles - 1) ++items_done;
+        cursor_step(p, pc);
+    }
+    if (!ok) raise_device_error(sh, p.status);
+    umma_commit(&sh.mma_done[1]);
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&sh.mma_done[1], 0, &never)) raise_device_error(sh, p.status);
 }
 
 // ============================== softmax warps ==============================
@@ -411,9 +490,9 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         for (int k = 0; k < it.n_tiles; ++k, ++g) {
             const int buf = g & 1;
             const int rows = rows_in_tile(it, k);
-            // the tile's row flags come from the producer: acquire its barrier too
+            // sparse tiles' row flags come from the producer: acquire its barrier too
             if (!mbar_wait_bounded(&sh.s_full[buf], (g >> 1) & 1, &sh.abort_flag) ||
-                !mbar_wait_bounded(&sh.full[buf], (g >> 1) & 1, &sh.abort_flag)) {
+                (p.sparse && !mbar_wait_bounded(&sh.full[buf], (g >> 1) & 1, &sh.abort_flag))) {
                 ok = false;
                 break;
             }
@@ -425,7 +504,13 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
 #pragma unroll
                 for (int h = 0; h < 16; ++h) s[h] = 0.f;
             }
-            const bool row_ok = t < rows && sh.valid[buf][t] != 0;
+            bool row_ok;
+            if (p.sparse) {
+                row_ok = t < rows && sh.valid[buf][t] != 0;
+            } else {
+                const long long row = it.base + it.e0 + static_cast<long long>(k) * kTileRows + t;
+                row_ok = t < rows && row >= 0 && row < p.kv_rows;
+            }
 #pragma unroll
             for (int h = 0; h < 16; ++h) s[h] = row_ok ? s[h] * p.scale_log2 : -INFINITY;
 
@@ -442,40 +527,50 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             }
             float alpha[16];
             bool rescale = false;
+            {
+                const float4* rm = reinterpret_cast<const float4*>(&sh.red_max[buf][0][0]);
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                const float tmax = fmaxf(fmaxf(sh.red_max[buf][0][h], sh.red_max[buf][1][h]),
-                                         fmaxf(sh.red_max[buf][2][h], sh.red_max[buf][3][h]));
-                float ref = m_ref[h];
-                alpha[h] = 1.f;
-                if (tmax > -INFINITY && (ref == -INFINITY || tmax > ref + kRescaleLog2)) {
-                    if (ref != -INFINITY && l_run[h] > 0.f) {
-                        alpha[h] = exp2f(ref - tmax);
-                        rescale = true;
+                for (int h4 = 0; h4 < 4; ++h4) {
+                    const float4 a = rm[h4], b = rm[4 + h4], c = rm[8 + h4], d = rm[12 + h4];
+                    const float tm[4] = {fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x)), fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y)),
+                                         fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z)), fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w))};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        // branch-free: the reference moves to the tile max when that
+                        // exceeds it by more than 2^8 (or nothing was referenced yet)
+                        const int h = 4 * h4 + i;
+                        const float tmax = tm[i];
+                        const float ref = m_ref[h];
+                        const bool move = tmax > ref + kRescaleLog2;          // false while tmax == -inf
+                        const float nref = move ? tmax : ref;
+                        const bool scale_o = move && l_run[h] > 0.f;            // l > 0 implies ref finite
+                        const float a = ex2_approx(scale_o ? ref - nref : 0.f);
+                        alpha[h] = a;
+                        rescale |= scale_o;
+                        m_ref[h] = nref;
                     }
-                    ref = tmax;
                 }
-                m_ref[h] = ref;
             }
 
             // ---- probabilities, written as the bf16 pair [P_hi | P_lo]^T --------
             float pr[16];
 #pragma unroll
-            for (int h = 0; h < 16; ++h) pr[h] = (row_ok && m_ref[h] > -INFINITY) ? exp2f(s[h] - m_ref[h]) : 0.f;
+            for (int h = 0; h < 16; ++h) pr[h] = (row_ok && m_ref[h] > -INFINITY) ? ex2_approx(s[h] - m_ref[h]) : 0.f;
             if (g >= 2 && !mbar_wait_bounded(&sh.o_done[buf], ((g >> 1) - 1) & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
             }
             if (t < kTileRows) {
-                const uint32_t pbase = smem_u32(sh.p[buf]) + (t >> 6) * kPAtomBytes;
-                const uint32_t byte = 2u * (t & 63);
+                // row t of head h: line h (hi) / 16 + h (lo) of the K atom t / 64, byte 2 * (t % 64)
+                const uint32_t pbase = smem_u32(sh.p[buf]) + (t >> 6) * kPAtomBytes + 2u * (t & 7);
+                const uint32_t unit = static_cast<uint32_t>((t & 63) >> 3);
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const __nv_bfloat16 hi = __float2bfloat16_rn(pr[h]);
                     const __nv_bfloat16 lo = __float2bfloat16_rn(pr[h] - __bfloat162float(hi));
-                    const int vh = h, vl = 16 + h;
-                    st_shared_u16(pbase + (vh >> 3) * 1024 + sw128_offset(vh & 7, byte), __bfloat16_as_ushort(hi));
-                    st_shared_u16(pbase + (vl >> 3) * 1024 + sw128_offset(vl & 7, byte), __bfloat16_as_ushort(lo));
+                    const uint32_t a = pbase + (h >> 3) * 1024 + (h & 7) * 128 + ((unit ^ (h & 7)) << 4);
+                    st_shared_u16(a, __bfloat16_as_ushort(hi));
+                    st_shared_u16(a + 2048, __bfloat16_as_ushort(lo));
                 }
             }
             // ---- row sums -------------------------------------------------------
@@ -488,11 +583,16 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                 ok = false;
                 break;
             }
+            {
+                const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[buf][0][0]);
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                const float ts = ((sh.red_sum[buf][0][h] + sh.red_sum[buf][1][h]) + sh.red_sum[buf][2][h]) +
-                                 sh.red_sum[buf][3][h];
-                l_run[h] = l_run[h] * alpha[h] + ts;
+                for (int h4 = 0; h4 < 4; ++h4) {
+                    const float4 a = rs[h4], b = rs[4 + h4], c = rs[8 + h4], d = rs[12 + h4];
+                    l_run[4 * h4 + 0] = l_run[4 * h4 + 0] * alpha[4 * h4 + 0] + (((a.x + b.x) + c.x) + d.x);
+                    l_run[4 * h4 + 1] = l_run[4 * h4 + 1] * alpha[4 * h4 + 1] + (((a.y + b.y) + c.y) + d.y);
+                    l_run[4 * h4 + 2] = l_run[4 * h4 + 2] * alpha[4 * h4 + 2] + (((a.z + b.z) + c.z) + d.z);
+                    l_run[4 * h4 + 3] = l_run[4 * h4 + 3] * alpha[4 * h4 + 3] + (((a.w + b.w) + c.w) + d.w);
+                }
             }
             // ---- rare: move O to the new reference --------------------------------
             if (rescale && g > first_g) {
@@ -575,8 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        prefetch_tensormap(&maps.kv);
+        prefetch_tensormap(&maps.q);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.full[i], kProducerThreads);
+            mbar_init(&sh.full[i], p.sparse ? kProducerThreads : 1);
             mbar_init(&sh.empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
             mbar_init(&sh.p_full[i], 128);
@@ -587,7 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, 1);
         mbar_init(&sh.o_free, 128);
-        mbar_init(&sh.mma_done, 1);
+        mbar_init(&sh.mma_done[0], 1);
+        mbar_init(&sh.mma_done[1], 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }
@@ -607,8 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
         producer(maps, p, sh, threadIdx.x);
     } else if (warp < kMmaWarp) {
         softmax_warps(p, sh, tmem, warp - kSoftmaxWarp0, lane);
-    } else if (lane == 0) {
-        mma_issuer(p, sh, tmem);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issue_qk(p, sh, tmem);
+    } else if (warp == kPvWarp && lane == 0) {
+        mma_issue_pv(p, sh, tmem);
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -28,6 +28,8 @@ D_ROW = 576
 MAX_SPLITS = 256
 
 OK, EINVAL, EUNSUPPORTED, ESCRATCH, EALIGN, ECUDA, EDEVICE, ENOTREADY = 0, -1, -2, -3, -4, -5, -6, -7
+ESTATICLIMIT = -8
+STATIC_SCRATCH_BYTES = 8 << 20      # scratch of mla_decode_forward_static
 
 
 class Shape(ctypes.Structure):
@@ -71,7 +73,7 @@ _lib = None
 
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
-            "mla_decode_strerror")
+            "mla_decode_strerror", "mla_decode_forward_static")
 
 
 def lib():
@@ -93,6 +95,8 @@ def lib():
             fn = getattr(L, name)
             fn.restype = I
             fn.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P, SZ, P]
+        L.mla_decode_forward_static.restype = I
+        L.mla_decode_forward_static.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P]
         L.mla_decode_append.restype = I
         L.mla_decode_append.argtypes = [P, LL, LL, P, P, P, I, P]
         L.mla_decode_advance.restype = I
@@ -208,6 +212,15 @@ def forward(p: Plan, q, kv, out, lse, scratch, *, d_pos=None, row_offset=None, c
     a = make_args(q, kv, out, lse, d_pos=d_pos, row_offset=row_offset, cache_len=cache_len, indices=indices,
                   kv_rows=kv_rows, row_stride=row_stride)
     forward_args(p, a, scratch, stream)
+
+
+def forward_static(p: Plan, q, kv, out, lse, *, d_pos=None, row_offset=None, cache_len=None, indices=None,
+                   kv_rows=None, row_stride=None, stream=None) -> None:
+    """``mla_decode_forward_static``: as :func:`forward`, with the library's own 8 MiB static scratch."""
+    a = make_args(q, kv, out, lse, d_pos=d_pos, row_offset=row_offset, cache_len=cache_len, indices=indices,
+                  kv_rows=kv_rows, row_stride=row_stride)
+    _check(lib().mla_decode_forward_static(ctypes.byref(p), ctypes.byref(a), _stream(stream)),
+           "mla_decode_forward_static")
 
 
 def append(kv, new_rows, d_pos, *, row_offset=None, kv_rows=None, row_stride=None, stream=None) -> None:

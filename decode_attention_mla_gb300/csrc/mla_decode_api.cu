@@ -15,6 +15,7 @@
 namespace {
 
 constexpr int kPlanMagic = 0x4d4c4131;       // "MLA1"
+static_assert(mla::kStaticScratchBytes == MLA_STATIC_SCRATCH_BYTES, "static scratch size differs from the header");
 constexpr int kMaxDevices = 64;
 // The partial kernel is persistent with one CTA per SM: its 5-stage ring of
 // cache rows fills the shared memory.  The two-CTAs-per-SM target named in
@@ -364,6 +365,30 @@ int mla_decode_advance(int* d_pos, int batch, void* stream) {
     return launch_status(mla::launch_advance(d_pos, batch, false, static_cast<cudaStream_t>(stream)));
 }
 
+int mla_decode_forward_static(const mla_decode_plan_t* plan, const mla_decode_args* args, void* stream) {
+    int rc = check_plan(plan);
+    if (rc == MLA_OK) rc = check_args(plan, args);
+    if (rc != MLA_OK) return rc;
+    if (plan->scratch_bytes > mla::kStaticScratchBytes) return MLA_ESTATICLIMIT;
+    int dev = 0;
+    rc = current_device(&dev);
+    if (rc != MLA_OK) return rc;
+    void* scratch = mla::static_scratch_if_ready(dev);
+    if (!scratch) {
+        // first call on this device: look the array up (not while capturing)
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return MLA_ECUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return MLA_ENOTREADY;
+        if (mla::static_scratch_set_up(dev, &scratch) != cudaSuccess) return MLA_ECUDA;
+    }
+    rc = do_run(plan, args, scratch, mla::kStaticScratchBytes, stream);
+    if (rc != MLA_OK) return rc;
+    return do_combine(plan, args, scratch, mla::kStaticScratchBytes, stream);
+}
+
 int mla_decode_scratch_init(void* scratch, size_t scratch_bytes, void* stream) {
     if (!scratch || scratch_bytes == 0) return MLA_EINVAL;
     return launch_status(cudaMemsetAsync(scratch, 0, scratch_bytes, static_cast<cudaStream_t>(stream)));
@@ -379,6 +404,8 @@ const char* mla_decode_strerror(int status) {
         case MLA_ECUDA: return "CUDA runtime error";
         case MLA_EDEVICE: return "a kernel wait ran out of time (device status word set)";
         case MLA_ENOTREADY: return "kernels not prepared on this device; call mla_decode_plan before capture";
+        case MLA_ESTATICLIMIT:
+            return "plan scratch_bytes exceeds the 8 MiB static scratch of mla_decode_forward_static";
         default: return "unknown status";
     }
 }

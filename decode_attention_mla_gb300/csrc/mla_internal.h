@@ -17,6 +17,9 @@ constexpr int kStageRows = 32;                 // rows per pipeline stage (warp-
 constexpr int kTcTileRows = 80;                // rows per tile (tcgen05 partial kernel)
 constexpr int kHeadGroup = 16;                 // heads per CTA of the warp-MMA kernel
 constexpr int kCombineChunk = 128;             // features per combine CTA
+// Size of the library's own scratch array used by mla_decode_forward_static
+// (8 MiB: e.g. 16 heads x 256 slices x 2 KiB partial rows fits with room).
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 
 // Everything the split partial kernel needs; passed by value.
 struct PartialParams {
@@ -82,6 +85,11 @@ int partial_tc_block_threads();
 cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
 int combine_block_threads();
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
+
+// Static scratch (mla_static_scratch.cu): its address on `device` once set up
+// there (nullptr before), and the one-time set-up with `device` current.
+void* static_scratch_if_ready(int device);
+cudaError_t static_scratch_set_up(int device, void** out);
 cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_advance(int* d_pos, int batch, bool pdl, cudaStream_t stream);
 

@@ -69,7 +69,8 @@ typedef enum {
     MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 */
     MLA_ECUDA = -5,         /* the CUDA runtime reported an error for a launch or query */
     MLA_EDEVICE = -6,       /* a kernel's bounded wait ran out (see the scratch status word) */
-    MLA_ENOTREADY = -7      /* kernels not prepared on this device and the stream is capturing */
+    MLA_ENOTREADY = -7,     /* kernels not prepared on this device and the stream is capturing */
+    MLA_ESTATICLIMIT = -8   /* plan->scratch_bytes > MLA_STATIC_SCRATCH_BYTES (forward_static) */
 } mla_status;
 
 /* Problem description given to the planner. */
@@ -166,6 +167,34 @@ MLA_API int mla_decode_combine(const mla_decode_plan_t *plan, const mla_decode_a
 /* mla_decode_run followed by mla_decode_combine (two launches). */
 MLA_API int mla_decode_forward(const mla_decode_plan_t *plan, const mla_decode_args *args, void *scratch,
                        size_t scratch_bytes, void *stream);
+
+/* Size of the library's own scratch array used by mla_decode_forward_static. */
+#define MLA_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* mla_decode_forward without a caller scratch buffer and without allocating.
+ * The pages that define the method have no counterpart of this call: it
+ * exists for callers that may not allocate device memory.  The partial and
+ * combine kernels run exactly as in mla_decode_forward (same plan, same
+ * results bit for bit), but their scratch is an 8 MiB (MLA_STATIC_SCRATCH_BYTES)
+ * file-scope __device__ array of the library, one per device; the call makes
+ * no cudaMalloc/cudaFree or other allocating call.
+ *   - Set-up: the first call on a device looks the array's address up
+ *     (cudaGetSymbolAddress, with that device current, its return code
+ *     checked) and keeps it; make that first call before any stream capture
+ *     (a first call on a capturing stream returns MLA_ENOTREADY).
+ *   - Size: a plan whose scratch_bytes exceeds MLA_STATIC_SCRATCH_BYTES is
+ *     rejected with MLA_ESTATICLIMIT before anything is launched; use
+ *     mla_decode_forward with a caller buffer for such plans.
+ *   - Zero start: only the status word (offset 0) must start at zero; the
+ *     array is zero when the library's module is loaded.  A device-side
+ *     wait timeout sets it and nothing here clears it or reports it.  The
+ *     partial and LSE arrays need no initial value.
+ *   - Races: every call on a device shares the one array, so calls that can
+ *     overlap (on different streams, or from several host threads without
+ *     ordering) race on it and give wrong results; calls on one stream are
+ *     ordered and safe.
+ * Errors: as mla_decode_forward, minus MLA_ESCRATCH, plus MLA_ESTATICLIMIT. */
+MLA_API int mla_decode_forward_static(const mla_decode_plan_t *plan, const mla_decode_args *args, void *stream);
 
 /* Write the new token's cache row from device memory: for each request b,
  * copy new_rows[b] (bf16 [576]) to row base_b + d_pos[b] of kv, where base_b

@@ -127,6 +127,14 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
     return r != 0;
 }
 
+// Maximum of a float over the 32 lanes of the warp, in one instruction (the
+// result is the same on every lane; -inf is an ordinary value).
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // ---- warp-level bf16 MMA (m16n8k16, fp32 accumulate) ---------------------
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(

@@ -28,7 +28,7 @@ constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 3
 constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
 
 int variant_tile_rows(int v) { return v == kVariantTc ? mla::kTcTileRows : mla::kStageRows; }
-int variant_granule(int v) { return v == kVariantTc ? 16 : mla::kStageRows; }
+int variant_granule(int v) { return v == kVariantTc ? mla::kTcGranule : mla::kStageRows; }
 
 // cuTensorMapEncodeTiled, reached through the runtime (no link-time libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -48,15 +48,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return g_encode;
 }
 
-int encode_bf16_rows(CUtensorMap* map, const void* base, long long rows, long long row_stride_elems,
-                     uint32_t box_rows) {
+// Rank-3 view of bf16 rows of 576: {64 elements, rows, 9 chunks of 64} with
+// strides {row stride, 128 bytes}; a box {64, box_rows, box_chunks} lands in
+// shared memory as [chunk][row][64], 128-byte swizzled.
+int encode_bf16_row_chunks(CUtensorMap* map, const void* base, long long rows, long long row_stride_elems,
+                           uint32_t box_rows, uint32_t box_chunks) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return MLA_ECUDA;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLA_D_ROW), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_elems) * 2u};
-    const cuuint32_t box[2] = {64u, box_rows};
-    const cuuint32_t elem_strides[2] = {1u, 1u};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(MLA_D_ROW / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride_elems) * 2u, 128u};
+    const cuuint32_t box[3] = {64u, box_rows, box_chunks};
+    const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
@@ -214,10 +217,10 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
         // TMA coordinates are 32-bit: the cache must be addressable by them
         if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
         mla::TcMaps maps;
-        rc = encode_bf16_rows(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kTcTileRows);
+        rc = encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kTcTileRows, mla::kTcBoxChunks);
         if (rc == MLA_OK)
-            rc = encode_bf16_rows(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads, MLA_D_ROW,
-                                  mla::kHeadGroup);
+            rc = encode_bf16_row_chunks(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads,
+                                        MLA_D_ROW, mla::kHeadGroup, MLA_D_ROW / 64);
         if (rc != MLA_OK) return rc;
         return launch_status(mla::launch_partial_tc(maps, p, grid, pl->shape.pdl != 0, st));
     }

@@ -15,6 +15,7 @@ constexpr int kDRow = kDLatent + kDRope;       // 576 bf16 per cache row
 constexpr int kRowBytes = kDRow * 2;           // 1152
 constexpr int kStageRows = 32;                 // rows per pipeline stage (warp-MMA partial kernel)
 constexpr int kTcTileRows = 80;                // rows per tile (tcgen05 partial kernel)
+constexpr int kTcGranule = 16;                 // slice granule of the tcgen05 kernel (one MMA k-step)
 constexpr int kHeadGroup = 16;                 // heads per CTA of the warp-MMA kernel
 constexpr int kCombineChunk = 128;             // features per combine CTA
 // Size of the library's own scratch array used by mla_decode_forward_static
@@ -65,9 +66,13 @@ struct AppendParams {
     int batch;
 };
 
-// TMA descriptors of the tcgen05 kernel: the cache rows [kv_rows x 576] in
-// boxes of 64 x 80 and the queries [B*H x 576] in boxes of 64 x 16, both
-// with the 128-byte swizzle.
+// TMA descriptors of the tcgen05 kernel, both rank 3 with the 128-byte
+// swizzle: dimension 0 = 64 bf16 of a row (128 bytes), dimension 1 = rows
+// (stride: the row stride), dimension 2 = the 9 column chunks of a row
+// (stride 128 bytes).  One box lands as [chunk][row][64 bf16], the layout the
+// tensor cores read.  kv: boxes of 64 x 80 rows x 3 chunks (a third of a
+// tile); q: boxes of 64 x 16 heads x 9 chunks (the whole head group).
+constexpr int kTcBoxChunks = 3;
 struct TcMaps {
     CUtensorMap kv;
     CUtensorMap q;

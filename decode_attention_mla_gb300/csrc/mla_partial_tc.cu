@@ -10,9 +10,11 @@
 //
 // A slice is walked in tiles of 80 cache rows, double-buffered in shared
 // memory as 9 column chunks of [80 rows x 64 bf16] in the 128-byte-swizzled
-// layout the tensor cores read.  With the 16 heads of a group the products
-// are taken "swapped", so the long axis (cache rows, or latent features)
-// is the 128-wide M of the MMA and the 16 heads are N:
+// layout the tensor cores read; a tile arrives as three TMA boxes of three
+// chunks, each with its own barrier, so the score MMAs start on the first
+// third while the rest is in flight.  With the 16 heads of a group the
+// products are taken "swapped", so the long axis (cache rows, or latent
+// features) is the 128-wide M of the MMA and the 16 heads are N:
 //   S^T[rows x 16]   = K_tile[rows x 576] . Q^T           36 MMAs, M=128 (80 valid rows), N=16
 //   O^T[512 x 32]   += V_tile^T[512 x rows] . [P_hi | P_lo]^T
 //                                                          4 x 5 MMAs, M=128 features, N=32
@@ -20,25 +22,32 @@
 // side along N (~16 significant bits of P in one MMA); O = O_hi + O_lo at the
 // end.  Scores and O live in tensor memory (fp32).
 //
+// Online softmax in base 2 with a lazily moved reference m (per head, the
+// same in every thread): a tile whose scores all stay below m + 8 is turned
+// into probabilities at once (one barrier that ORs "some score is above");
+// only otherwise (the first tile of a slice, or a max that grew by more than
+// 2^8) the tile max is taken (warp max instructions and a four-warp exchange
+// through shared memory), m moves to it and O is rescaled.  Row sums stay
+// per thread (each thread owns one tile row) and are added across the 128
+// threads once per slice, in a fixed order.
+//
 // Warp roles (320 threads):
-//   warps 0-3  producer: TMA tiled loads of the dense tile (9 boxes of 80 rows,
-//              rows past the cache zero-filled by the TMA unit) or, for the
-//              sparse top-k gather ("The Commit That Changed Direction"),
-//              16-byte cp.async copies of the indexed rows straight into the
-//              swizzled layout; also the item's 16 query rows (9 TMA boxes).
-//   warps 4-7  softmax: thread t owns tile row t (TMEM lane t); per-head max
-//              and sum by warp butterflies and a 4-warp exchange through shared
-//              memory; online softmax in base 2 with a lazily moved reference
-//              (the reference moves, and O and l are rescaled, only when a
-//              head's max grows by more than 2^8, so p <= 256); writes P as
-//              the bf16 pair; at the end of an item reads O from tensor memory
-//              and writes the partial.
+//   warps 0-3  producer.  Dense: one thread issues the TMA boxes (rows past
+//              the cache are zero-filled by the TMA unit).  Sparse top-k
+//              gather ("The Commit That Changed Direction"): 128 threads
+//              copy the indexed rows with 16-byte cp.async straight into the
+//              swizzled layout, one commit group per third of the tile.
+//              Also the item's 16 query rows (one TMA box).
+//   warps 4-7  softmax: thread t owns tile row t (tensor-memory lane t);
+//              writes P as the bf16 pair; at the end of an item reads O from
+//              tensor memory and writes the partial.
 //   warp 8     score MMA issue and tensor-memory allocation; warp 9 P . V
 //              MMA issue.
 // Every wait is bounded (MLA_EDEVICE in the status word on a timeout); the
-// CTA drains its copies and its MMAs and frees its tensor memory before it
-// exits.  No floating-point atomics: results are a pure function of the
-// inputs and the split count.
+// threads of a hardware barrier leave a loop together (the decision to leave
+// is the barrier's own OR-reduction); the CTA drains its copies and its MMAs
+// and frees its tensor memory before it exits.  No floating-point atomics:
+// results are a pure function of the inputs and the split count.
 #include <cfloat>
 #include <cmath>
 
@@ -55,15 +64,21 @@ constexpr int kTileRows = kTcTileRows;                  // 80 cache rows per til
 constexpr int kChunks = kDRow / 64;                     // 9 column chunks of 64 bf16
 constexpr int kChunkBytes = kTileRows * 128;            // 10240
 constexpr int kTileBytes = kChunks * kChunkBytes;       // 92160
+constexpr int kGroups = kChunks / kTcBoxChunks;         // 3 TMA boxes (and barriers) per tile
+constexpr int kGroupBytes = kTcBoxChunks * kChunkBytes; // 30720
 constexpr int kQChunkBytes = kHeadGroup * 128;          // 2048
+constexpr int kQBytes = kChunks * kQChunkBytes;         // 18432
 constexpr int kPVHeads = 2 * kHeadGroup;                // [P_hi | P_lo] along N
 constexpr int kPAtomBytes = kPVHeads * 128;             // one 64-row K atom of P^T
 constexpr int kPBytes = 2 * kPAtomBytes;                // 80 rows need two K atoms
 constexpr int kProducerThreads = 128;
+constexpr int kSoftmaxThreads = 128;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kMmaWarp = 8;                             // QK issue + TMEM allocation
 constexpr int kPvWarp = 9;                              // P . V issue (its own warp: no divergent waits)
 constexpr int kThreads = 320;
+constexpr int kBarProducer = 1;                         // hardware barrier ids (0 is __syncthreads)
+constexpr int kBarSoftmax = 2;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns 16*buf
 constexpr uint32_t kTmemO = 32;                         // O^T block j at 32 + 32j: hi 0..15, lo 16..31
@@ -72,60 +87,63 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 static_assert(kTileRows % 16 == 0 && kTileRows <= 128, "tile rows: whole k-steps, at most M=128");
 static_assert(kChunkBytes % 1024 == 0, "chunks stay 1024-byte aligned for the 128-byte swizzle");
+static_assert(kChunks % kTcBoxChunks == 0, "a tile is a whole number of TMA boxes");
+static_assert((kTcGranule & (kTcGranule - 1)) == 0, "power-of-two granule");
 
 struct __align__(1024) SharedStorage {
     uint8_t kv[2][kTileBytes];            // double-buffered tile (chunk c of buffer b at kv[b] + c*kChunkBytes)
-    uint8_t q[kChunks * kQChunkBytes];    // Q^T: also absorbs the M=128 over-read of the last chunk
+    uint8_t q[kQBytes];                   // Q^T: also absorbs the M=128 over-read of the last chunk
     uint8_t p[2][kPBytes];                // [P_hi | P_lo]^T, K-major, per tile buffer
     alignas(16) float red_max[2][4][16];
-    alignas(16) float red_sum[2][4][16];
+    alignas(16) float red_sum[4][16];
     int valid[2][kTileRows];
     long long rowid[2][kTileRows];        // sparse: the tile's absolute cache rows (-1 = masked)
-    uint64_t full[2], empty[2], s_full[2], p_full[2], o_done[2];
-    uint64_t q_full, q_empty, o_free, bar_max[2], bar_sum[2], mma_done[2];
+    uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
+    uint64_t q_full, q_empty, o_free, mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
 };
 
 struct Item {
     int b, hg, s, n_tiles;
-    long long base, e0, e1;
+    int e0, e1;                           // entries [e0, e1) of the request
+    long long base;                       // first cache row of the request
 };
 
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     Item it;
-    it.hg = item % p.n_groups;
-    const int rest = item / p.n_groups;
-    it.s = rest % p.splits;
-    it.b = rest / p.splits;
-    const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base);
-    const long long per = slice_entries(n, p.splits, p.granule);
-    long long e0 = static_cast<long long>(it.s) * per;
-    long long e1 = e0 + per;
+    const uint32_t ui = static_cast<uint32_t>(item);
+    const uint32_t rest = ui / static_cast<uint32_t>(p.n_groups);
+    it.hg = static_cast<int>(ui - rest * static_cast<uint32_t>(p.n_groups));
+    const uint32_t b = rest / static_cast<uint32_t>(p.splits);
+    it.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
+    it.b = static_cast<int>(b);
+    // the kernel runs only on caches below 2^31 rows, so counts fit 32 bits
+    const uint32_t n = static_cast<uint32_t>(
+        request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
+    const uint32_t per = slice_entries_u32(n, static_cast<uint32_t>(p.splits), kTcGranule);
+    uint32_t e0 = static_cast<uint32_t>(it.s) * per;
+    uint32_t e1 = e0 + per;
     if (e1 > n) e1 = n;
     if (e0 > e1) e0 = e1;
-    it.e0 = e0;
-    it.e1 = e1;
+    it.e0 = static_cast<int>(e0);
+    it.e1 = static_cast<int>(e1);
     it.n_tiles = static_cast<int>((e1 - e0 + kTileRows - 1) / kTileRows);
     return it;
 }
 
 __device__ __forceinline__ int rows_in_tile(const Item& it, int k) {
-    const long long r0 = it.e0 + static_cast<long long>(k) * kTileRows;
-    const long long left = it.e1 - r0;
-    return static_cast<int>(left < kTileRows ? left : kTileRows);
+    const int left = it.e1 - (it.e0 + k * kTileRows);
+    return left < kTileRows ? left : kTileRows;
 }
 
-// The next item of this CTA that has tiles, or -1.
-__device__ __forceinline__ int next_busy_item(const PartialParams& p, int item, Item* out) {
-    for (int i = item + static_cast<int>(gridDim.x); i < p.n_items; i += gridDim.x) {
-        const Item it = decode_item(p, i);
-        if (it.n_tiles > 0) {
-            *out = it;
-            return i;
-        }
-    }
-    return -1;
+__device__ __forceinline__ int item_key(const PartialParams& p, const Item& it) { return it.b * p.n_groups + it.hg; }
+
+// Query tile of the CTA's first item: known without the context length.
+__device__ __forceinline__ int first_key(const PartialParams& p) {
+    const int item = static_cast<int>(blockIdx.x);
+    const int rest = item / p.n_groups;
+    return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
 }
 
 __device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* status) {
@@ -164,44 +182,48 @@ __device__ __forceinline__ void cursor_step(const PartialParams& p, Cursor& c) {
     ++c.g;
     if (++c.k == c.it.n_tiles) cursor_next_item(p, c);
 }
+__device__ __forceinline__ int cursor_row(const Cursor& c) {
+    return static_cast<int>(c.it.base) + c.it.e0 + c.k * kTileRows;
+}
+
+__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int key,
+                                       uint64_t policy) {
+    const int b = key / p.n_groups;
+    const int hg = key - b * p.n_groups;
+    mbar_arrive_expect_tx(&sh.q_full, kQBytes);
+    tma_load_3d(sh.q, &maps.q, 0, b * p.heads + hg * kHeadGroup, 0, &sh.q_full, policy);
+}
 
 // ============================== producer ==================================
-// Dense: one thread issues every TMA (the other producer threads do nothing
-// and wait at the final barrier, so they take no issue slots from the
-// softmax warps); rows past the slice or the cache are masked by the softmax.
-// Sparse: thread 0 alone polls the barriers and a hardware barrier releases
-// the 128 gather threads; every thread reaches every hardware barrier, also
-// when a wait runs out (then all of them leave together).
+// Query tiles: the first one is requested before the context length is
+// known; the score-MMA thread follows the same sequence of keys (a new load
+// whenever the next busy item's key differs) and releases a tile through
+// q_empty before the next one is loaded over it.
 __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int t) {
     if (!p.sparse && t != 0) return;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_normal();
+    int q_key = first_key(p);
+    if (t == 0) load_q(maps, p, sh, q_key, pol_q);
+    int q_loads = 1;
     // L2 prefetch runs two tiles ahead of the shared-memory loads: shared memory
     // holds two tiles, L2 the next two in flight
     Cursor pf;
     cursor_init(p, pf);
     for (int i = 0; i < 2 && pf.valid; ++i) cursor_step(p, pf);
     int g = 0;
-    int q_loads = 0;
-    int q_key = -1;
     // `stop` is uniform over the producer threads (sparse: agreed at a barrier)
     bool stop = false;
     for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
         const Item it = decode_item(p, item);
         if (it.n_tiles == 0) continue;
-        const int key = it.b * p.n_groups + it.hg;
-        const bool new_q = key != q_key;
-        if (new_q) {
+        const int key = item_key(p, it);
+        if (key != q_key) {
             if (t == 0) {
-                if (q_loads > 0 && !mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
+                if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag))
                     raise_device_error(sh, p.status);
-                } else {
-                    mbar_arrive_expect_tx(&sh.q_full, kChunks * kQChunkBytes);
-                    const int y = it.b * p.heads + it.hg * kHeadGroup;
-#pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_2d(sh.q + c * kQChunkBytes, &maps.q, 64 * c, y, &sh.q_full, pol_q);
-                }
+                else
+                    load_q(maps, p, sh, key, pol_q);
             }
             q_key = key;
             ++q_loads;
@@ -211,24 +233,26 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             const int buf = g & 1;
             if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
                 raise_device_error(sh, p.status);
-            const long long r0 = it.e0 + static_cast<long long>(k) * kTileRows;
+            const int r0 = it.e0 + k * kTileRows;
             const int rows = rows_in_tile(it, k);
             if (!p.sparse) {
                 stop = sh.abort_flag != 0;
                 if (stop) break;
-                mbar_arrive_expect_tx(&sh.full[buf], kTileBytes);
-                const int y = static_cast<int>(it.base + r0);
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_2d(sh.kv[buf] + c * kChunkBytes, &maps.kv, 64 * c, y, &sh.full[buf], pol_kv);
+                const int y = static_cast<int>(it.base) + r0;
+#pragma unroll
+                for (int grp = 0; grp < kGroups; ++grp) {
+                    mbar_arrive_expect_tx(&sh.full[buf][grp], kGroupBytes);
+                    tma_load_3d(sh.kv[buf] + grp * kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
+                                pol_kv);
+                }
                 if (pf.valid) {
-                    const int yp = static_cast<int>(pf.it.base + pf.it.e0 + static_cast<long long>(pf.k) * kTileRows);
-#pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c) tma_prefetch_2d(&maps.kv, 64 * c, yp);
+                    const int yp = cursor_row(pf);
+#pragma unroll
+                    for (int grp = 0; grp < kGroups; ++grp) tma_prefetch_3d(&maps.kv, 0, yp, grp * kTcBoxChunks);
                 }
             } else {
                 // the buffer is free, or some thread saw the CTA abort
-                stop = named_barrier_or(1, kProducerThreads, sh.abort_flag != 0);
+                stop = named_barrier_or(kBarProducer, kProducerThreads, sh.abort_flag != 0);
                 if (stop) break;
                 // the tile's row ids, resolved once into shared memory
                 const int* idx = p.indices + static_cast<long long>(it.b) * p.topk + r0;
@@ -241,29 +265,33 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                     sh.rowid[buf][t] = row;
                     sh.valid[buf][t] = row >= 0 ? 1 : 0;
                 }
-                named_barrier_sync(1, kProducerThreads);      // row ids ready
+                named_barrier_sync(kBarProducer, kProducerThreads);      // row ids ready
                 // rows past the tile's last k-step are never read by P . V; masked
                 // rows inside it must hold zeros (they meet p = 0)
                 const int rows_read = (rows + 15) & ~15;
                 const uint32_t dst0 = smem_u32(sh.kv[buf]);
                 const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
                 const long long stride_bytes = p.row_stride * 2;
+                constexpr int kUnits = kTcBoxChunks * 8;                  // 16-byte units of a row in one box
+#pragma unroll
+                for (int grp = 0; grp < kGroups; ++grp) {
 #pragma unroll 4
-                for (int piece = t; piece < rows_read * 72; piece += kProducerThreads) {
-                    const int r = piece / 72;
-                    const int u = piece - r * 72;
-                    const int c = u >> 3;
-                    const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
-                    const long long row = sh.rowid[buf][r];
-                    if (row >= 0)
-                        cp_async_16(dst, kvb + row * stride_bytes + u * 16);
-                    else
-                        st_shared_v4_zero(dst);
+                    for (int piece = t; piece < rows_read * kUnits; piece += kProducerThreads) {
+                        const int r = piece / kUnits;
+                        const int u = grp * kUnits + (piece - r * kUnits);
+                        const int c = u >> 3;
+                        const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
+                        const long long row = sh.rowid[buf][r];
+                        if (row >= 0)
+                            cp_async_16(dst, kvb + row * stride_bytes + u * 16);
+                        else
+                            st_shared_v4_zero(dst);
+                    }
+                    cp_async_commit();
                 }
-                cp_async_commit();
                 if (pf.valid && t < kTileRows) {
                     // rows of the tile two ahead into L2 while this tile's copies land
-                    const long long pr0 = pf.it.e0 + static_cast<long long>(pf.k) * kTileRows;
+                    const int pr0 = pf.it.e0 + pf.k * kTileRows;
                     if (t < rows_in_tile(pf.it, pf.k)) {
                         const int id = p.indices[static_cast<long long>(pf.it.b) * p.topk + pr0 + t];
                         const int plen = p.cache_len[pf.it.b];
@@ -272,9 +300,15 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                             bulk_prefetch_l2(kvb + prow * stride_bytes, kRowBytes);
                     }
                 }
+                cp_async_wait_group<2>();
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.full[buf][0]);
+                cp_async_wait_group<1>();
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.full[buf][1]);
                 cp_async_wait_group<0>();
                 fence_proxy_async_smem();
-                mbar_arrive(&sh.full[buf]);
+                mbar_arrive(&sh.full[buf][2]);
             }
             if (pf.valid) cursor_step(p, pf);
         }
@@ -284,19 +318,20 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
         volatile int never = 0;
         for (int b = 0; b < 2 && b < g; ++b) {
             const int last = g - 1 - ((g - 1 - b) & 1);    // last tile number that used buffer b
-            if (!mbar_wait_bounded(&sh.full[b], (last >> 1) & 1, &never)) raise_device_error(sh, p.status);
+            for (int grp = 0; grp < kGroups; ++grp)
+                if (!mbar_wait_bounded(&sh.full[b][grp], (last >> 1) & 1, &never)) raise_device_error(sh, p.status);
         }
-        if (q_loads > 0 && !mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never)) raise_device_error(sh, p.status);
+        if (!mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never)) raise_device_error(sh, p.status);
     }
 }
 
 // ============================== MMA issue ==================================
 // Two threads in two warps issue the MMAs (the tensor pipe overlaps
 // instructions from different issuers, and a waiting issuer does not stall
-// the other): the scores of each tile, and the P . V products.  QK of tile g waits for its tile and for the softmax of
-// tile g-2 (the owner of its score buffer); P . V of tile g waits for the
-// softmax of tile g, and the first one of an item for the previous item's
-// epilogue.
+// the other): the scores of each tile, and the P . V products.  QK of tile g
+// waits for each third of its tile and for the softmax of tile g-2 (the
+// owner of its score buffer); P . V of tile g waits for the softmax of tile
+// g, and the first one of an item for the previous item's epilogue.
 __device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
     const uint32_t idesc_qk = make_idesc_bf16(128, kHeadGroup, 0, 0);
     // K-major 128-byte-swizzled operands: 8-row groups 1024 bytes apart
@@ -304,45 +339,59 @@ __device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t
     const uint64_t q_desc0 = make_sdesc(smem_u32(sh.q), 16, 1024, kLayoutSw128);
     Cursor qc;
     cursor_init(p, qc);
-    int q_loads = 0;
-    int cur_key = -1;
+    int q_key = first_key(p);
+    int q_phase = 0;
+    bool q_ready = false;
     bool ok = true;
     while (qc.valid && ok) {
-        const int key = qc.it.b * p.n_groups + qc.it.hg;
+        const int key = item_key(p, qc.it);
         const int buf = qc.g & 1;
-        if (qc.k == 0 && key != cur_key) {
-            if (!mbar_wait_bounded(&sh.q_full, q_loads & 1, &sh.abort_flag)) {
+        if (key != q_key) {
+            // the producer loads the next query tile over this one: it must have
+            // landed (never read, possibly) and its MMAs must be complete
+            if (!q_ready && !mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
             }
-            ++q_loads;
-            cur_key = key;
+            umma_commit(&sh.q_empty);
+            ++q_phase;
+            q_key = key;
+            q_ready = false;
         }
-        if (!mbar_wait_bounded(&sh.full[buf], (qc.g >> 1) & 1, &sh.abort_flag) ||
-            (qc.g >= 2 && !mbar_wait_bounded(&sh.p_full[buf], ((qc.g >> 1) - 1) & 1, &sh.abort_flag))) {
+        if (!q_ready) {
+            if (!mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
+                ok = false;
+                break;
+            }
+            q_ready = true;
+        }
+        if (qc.g >= 2 && !mbar_wait_bounded(&sh.p_full[buf], ((qc.g >> 1) - 1) & 1, &sh.abort_flag)) {
             ok = false;
             break;
         }
-        tc_fence_after_sync();
         const uint64_t kb = kv_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
         // fully unrolled: every descriptor is a constant offset from kb / q_desc0,
         // so the issuing thread keeps pace with the tensor pipe
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
+        for (int grp = 0; grp < kGroups; ++grp) {
+            if (!mbar_wait_bounded(&sh.full[buf][grp], (qc.g >> 1) & 1, &sh.abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t off = (c * kChunkBytes + kk * 32u) >> 4;
-                const uint32_t qoff = (c * kQChunkBytes + kk * 32u) >> 4;
-                umma_bf16(tmem + kTmemS + 16 * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
+            for (int cc = 0; cc < kTcBoxChunks; ++cc) {
+                const int c = grp * kTcBoxChunks + cc;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t off = (c * kChunkBytes + kk * 32u) >> 4;
+                    const uint32_t qoff = (c * kQChunkBytes + kk * 32u) >> 4;
+                    umma_bf16(tmem + kTmemS + 16 * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
+                }
             }
         }
+        if (!ok) break;
         umma_commit(&sh.s_full[buf]);
-        if (qc.k == qc.it.n_tiles - 1) {
-            // last user of this query tile: release it if the next item needs another
-            Item nx;
-            const int ni = next_busy_item(p, qc.item, &nx);
-            if (ni >= 0 && nx.b * p.n_groups + nx.hg != key) umma_commit(&sh.q_empty);
-        }
         cursor_step(p, qc);
     }
     if (!ok) raise_device_error(sh, p.status);
@@ -409,38 +458,8 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage& sh, uint32_t
 }
 
 // ============================== softmax warps ==============================
-__device__ __forceinline__ void warp_max16(float (&v)[16], int lane) {
-    // After the halving steps lane L holds head (L >> 1); the last step joins the pair.
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const bool up = lane & 16;
-        const float send = up ? v[k] : v[k + 8];
-        const float keep = up ? v[k + 8] : v[k];
-        v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const bool up = lane & 8;
-        const float send = up ? v[k] : v[k + 4];
-        const float keep = up ? v[k + 4] : v[k];
-        v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const bool up = lane & 4;
-        const float send = up ? v[k] : v[k + 2];
-        const float keep = up ? v[k + 2] : v[k];
-        v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-    }
-    {
-        const bool up = lane & 2;
-        const float send = up ? v[0] : v[1];
-        const float keep = up ? v[1] : v[0];
-        v[0] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    }
-    v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
-}
 __device__ __forceinline__ void warp_sum16(float (&v)[16], int lane) {
+    // After the halving steps lane L holds head (L >> 1); the last step joins the pair.
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const bool up = lane & 16;
@@ -471,34 +490,40 @@ __device__ __forceinline__ void warp_sum16(float (&v)[16], int lane) {
     v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// The four softmax warps meet at hardware barrier kBarSoftmax; a bounded wait
+// that ran out in any of them turns the barrier's OR true, and then all 128
+// threads leave together (a thread that left alone would strand the others).
+__device__ __forceinline__ bool softmax_barrier_or(bool pred) {
+    return named_barrier_or(kBarSoftmax, kSoftmaxThreads, pred);
+}
+
 __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_t tmem, int q, int lane) {
     const int t = q * 32 + lane;                     // tile row / TMEM lane of this thread
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const bool has_rows = q * 32 < kTileRows;        // warp-uniform
     int g = 0;
-    int items_done = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
         if (it.n_tiles == 0) continue;
-        float m_ref[16], l_run[16];
+        float m_ref[16], l_part[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
             m_ref[h] = -INFINITY;
-            l_run[h] = 0.f;
+            l_part[h] = 0.f;
         }
         const int first_g = g;
         for (int k = 0; k < it.n_tiles; ++k, ++g) {
             const int buf = g & 1;
             const int rows = rows_in_tile(it, k);
-            // sparse tiles' row flags come from the producer: acquire its barrier too
-            if (!mbar_wait_bounded(&sh.s_full[buf], (g >> 1) & 1, &sh.abort_flag) ||
-                (p.sparse && !mbar_wait_bounded(&sh.full[buf], (g >> 1) & 1, &sh.abort_flag))) {
-                ok = false;
-                break;
-            }
+            // scores of tile g; sparse: the producer's row flags; P buffer free (P . V of g-2 done)
+            bool w = mbar_wait_bounded(&sh.s_full[buf], (g >> 1) & 1, &sh.abort_flag);
+            if (p.sparse) w = w && mbar_wait_bounded(&sh.full[buf][0], (g >> 1) & 1, &sh.abort_flag);
+            if (g >= 2) w = w && mbar_wait_bounded(&sh.o_done[buf], ((g >> 1) - 1) & 1, &sh.abort_flag);
+            w = __all_sync(0xffffffffu, w);
             tc_fence_after_sync();
             float s[16];
-            if (q * 32 < kTileRows) {
+            if (w && has_rows) {
                 tmem_ld16(tmem + lane_addr + kTmemS + 16 * buf, s);
             } else {
 #pragma unroll
@@ -508,26 +533,32 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             if (p.sparse) {
                 row_ok = t < rows && sh.valid[buf][t] != 0;
             } else {
-                const long long row = it.base + it.e0 + static_cast<long long>(k) * kTileRows + t;
+                const long long row = it.base + it.e0 + k * kTileRows + t;
                 row_ok = t < rows && row >= 0 && row < p.kv_rows;
             }
+            bool need = !w;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) s[h] = row_ok ? s[h] * p.scale_log2 : -INFINITY;
-
-            // ---- tile max per head (fixed butterfly + 4-warp exchange) ----------
-            float red[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) red[h] = s[h];
-            warp_max16(red, lane);
-            if ((lane & 1) == 0) sh.red_max[buf][q][lane >> 1] = red[0];
-            mbar_arrive(&sh.bar_max[buf]);
-            if (!mbar_wait_bounded(&sh.bar_max[buf], (g >> 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
+            for (int h = 0; h < 16; ++h) {
+                s[h] = row_ok ? s[h] * p.scale_log2 : -INFINITY;
+                need |= s[h] > m_ref[h] + kRescaleLog2;             // false for masked rows and -inf refs alike
             }
             float alpha[16];
-            bool rescale = false;
-            {
+#pragma unroll
+            for (int h = 0; h < 16; ++h) alpha[h] = 1.f;
+            if (softmax_barrier_or(need)) {
+                // ---- tile max per head: warp max, then the four warps through shared memory
+                float mine = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    const float r = warp_max_f32(s[h]);
+                    if (lane == h) mine = r;
+                }
+                if (lane < 16) sh.red_max[buf][q][lane] = mine;
+                if (softmax_barrier_or(!w)) {
+                    ok = false;
+                    break;
+                }
+                bool rescale = false;
                 const float4* rm = reinterpret_cast<const float4*>(&sh.red_max[buf][0][0]);
 #pragma unroll
                 for (int h4 = 0; h4 < 4; ++h4) {
@@ -536,30 +567,48 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                                          fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z)), fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w))};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        // branch-free: the reference moves to the tile max when that
-                        // exceeds it by more than 2^8 (or nothing was referenced yet)
+                        // the reference moves to the tile max when that exceeds it by
+                        // more than 2^8 (or nothing was referenced yet); sums and O taken
+                        // against a finite old reference are scaled to the new one
                         const int h = 4 * h4 + i;
-                        const float tmax = tm[i];
                         const float ref = m_ref[h];
-                        const bool move = tmax > ref + kRescaleLog2;          // false while tmax == -inf
-                        const float nref = move ? tmax : ref;
-                        const bool scale_o = move && l_run[h] > 0.f;            // l > 0 implies ref finite
-                        const float a = ex2_approx(scale_o ? ref - nref : 0.f);
-                        alpha[h] = a;
-                        rescale |= scale_o;
+                        const bool move = tm[i] > ref + kRescaleLog2;     // false while the tile max is -inf
+                        const float nref = move ? tm[i] : ref;
+                        const bool scale = move && ref > -INFINITY;
+                        alpha[h] = scale ? ex2_approx(ref - nref) : 1.f;
+                        rescale |= scale;
                         m_ref[h] = nref;
+                    }
+                }
+                if (rescale && g > first_g) {
+                    // ---- rare: O holds earlier tiles of this slice; move it to the new reference
+                    const int gp = g - 1;
+                    bool w2 = mbar_wait_bounded(&sh.o_done[gp & 1], (gp >> 1) & 1, &sh.abort_flag);
+                    w2 = __all_sync(0xffffffffu, w2);
+                    if (softmax_barrier_or(!w2)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll 1
+                        for (int half = 0; half < 2; ++half) {
+                            float o[16];
+                            const uint32_t a = tmem + lane_addr + kTmemO + 32 * j + 16 * half;
+                            tmem_ld16(a, o);
+#pragma unroll
+                            for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
+                            tmem_st16(a, o);
+                        }
                     }
                 }
             }
 
-            // ---- probabilities, written as the bf16 pair [P_hi | P_lo]^T --------
+            // ---- probabilities, written as the bf16 pair [P_hi | P_lo]^T ----------
             float pr[16];
 #pragma unroll
             for (int h = 0; h < 16; ++h) pr[h] = (row_ok && m_ref[h] > -INFINITY) ? ex2_approx(s[h] - m_ref[h]) : 0.f;
-            if (g >= 2 && !mbar_wait_bounded(&sh.o_done[buf], ((g >> 1) - 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
             if (t < kTileRows) {
                 // row t of head h: line h (hi) / 16 + h (lo) of the K atom t / 64, byte 2 * (t % 64)
                 const uint32_t pbase = smem_u32(sh.p[buf]) + (t >> 6) * kPAtomBytes + 2u * (t & 7);
@@ -573,49 +622,9 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     st_shared_u16(a + 2048, __bfloat16_as_ushort(lo));
                 }
             }
-            // ---- row sums -------------------------------------------------------
 #pragma unroll
-            for (int h = 0; h < 16; ++h) red[h] = pr[h];
-            warp_sum16(red, lane);
-            if ((lane & 1) == 0) sh.red_sum[buf][q][lane >> 1] = red[0];
-            mbar_arrive(&sh.bar_sum[buf]);
-            if (!mbar_wait_bounded(&sh.bar_sum[buf], (g >> 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
-            {
-                const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[buf][0][0]);
-#pragma unroll
-                for (int h4 = 0; h4 < 4; ++h4) {
-                    const float4 a = rs[h4], b = rs[4 + h4], c = rs[8 + h4], d = rs[12 + h4];
-                    l_run[4 * h4 + 0] = l_run[4 * h4 + 0] * alpha[4 * h4 + 0] + (((a.x + b.x) + c.x) + d.x);
-                    l_run[4 * h4 + 1] = l_run[4 * h4 + 1] * alpha[4 * h4 + 1] + (((a.y + b.y) + c.y) + d.y);
-                    l_run[4 * h4 + 2] = l_run[4 * h4 + 2] * alpha[4 * h4 + 2] + (((a.z + b.z) + c.z) + d.z);
-                    l_run[4 * h4 + 3] = l_run[4 * h4 + 3] * alpha[4 * h4 + 3] + (((a.w + b.w) + c.w) + d.w);
-                }
-            }
-            // ---- rare: move O to the new reference --------------------------------
-            if (rescale && g > first_g) {
-                const int gp = g - 1;
-                if (!mbar_wait_bounded(&sh.o_done[gp & 1], (gp >> 1) & 1, &sh.abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-#pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        float o[16];
-                        const uint32_t a = tmem + lane_addr + kTmemO + 32 * j + 16 * half;
-                        tmem_ld16(a, o);
-#pragma unroll
-                        for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
-                        tmem_st16(a, o);
-                    }
-                }
-            }
-            // ---- dense: masked rows the P . V k-steps read must hold zeros -------
+            for (int h = 0; h < 16; ++h) l_part[h] = l_part[h] * alpha[h] + pr[h];
+            // ---- dense: masked rows the P . V k-steps read must hold zeros ---------
             if (!p.sparse && t < kTileRows && !row_ok && t < ((rows + 15) & ~15)) {
                 const uint32_t row_base = smem_u32(sh.kv[buf]) + t * 128;
 #pragma unroll 1
@@ -629,13 +638,35 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         }
         if (!ok) break;
 
-        // ---- epilogue: O = (O_hi + O_lo) / l, lse = m + log2(l) (to natural log) ---
+        // ---- epilogue: l = sum of the rows' sums (fixed order), O = (O_hi + O_lo) / l,
+        //      lse = m + log2(l) (to natural log) --------------------------------------
         const int gl = g - 1;
-        if (!mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag)) {
+        bool w = mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag);
+        w = __all_sync(0xffffffffu, w);
+        {
+            float red[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) red[h] = l_part[h];
+            warp_sum16(red, lane);
+            if ((lane & 1) == 0) sh.red_sum[q][lane >> 1] = red[0];
+        }
+        if (softmax_barrier_or(!w)) {
             ok = false;
             break;
         }
         tc_fence_after_sync();
+        float l_run[16];
+        {
+            const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[0][0]);
+#pragma unroll
+            for (int h4 = 0; h4 < 4; ++h4) {
+                const float4 a = rs[h4], b = rs[4 + h4], c = rs[8 + h4], d = rs[12 + h4];
+                l_run[4 * h4 + 0] = ((a.x + b.x) + c.x) + d.x;
+                l_run[4 * h4 + 1] = ((a.y + b.y) + c.y) + d.y;
+                l_run[4 * h4 + 2] = ((a.z + b.z) + c.z) + d.z;
+                l_run[4 * h4 + 3] = ((a.w + b.w) + c.w) + d.w;
+            }
+        }
         float inv[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
@@ -662,7 +693,6 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         }
         tc_fence_before_sync();
         mbar_arrive(&sh.o_free);
-        ++items_done;
     }
     if (!ok && lane == 0) raise_device_error(sh, p.status);
 }
@@ -678,17 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
         prefetch_tensormap(&maps.kv);
         prefetch_tensormap(&maps.q);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.full[i], p.sparse ? kProducerThreads : 1);
+            for (int grp = 0; grp < kGroups; ++grp) mbar_init(&sh.full[i][grp], p.sparse ? kProducerThreads : 1);
             mbar_init(&sh.empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], 128);
+            mbar_init(&sh.p_full[i], kSoftmaxThreads);
             mbar_init(&sh.o_done[i], 1);
-            mbar_init(&sh.bar_max[i], 128);
-            mbar_init(&sh.bar_sum[i], 128);
         }
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, 1);
-        mbar_init(&sh.o_free, 128);
+        mbar_init(&sh.o_free, kSoftmaxThreads);
         mbar_init(&sh.mma_done[0], 1);
         mbar_init(&sh.mma_done[1], 1);
         sh.abort_flag = 0;

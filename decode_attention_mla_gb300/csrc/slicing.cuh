@@ -29,4 +29,12 @@ __host__ __device__ __forceinline__ long long slice_entries(long long n, int spl
     return (per + granule - 1) / granule * granule;
 }
 
+// The same cut in 32-bit arithmetic for counts below 2^31 with a power-of-two
+// granule (the tcgen05 kernel's item decode runs on the critical path of
+// every CTA's first load; 64-bit division there costs hundreds of cycles).
+__device__ __forceinline__ uint32_t slice_entries_u32(uint32_t n, uint32_t splits, uint32_t granule_pow2) {
+    const uint32_t per = (n + splits - 1u) / splits;
+    return (per + granule_pow2 - 1u) & ~(granule_pow2 - 1u);
+}
+
 }  // namespace mla

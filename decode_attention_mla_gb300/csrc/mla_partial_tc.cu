@@ -79,6 +79,7 @@ constexpr int kPvWarp = 9;                              // P . V issue (its own 
 constexpr int kThreads = 320;
 constexpr int kBarProducer = 1;                         // hardware barrier ids (0 is __syncthreads)
 constexpr int kBarSoftmax = 2;
+constexpr int kBarTmem = 3;                             // softmax + MMA warps: tensor memory allocated
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns 16*buf
 constexpr uint32_t kTmemO = 32;                         // O^T block j at 32 + 32j: hi 0..15, lo 16..31
@@ -195,127 +196,131 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 }
 
 // ============================== producer ==================================
-// Query tiles: the first one is requested before the context length is
-// known; the score-MMA thread follows the same sequence of keys (a new load
-// whenever the next busy item's key differs) and releases a tile through
-// q_empty before the next one is loaded over it.
+// Query tiles: the first one is requested by a thread of the P . V warp at
+// kernel start (before the context length is known, and off the producer's
+// path); the producer and the score-MMA thread follow the same sequence of
+// keys (a new load whenever the next busy item's key differs), and the MMA
+// thread releases a tile through q_empty before the next one is loaded over it.
 __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int t) {
     if (!p.sparse && t != 0) return;
-    const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_normal();
     int q_key = first_key(p);
-    if (t == 0) load_q(maps, p, sh, q_key, pol_q);
+    const uint64_t pol_kv = l2_policy_evict_first();
     int q_loads = 1;
+    Cursor cur;
+    cursor_init(p, cur);
     // L2 prefetch runs two tiles ahead of the shared-memory loads: shared memory
     // holds two tiles, L2 the next two in flight
-    Cursor pf;
-    cursor_init(p, pf);
+    Cursor pf = cur;
     for (int i = 0; i < 2 && pf.valid; ++i) cursor_step(p, pf);
-    int g = 0;
+    int seg_len = 0;
     // `stop` is uniform over the producer threads (sparse: agreed at a barrier)
     bool stop = false;
-    for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
-        const Item it = decode_item(p, item);
-        if (it.n_tiles == 0) continue;
-        const int key = item_key(p, it);
-        if (key != q_key) {
-            if (t == 0) {
-                if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag))
-                    raise_device_error(sh, p.status);
-                else
-                    load_q(maps, p, sh, key, pol_q);
+    while (cur.valid && !stop) {
+        const Item& it = cur.it;
+        const int g = cur.g;
+        const int k = cur.k;
+        if (k == 0) {
+            const int key = item_key(p, it);
+            if (key != q_key) {
+                if (t == 0) {
+                    if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag))
+                        raise_device_error(sh, p.status);
+                    else
+                        load_q(maps, p, sh, key, pol_q);
+                }
+                q_key = key;
+                ++q_loads;
             }
-            q_key = key;
-            ++q_loads;
+            if (p.sparse) seg_len = p.cache_len[it.b];
         }
-        const int seg_len = p.sparse ? p.cache_len[it.b] : 0;
-        for (int k = 0; k < it.n_tiles; ++k, ++g) {
-            const int buf = g & 1;
-            if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
-                raise_device_error(sh, p.status);
-            const int r0 = it.e0 + k * kTileRows;
-            const int rows = rows_in_tile(it, k);
-            if (!p.sparse) {
-                stop = sh.abort_flag != 0;
-                if (stop) break;
-                const int y = static_cast<int>(it.base) + r0;
+        const int buf = g & 1;
+        if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
+            raise_device_error(sh, p.status);
+        const int r0 = it.e0 + k * kTileRows;
+        const int rows = rows_in_tile(it, k);
+        if (!p.sparse) {
+            stop = sh.abort_flag != 0;
+            if (stop) break;
+            const int y = static_cast<int>(it.base) + r0;
 #pragma unroll
-                for (int grp = 0; grp < kGroups; ++grp) {
-                    mbar_arrive_expect_tx(&sh.full[buf][grp], kGroupBytes);
-                    tma_load_3d(sh.kv[buf] + grp * kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
-                                pol_kv);
-                }
-                if (pf.valid) {
-                    const int yp = cursor_row(pf);
+            for (int grp = 0; grp < kGroups; ++grp) {
+                mbar_arrive_expect_tx(&sh.full[buf][grp], kGroupBytes);
+                tma_load_3d(sh.kv[buf] + grp * kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
+                            pol_kv);
+            }
+            if (pf.valid) {
+                const int yp = cursor_row(pf);
 #pragma unroll
-                    for (int grp = 0; grp < kGroups; ++grp) tma_prefetch_3d(&maps.kv, 0, yp, grp * kTcBoxChunks);
+                for (int grp = 0; grp < kGroups; ++grp) tma_prefetch_3d(&maps.kv, 0, yp, grp * kTcBoxChunks);
+            }
+        } else {
+            // the buffer is free, or some thread saw the CTA abort
+            stop = named_barrier_or(kBarProducer, kProducerThreads, sh.abort_flag != 0);
+            if (stop) break;
+            // the tile's row ids, resolved once into shared memory
+            const int* idx = p.indices + static_cast<long long>(it.b) * p.topk + r0;
+            if (t < kTileRows) {
+                long long row = -1;
+                if (t < rows) {
+                    const int id = idx[t];
+                    if (id >= 0 && id < seg_len && it.base + id >= 0 && it.base + id < p.kv_rows) row = it.base + id;
                 }
-            } else {
-                // the buffer is free, or some thread saw the CTA abort
-                stop = named_barrier_or(kBarProducer, kProducerThreads, sh.abort_flag != 0);
-                if (stop) break;
-                // the tile's row ids, resolved once into shared memory
-                const int* idx = p.indices + static_cast<long long>(it.b) * p.topk + r0;
-                if (t < kTileRows) {
-                    long long row = -1;
-                    if (t < rows) {
-                        const int id = idx[t];
-                        if (id >= 0 && id < seg_len && it.base + id >= 0 && it.base + id < p.kv_rows) row = it.base + id;
-                    }
-                    sh.rowid[buf][t] = row;
-                    sh.valid[buf][t] = row >= 0 ? 1 : 0;
-                }
-                named_barrier_sync(kBarProducer, kProducerThreads);      // row ids ready
-                // rows past the tile's last k-step are never read by P . V; masked
-                // rows inside it must hold zeros (they meet p = 0)
-                const int rows_read = (rows + 15) & ~15;
-                const uint32_t dst0 = smem_u32(sh.kv[buf]);
-                const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
-                const long long stride_bytes = p.row_stride * 2;
-                constexpr int kUnits = kTcBoxChunks * 8;                  // 16-byte units of a row in one box
+                sh.rowid[buf][t] = row;
+                sh.valid[buf][t] = row >= 0 ? 1 : 0;
+            }
+            named_barrier_sync(kBarProducer, kProducerThreads);      // row ids ready
+            // rows past the tile's last k-step are never read by P . V; masked
+            // rows inside it must hold zeros (they meet p = 0)
+            const int rows_read = (rows + 15) & ~15;
+            const uint32_t dst0 = smem_u32(sh.kv[buf]);
+            const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
+            const long long stride_bytes = p.row_stride * 2;
+            constexpr int kUnits = kTcBoxChunks * 8;                  // 16-byte units of a row in one box
 #pragma unroll
-                for (int grp = 0; grp < kGroups; ++grp) {
+            for (int grp = 0; grp < kGroups; ++grp) {
 #pragma unroll 4
-                    for (int piece = t; piece < rows_read * kUnits; piece += kProducerThreads) {
-                        const int r = piece / kUnits;
-                        const int u = grp * kUnits + (piece - r * kUnits);
-                        const int c = u >> 3;
-                        const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
-                        const long long row = sh.rowid[buf][r];
-                        if (row >= 0)
-                            cp_async_16(dst, kvb + row * stride_bytes + u * 16);
-                        else
-                            st_shared_v4_zero(dst);
-                    }
-                    cp_async_commit();
+                for (int piece = t; piece < rows_read * kUnits; piece += kProducerThreads) {
+                    const int r = piece / kUnits;
+                    const int u = grp * kUnits + (piece - r * kUnits);
+                    const int c = u >> 3;
+                    const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
+                    const long long row = sh.rowid[buf][r];
+                    if (row >= 0)
+                        cp_async_16(dst, kvb + row * stride_bytes + u * 16);
+                    else
+                        st_shared_v4_zero(dst);
                 }
-                if (pf.valid && t < kTileRows) {
-                    // rows of the tile two ahead into L2 while this tile's copies land
-                    const int pr0 = pf.it.e0 + pf.k * kTileRows;
-                    if (t < rows_in_tile(pf.it, pf.k)) {
-                        const int id = p.indices[static_cast<long long>(pf.it.b) * p.topk + pr0 + t];
-                        const int plen = p.cache_len[pf.it.b];
-                        const long long prow = pf.it.base + id;
-                        if (id >= 0 && id < plen && prow >= 0 && prow < p.kv_rows)
-                            bulk_prefetch_l2(kvb + prow * stride_bytes, kRowBytes);
-                    }
-                }
-                cp_async_wait_group<2>();
-                fence_proxy_async_smem();
-                mbar_arrive(&sh.full[buf][0]);
-                cp_async_wait_group<1>();
-                fence_proxy_async_smem();
-                mbar_arrive(&sh.full[buf][1]);
-                cp_async_wait_group<0>();
-                fence_proxy_async_smem();
-                mbar_arrive(&sh.full[buf][2]);
+                cp_async_commit();
             }
-            if (pf.valid) cursor_step(p, pf);
+            if (pf.valid && t < kTileRows) {
+                // rows of the tile two ahead into L2 while this tile's copies land
+                const int pr0 = pf.it.e0 + pf.k * kTileRows;
+                if (t < rows_in_tile(pf.it, pf.k)) {
+                    const int id = p.indices[static_cast<long long>(pf.it.b) * p.topk + pr0 + t];
+                    const int plen = p.cache_len[pf.it.b];
+                    const long long prow = pf.it.base + id;
+                    if (id >= 0 && id < plen && prow >= 0 && prow < p.kv_rows)
+                        bulk_prefetch_l2(kvb + prow * stride_bytes, kRowBytes);
+                }
+            }
+            cp_async_wait_group<2>();
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[buf][0]);
+            cp_async_wait_group<1>();
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[buf][1]);
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[buf][2]);
         }
+        if (pf.valid) cursor_step(p, pf);
+        cursor_step(p, cur);
     }
     // Never retire the CTA with copies into its shared memory in flight.
     if (t == 0) {
         volatile int never = 0;
+        const int g = cur.g;                             // tiles issued
         for (int b = 0; b < 2 && b < g; ++b) {
             const int last = g - 1 - ((g - 1 - b) & 1);    // last tile number that used buffer b
             for (int grp = 0; grp < kGroups; ++grp)
@@ -592,15 +597,17 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     tc_fence_after_sync();
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
-#pragma unroll 1
-                        for (int half = 0; half < 2; ++half) {
-                            float o[16];
-                            const uint32_t a = tmem + lane_addr + kTmemO + 32 * j + 16 * half;
-                            tmem_ld16(a, o);
+                        float o[32];
+                        const uint32_t a = tmem + lane_addr + kTmemO + 32 * j;
+                        tmem_ld32(a, o);
+                        float hi[16], lo[16];
 #pragma unroll
-                            for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
-                            tmem_st16(a, o);
+                        for (int h = 0; h < 16; ++h) {
+                            hi[h] = o[h] * alpha[h];
+                            lo[h] = o[16 + h] * alpha[h];
                         }
+                        tmem_st16(a, hi);
+                        tmem_st16(a + 16, lo);
                     }
                 }
             }
@@ -639,10 +646,8 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         if (!ok) break;
 
         // ---- epilogue: l = sum of the rows' sums (fixed order), O = (O_hi + O_lo) / l,
-        //      lse = m + log2(l) (to natural log) --------------------------------------
-        const int gl = g - 1;
-        bool w = mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag);
-        w = __all_sync(0xffffffffu, w);
+        //      lse = m + log2(l) (to natural log).  The sums and lse do not need
+        //      the last P . V, so they are formed while it runs. -----------------
         {
             float red[16];
 #pragma unroll
@@ -650,11 +655,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             warp_sum16(red, lane);
             if ((lane & 1) == 0) sh.red_sum[q][lane >> 1] = red[0];
         }
-        if (softmax_barrier_or(!w)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after_sync();
+        named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
         float l_run[16];
         {
             const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[0][0]);
@@ -667,20 +668,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                 l_run[4 * h4 + 3] = ((a.w + b.w) + c.w) + d.w;
             }
         }
-        float inv[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
         const long long row0 = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s;
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-            float hi[16], lo[16];
-            tmem_ld16(tmem + lane_addr + kTmemO + 32 * j, hi);
-            tmem_ld16(tmem + lane_addr + kTmemO + 32 * j + 16, lo);
-            const int f = 128 * j + t;
-#pragma unroll
-            for (int h = 0; h < 16; ++h)
-                p.o_part[(row0 + static_cast<long long>(h) * p.splits) * kDLatent + f] = (hi[h] + lo[h]) * inv[h];
-        }
         if (t < 16) {
             float lv = 0.f, mv = 0.f;
 #pragma unroll
@@ -690,6 +678,26 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     mv = m_ref[h];
                 }
             p.lse_part[row0 + static_cast<long long>(t) * p.splits] = lv > 0.f ? (mv + log2f(lv)) * kLn2 : -INFINITY;
+        }
+        float inv[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) inv[h] = l_run[h] > 0.f ? __frcp_rn(l_run[h]) : 0.f;
+        const int gl = g - 1;
+        bool w = mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag);
+        w = __all_sync(0xffffffffu, w);
+        if (softmax_barrier_or(!w)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        float* o_row = p.o_part + row0 * kDLatent + t;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            float o[32];                                  // hi in 0..15, lo in 16..31
+            tmem_ld32(tmem + lane_addr + kTmemO + 32 * j, o);
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                o_row[static_cast<long long>(h) * p.splits * kDLatent + 128 * j] = (o[h] + o[16 + h]) * inv[h];
         }
         tc_fence_before_sync();
         mbar_arrive(&sh.o_free);
@@ -722,18 +730,24 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
         sh.abort_flag = 0;
         mbar_init_fence();
     }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&sh.tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = sh.tmem_base;
+    __syncthreads();                                     // barriers initialised
     // Inputs (d_pos, cache rows, indices, q) may be written by the kernel
     // before this one on the stream: wait for it before any global read.
     grid_dependency_wait();
     allow_dependent_launch();
+    if (warp == kPvWarp && lane == 1) load_q(maps, p, sh, first_key(p), l2_policy_evict_normal());
+    uint32_t tmem = 0;
+    if (warp >= kSoftmaxWarp0) {
+        // the tensor-memory users wait for the allocation; the producer does not
+        if (warp == kMmaWarp) {
+            tmem_alloc(&sh.tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before_sync();
+        named_barrier_sync(kBarTmem, kThreads - kProducerThreads);
+        tc_fence_after_sync();
+        tmem = sh.tmem_base;
+    }
     if (warp < 4) {
         producer(maps, p, sh, threadIdx.x);
     } else if (warp < kMmaWarp) {

@@ -360,6 +360,22 @@ def e2e_dense(bench, calls):
             "calls": calls}
 
 
+# --------------------------------------------------------------------------- replicas
+def max_over_ranks(elapsed: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it); identity at world 1."""
+    if world <= 1:
+        return elapsed
+    import torch.distributed as dist
+    t = torch.tensor([elapsed], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(alg_bytes_per_call: int, calls_per_rank: int, world: int, elapsed_max: float) -> float:
+    """Algorithmic bytes all ranks moved / the slowest rank's time, in GB/s."""
+    return world * alg_bytes_per_call * calls_per_rank / elapsed_max / 1e9
+
+
 # --------------------------------------------------------------------------- main arms
 def run_ours(args, rank, world):
     import decode_attention_mla_gb300 as mla
@@ -386,15 +402,13 @@ def run_ours(args, rank, world):
     with ClockSampler(dev_index) as clk:
         elapsed = time_graph(g, steps, warm)
     torch.cuda.synchronize()
+    elapsed = max_over_ranks(elapsed, world)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([elapsed], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
         dist.barrier()
     calls = steps * copies
     us_call = elapsed / calls * 1e6
-    value = world * bench.alg_bytes * calls / elapsed / 1e9
+    value = whole_job_gbs(bench.alg_bytes, calls, world, elapsed)
 
     # dominant kernel (split partial): live CUDA-event time per launch, same copies
     t_part = time_graph(gp, max(10, steps // 2), warm) / (max(10, steps // 2) * copies)

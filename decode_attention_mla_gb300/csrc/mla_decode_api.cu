@@ -253,6 +253,46 @@ int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void
                                              pl->shape.pdl != 0, static_cast<cudaStream_t>(stream)));
 }
 
+// Split count derived from the shape ("Launch Geometry", Lecture 04, s.4:
+// derive it, do not pin it): minimise the modelled partial-kernel time
+//   waves(S) * (kernel steps per slice(S) + 1),  waves = ceil(items / grid),
+// over S, where a slice is ceil(rows / S) rounded up to the kernel's granule,
+// a step is its tile (80 rows tcgen05, 32 rows warp-MMA) and only non-empty
+// slices are items; the smallest S wins ties.
+long long derive_splits(long long rows, long long pairs, long long grid_cap, int variant) {
+    const int tile = variant_tile_rows(variant);
+    const int granule = variant_granule(variant);
+    long long best_s = 1, best_cost = -1;
+    const long long s_hi = std::min<long long>(MLA_MAX_SPLITS, ceil_div(rows, granule));
+    for (long long S = 1; S <= s_hi; ++S) {
+        const long long per = mla::slice_entries(rows, static_cast<int>(S), granule);
+        const long long items = pairs * ceil_div(rows, per);
+        const long long waves = ceil_div(items, std::min(items, grid_cap));
+        const long long cost = waves * (ceil_div(per, tile) + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_s = S;
+        }
+    }
+    return best_s;
+}
+
+// Kernel choice when the caller leaves it open, from measurements on GB300:
+// the sparse gather moves more rows per SM with the warp-MMA kernel's
+// per-row bulk copies (the tcgen05 kernel's 16-byte gather is bound by the
+// requests an SM keeps in flight); dense decode with four or more head
+// groups, or with long slices (>= 320 rows per item), runs faster on tcgen05;
+// short dense slices are latency chains that the 32-row warp-MMA kernel
+// finishes sooner.
+constexpr long long kTcMinRowsPerItem = 320;
+int auto_variant(bool sparse, int head_groups, long long rows, long long pairs, long long grid_cap) {
+    if (sparse) return kVariantWarpMma;
+    if (head_groups >= 4) return kVariantTc;
+    const long long S = derive_splits(rows, pairs, grid_cap, kVariantTc);
+    const long long per = mla::slice_entries(rows, static_cast<int>(S), variant_granule(kVariantTc));
+    return per >= kTcMinRowsPerItem ? kVariantTc : kVariantWarpMma;
+}
+
 }  // namespace
 
 extern "C" {
@@ -275,38 +315,20 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     mla_decode_plan_t pl{};
     pl.shape = s;
     pl.magic = kPlanMagic;
-    pl.variant = s.variant == 0 ? kVariantTc : s.variant;
     pl.head_group = mla::kHeadGroup;
     pl.n_head_groups = s.heads / mla::kHeadGroup;
     pl.ctas_per_sm = kCtasPerSm;
     pl.num_sms = sms;
 
-    // Split count derived from the shape ("Launch Geometry", Lecture 04, s.4:
-    // derive it, do not pin it): minimise the modelled partial-kernel time
-    //   waves(S) * (stages per slice(S) + 1),  waves = ceil(items / grid),
-    // over S, where a slice is ceil(rows / S) rounded up to whole 32-row
-    // stages and only non-empty slices are items.
     const long long rows = s.sparse ? s.topk : s.max_ctx;
     const long long pairs = static_cast<long long>(s.batch) * pl.n_head_groups;
     const long long grid_cap = static_cast<long long>(kCtasPerSm) * sms;
-    const int tile = variant_tile_rows(pl.variant);
-    const int granule = variant_granule(pl.variant);
-    long long best_s = 1, best_cost = -1;
-    const long long s_hi = std::min<long long>(MLA_MAX_SPLITS, ceil_div(rows, granule));
-    for (long long S = 1; S <= s_hi; ++S) {
-        const long long per = mla::slice_entries(rows, static_cast<int>(S), granule);
-        const long long items = pairs * ceil_div(rows, per);
-        const long long waves = ceil_div(items, std::min(items, grid_cap));
-        const long long cost = waves * (ceil_div(per, tile) + 1);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best_s = S;
-        }
-    }
+    pl.variant = s.variant != 0 ? s.variant : auto_variant(s.sparse != 0, pl.n_head_groups, rows, pairs, grid_cap);
+    const long long best_s = derive_splits(rows, pairs, grid_cap, pl.variant);
     long long S = best_s;
     if (s.splits_override > 0) S = s.splits_override;
     pl.splits = static_cast<int>(S);
-    pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits, granule));
+    pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits, variant_granule(pl.variant)));
     const long long items = pairs * pl.splits;
     pl.grid_x = static_cast<int>(std::min(items, grid_cap));
     pl.grid_y = 1;

@@ -187,6 +187,34 @@ __device__ __forceinline__ int cursor_row(const Cursor& c) {
     return static_cast<int>(c.it.base) + c.it.e0 + c.k * kTileRows;
 }
 
+// Sparse: the request-local id of row t of a tile (or -1 past its rows),
+// with what it is checked against; fetched a tile or two before it is used
+// so the index load is off the gather's critical path.
+struct IdSlot {
+    int id, seg, rows;
+    long long base;
+    bool valid;
+};
+__device__ __forceinline__ IdSlot fetch_id(const PartialParams& p, const Cursor& c, int seg, int t) {
+    IdSlot s;
+    s.valid = c.valid;
+    s.id = -1;
+    s.seg = seg;
+    s.rows = 0;
+    s.base = 0;
+    if (c.valid) {
+        s.rows = rows_in_tile(c.it, c.k);
+        s.base = c.it.base;
+        if (t < s.rows) s.id = p.indices[static_cast<long long>(c.it.b) * p.topk + c.it.e0 + c.k * kTileRows + t];
+    }
+    return s;
+}
+// The absolute cache row of a fetched id, or -1 when the id is masked.
+__device__ __forceinline__ long long id_row(const PartialParams& p, const IdSlot& s) {
+    const long long row = s.base + s.id;
+    return (s.id >= 0 && s.id < s.seg && row >= 0 && row < p.kv_rows) ? row : -1;
+}
+
 __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int key,
                                        uint64_t policy) {
     const int b = key / p.n_groups;
@@ -211,9 +239,21 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     cursor_init(p, cur);
     // L2 prefetch runs two tiles ahead of the shared-memory loads: shared memory
     // holds two tiles, L2 the next two in flight
-    Cursor pf = cur;
-    for (int i = 0; i < 2 && pf.valid; ++i) cursor_step(p, pf);
-    int seg_len = 0;
+    Cursor nx = cur;
+    if (nx.valid) cursor_step(p, nx);
+    Cursor pf = nx;
+    if (pf.valid) cursor_step(p, pf);
+    // sparse: ids of this tile and the next, the segment length of the item the
+    // prefetch cursor is in
+    IdSlot id_cur{}, id_nx{};
+    int pf_seg = 0;
+    if (p.sparse && t < kTileRows) {
+        const int seg0 = cur.valid ? p.cache_len[cur.it.b] : 0;
+        const int seg1 = nx.valid ? (nx.it.b == cur.it.b ? seg0 : p.cache_len[nx.it.b]) : 0;
+        pf_seg = pf.valid ? (pf.it.b == nx.it.b ? seg1 : p.cache_len[pf.it.b]) : 0;
+        id_cur = fetch_id(p, cur, seg0, t);
+        id_nx = fetch_id(p, nx, seg1, t);
+    }
     // `stop` is uniform over the producer threads (sparse: agreed at a barrier)
     bool stop = false;
     while (cur.valid && !stop) {
@@ -232,7 +272,6 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 q_key = key;
                 ++q_loads;
             }
-            if (p.sparse) seg_len = p.cache_len[it.b];
         }
         const int buf = g & 1;
         if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
@@ -258,14 +297,9 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             // the buffer is free, or some thread saw the CTA abort
             stop = named_barrier_or(kBarProducer, kProducerThreads, sh.abort_flag != 0);
             if (stop) break;
-            // the tile's row ids, resolved once into shared memory
-            const int* idx = p.indices + static_cast<long long>(it.b) * p.topk + r0;
+            // the tile's row ids (fetched a tile ago), resolved once into shared memory
             if (t < kTileRows) {
-                long long row = -1;
-                if (t < rows) {
-                    const int id = idx[t];
-                    if (id >= 0 && id < seg_len && it.base + id >= 0 && it.base + id < p.kv_rows) row = it.base + id;
-                }
+                const long long row = id_row(p, id_cur);
                 sh.rowid[buf][t] = row;
                 sh.valid[buf][t] = row >= 0 ? 1 : 0;
             }
@@ -293,16 +327,13 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 }
                 cp_async_commit();
             }
-            if (pf.valid && t < kTileRows) {
-                // rows of the tile two ahead into L2 while this tile's copies land
-                const int pr0 = pf.it.e0 + pf.k * kTileRows;
-                if (t < rows_in_tile(pf.it, pf.k)) {
-                    const int id = p.indices[static_cast<long long>(pf.it.b) * p.topk + pr0 + t];
-                    const int plen = p.cache_len[pf.it.b];
-                    const long long prow = pf.it.base + id;
-                    if (id >= 0 && id < plen && prow >= 0 && prow < p.kv_rows)
-                        bulk_prefetch_l2(kvb + prow * stride_bytes, kRowBytes);
-                }
+            if (t < kTileRows) {
+                // the next tile's rows into L2 while this tile's copies land, and
+                // the ids of the tile after it
+                const long long nrow = id_nx.valid ? id_row(p, id_nx) : -1;
+                if (nrow >= 0) bulk_prefetch_l2(kvb + nrow * stride_bytes, kRowBytes);
+                id_cur = id_nx;
+                id_nx = fetch_id(p, pf, pf_seg, t);
             }
             cp_async_wait_group<2>();
             fence_proxy_async_smem();
@@ -314,7 +345,12 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             fence_proxy_async_smem();
             mbar_arrive(&sh.full[buf][2]);
         }
-        if (pf.valid) cursor_step(p, pf);
+        if (pf.valid) {
+            const int b_before = pf.it.b;
+            cursor_step(p, pf);
+            if (p.sparse && t < kTileRows && pf.valid && pf.it.b != b_before) pf_seg = p.cache_len[pf.it.b];
+        }
+        if (nx.valid) cursor_step(p, nx);
         cursor_step(p, cur);
     }
     // Never retire the CTA with copies into its shared memory in flight.

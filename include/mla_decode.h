@@ -85,8 +85,10 @@ typedef struct {
     float scale;          /* softmax scale, finite and > 0 (1/sqrt(576) for these shapes) */
     int num_sms;          /* SMs to plan for; 0 = query the current device */
     int splits_override;  /* 0 = derive; 1..MLA_MAX_SPLITS = force this split count */
-    int variant;          /* 0 = auto (2); 1 = warp-MMA (mma.sync) kernel, 32-row stages;
-                             2 = tcgen05/TMEM kernel, 80-row TMA tiles (both: 16 heads per CTA) */
+    int variant;          /* 1 = warp-MMA (mma.sync) kernel, 32-row stages; 2 = tcgen05/TMEM
+                             kernel, 80-row TMA tiles (both: 16 heads per CTA); 0 = auto:
+                             sparse -> 1; dense with >= 4 head groups -> 2; other dense -> 2
+                             when its slices hold >= 320 rows, else 1 (measured crossover) */
     int pdl;              /* 1 = launch with programmatic dependent launch */
 } mla_decode_shape;
 

@@ -66,19 +66,20 @@ def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     return best[1]
 
 
-@pytest.mark.parametrize("kw,splits,entries", [
-    (dict(max_ctx=256), 4, 64),
-    (dict(max_ctx=8192), 103, 80),
-    (dict(sparse=True, topk=2048), 26, 80),
-    (dict(batch=64, sparse=True, topk=2048), 2, 1024),
-    (dict(heads=128, max_ctx=32768 + 64), 19, 1728),
-    (dict(max_ctx=8192, variant=1), 128, 64),
-    (dict(sparse=True, topk=2048, variant=1), 64, 32),
+@pytest.mark.parametrize("kw,variant,splits,entries", [
+    (dict(max_ctx=256), 1, 8, 32),
+    (dict(max_ctx=8192), 1, 128, 64),
+    (dict(sparse=True, topk=2048), 1, 64, 32),
+    (dict(batch=64, sparse=True, topk=2048), 1, 2, 1024),
+    (dict(heads=128, max_ctx=32768 + 64), 2, 19, 1728),
+    (dict(max_ctx=131072), 2, 149, 880),
+    (dict(max_ctx=8192, variant=2), 2, 103, 80),
+    (dict(sparse=True, topk=2048, variant=2), 2, 26, 80),
+    (dict(batch=64, sparse=True, topk=2048, variant=2), 2, 2, 1024),
 ])
-def test_plan_derivation_for_the_workloads(kw, splits, entries):
+def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     p = _plan(**kw)
-    assert (p.splits, p.entries_per_split) == (splits, entries)
-    assert p.variant == (kw.get("variant") or 2)
+    assert (p.variant, p.splits, p.entries_per_split) == (variant, splits, entries)
     rows = kw.get("topk") or kw.get("max_ctx")
     B, H = kw.get("batch", 1), kw.get("heads", 16)
     assert p.splits * p.entries_per_split >= rows
@@ -104,15 +105,38 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
     assert ps.splits == p.splits
 
 
+def _model_auto(sparse, rows, pairs, groups, sms):
+    """The automatic kernel choice, restated: sparse -> warp-MMA; >= 4 head
+    groups -> tcgen05; else tcgen05 when its slices hold >= 320 rows."""
+    if sparse:
+        return 1
+    if groups >= 4:
+        return 2
+    S = _model_split(rows, pairs, sms, 2)
+    per = -(-(-(-rows // S)) // 16) * 16
+    return 2 if per >= 320 else 1
+
+
+@pytest.mark.parametrize("rows", [1, 100, 256, 8192, 20000, 32768, 65536, 131072])
+@pytest.mark.parametrize("batch,heads", [(1, 16), (4, 16), (1, 32), (1, 64), (2, 128)])
+@pytest.mark.parametrize("sparse", [False, True])
+def test_plan_automatic_kernel_choice(rows, batch, heads, sparse):
+    kw = dict(sparse=True, topk=rows) if sparse else dict(max_ctx=rows)
+    p = _plan(batch=batch, heads=heads, **kw)
+    v = _model_auto(sparse, rows, batch * heads // 16, heads // 16, 152)
+    assert p.variant == v
+    assert p.splits == _model_split(rows, batch * heads // 16, 152, v)
+
+
 def test_plan_scales_with_sm_count_and_is_deterministic():
-    a = _plan(max_ctx=131072, num_sms=132)
-    b = _plan(max_ctx=131072, num_sms=132)
+    a = _plan(max_ctx=131072, num_sms=132, variant=2)
+    b = _plan(max_ctx=131072, num_sms=132, variant=2)
     assert a.as_dict() == b.as_dict()
     assert a.splits == _model_split(131072, 1, 132) and a.grid_x <= 132
-    assert _plan(max_ctx=131072, num_sms=152).splits == _model_split(131072, 1, 152)
-    assert _plan(max_ctx=131072, batch=4, num_sms=132).splits == _model_split(131072, 4, 132)
+    assert _plan(max_ctx=131072, num_sms=152, variant=2).splits == _model_split(131072, 1, 152)
+    assert _plan(max_ctx=131072, batch=4, num_sms=132, variant=2).splits == _model_split(131072, 4, 132)
     # short contexts: one tile per slice
-    assert _plan(max_ctx=100, num_sms=152).entries_per_split <= 80
+    assert _plan(max_ctx=100, num_sms=152, variant=2).entries_per_split <= 80
 
 
 def test_plan_override():

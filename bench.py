@@ -168,6 +168,9 @@ class DenseBench:
     def partial(self, c, stream=None):
         self.mla.run(self.plan, self.args[c], self.scratch, stream)
 
+    def combine(self, c, stream=None):
+        self.mla.combine(self.plan, self.args[c], self.scratch, stream)
+
 
 class SparseBench:
     """Sparse decode; `copies` distinct caches when one cache is below 3x L2."""
@@ -204,6 +207,9 @@ class SparseBench:
 
     def partial(self, c, stream=None):
         self.mla.run(self.plan, self.args[c], self.scratch, stream)
+
+    def combine(self, c, stream=None):
+        self.mla.combine(self.plan, self.args[c], self.scratch, stream)
 
 
 class GraphBench:
@@ -480,14 +486,19 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- details (all workloads)
-def time_bench(bench, reps=200, warm=5):
+def time_bench(bench, reps=200, warm=5, with_combine=False):
     g = capture(bench.call, bench.copies)
     gp = capture(bench.partial, bench.copies)
     el = time_graph(g, reps, warm)
     elp = time_graph(gp, reps, warm)
     rep_list = per_rep_times(g, 20)
     us = el / (reps * bench.copies) * 1e6
-    return us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list]
+    res = (us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list])
+    if with_combine:
+        # the combines alone, on the partials the last replay left in scratch
+        gc = capture(bench.combine, bench.copies)
+        res = res + (time_graph(gc, reps, warm) / (reps * bench.copies) * 1e6,)
+    return res
 
 
 def time_graph_bench(gb, reps=10, warm=3):

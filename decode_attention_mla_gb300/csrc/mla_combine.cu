@@ -5,51 +5,59 @@
 // ("Graph-resident decode", Lecture 08, s.6: the merge is its own kernel with
 // a grid wider than n_head and no serial thread-0 prologue).
 //
-// Grid (B*H, 512/128): a CTA merges 128 output features of one (request,
-// head).  Only the slices that hold entries are read (the same slicing as the
-// partial kernel).  The 8 warps take contiguous runs of those slices; each
-// lane owns 4 consecutive features and loads its run's partials (16 at a time)
-// before the weights are known, so those loads are in flight together with
-// the lse loads.  Each warp adds its run in ascending slice order and the 8
-// run sums are added in warp order: a fixed association, so the result is
-// reproducible bit for bit.  An all-empty row set gives lse = -inf, out = 0.
+// Grid (ceil(B*H / U), 512/128) of 8-warp CTAs: a unit of W = 1, 2, 4 or 8
+// warps (fewer for fewer slices; U = 8 / W units per CTA, so batched decode
+// with short split lists runs few, full CTAs) merges 128 output features of
+// one (request, head) over all S slices (a slice without entries carries lse = -inf and
+// o = 0, written by the partial kernel, so the merge needs neither the
+// context length nor the slicing).  The 8 warps take contiguous runs of
+// slices; each lane owns 4 consecutive features and loads its run's partials
+// (16 at a time) before the weights are known, so those loads are in flight
+// together with the lse loads.  The max and the sum of exponentials are taken
+// in one pass of (max, sum) pairs.  Each warp adds its run in ascending slice
+// order and the run sums are added in warp order: a fixed association, so
+// the result is reproducible bit for bit.  An all-empty row set gives
+// lse = -inf, out = 0.
+#include <algorithm>
 #include <cmath>
 
 #include "device_utils.cuh"
 #include "mla_decode.h"
 #include "mla_internal.h"
-#include "slicing.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;                                        // most warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kBatch = 16;                                       // partials a lane loads at once
-static_assert(MLA_MAX_SPLITS <= kThreads, "one lse per thread");
+static_assert(MLA_MAX_SPLITS <= kThreads, "one lse per thread of an 8-warp unit");
 static_assert(MLA_MAX_SPLITS <= kWarps * 2 * kBatch, "a warp's run fits two load batches");
 
-__global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombineParams p) {
-    __shared__ float weight[MLA_MAX_SPLITS];
+template <int W>
+__global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombineParams p, int rows) {
+    __shared__ float weight[kThreads];                  // unit u's weights at u * 32 * unit_warps
     __shared__ float red_max[kWarps];
     __shared__ float red_sum[kWarps];
     __shared__ float4 part[kWarps][32];
     grid_dependency_wait();          // the partials come from the preceding kernel
     allow_dependent_launch();
-    const int bh = blockIdx.x;
-    const int b = bh / p.heads;
-    const int chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // W = warps per (request, head): 1, 2, 4 or 8
+    const int unit = warp / W;
+    const int wl = warp - unit * W;                    // warp within the unit
+    const int bh = blockIdx.x * (kWarps / W) + unit;   // (request, head) of this unit
+    const bool live = bh < rows;
+    const int chunk = blockIdx.y;
     const int S = p.splits;
-    // only the slices that hold entries were written by the partial kernel
-    long long base;
-    const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, b, &base);
-    const long long per = slice_entries(n, S, p.granule);
-    const int S_used = per > 0 ? static_cast<int>(min(static_cast<long long>(S), (n + per - 1) / per)) : 0;
-    const int run = (S_used + kWarps - 1) / kWarps;
-    const int s0 = warp * run;
-    const int s1 = min(S_used, s0 + run);
+    // Every slice holds a partial (the partial kernels write lse = -inf, o = 0
+    // for slices without entries), so nothing here depends on the context length.
+    const int tu = wl * 32 + lane;                     // thread within the unit: 32 * W >= S
+    const float ls = (live && tu < S) ? p.lse_part[static_cast<long long>(bh) * S + tu] : -INFINITY;
+    const int run = (S + W - 1) / W;                   // <= 2 * kBatch (the host sizes W that way)
+    const int s0 = wl * run;
+    const int s1 = live ? min(S, s0 + run) : s0;
 
     // the first batch of this warp's partials, loaded before the weights are known
     const float4* src = reinterpret_cast<const float4*>(p.o_part + static_cast<long long>(bh) * S * kDLatent) +
@@ -61,27 +69,36 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
         v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    // slice weights exp(lse_s - lse)
-    const int t = threadIdx.x;
-    const float ls = (t < S_used) ? p.lse_part[static_cast<long long>(bh) * S + t] : -INFINITY;
-    float mx = ls;
+    // (max, sum of exp relative to it) over the slices in one pass: a warp
+    // butterfly on the pairs (both partners form the same, commutative merge,
+    // so every lane ends with the same bits), then the unit's warps in order
+    float m = ls;
+    float e = (ls == -INFINITY) ? 0.f : 1.f;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red_max[warp] = mx;
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float e2 = __shfl_xor_sync(0xffffffffu, e, off);
+        const float nm = fmaxf(m, m2);
+        e = (nm == -INFINITY) ? 0.f : e * expf(m - nm) + e2 * expf(m2 - nm);
+        m = nm;
+    }
+    if (lane == 0) {
+        red_max[warp] = m;
+        red_sum[warp] = e;
+    }
     __syncthreads();
-    mx = red_max[0];
+    const int w0 = unit * W;
+    float mx = red_max[w0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w]);
-    float e = (mx == -INFINITY || t >= S_used) ? 0.f : expf(ls - mx);
+    for (int w = 1; w < W; ++w) mx = fmaxf(mx, red_max[w0 + w]);
+    float sum = 0.f;
+    if (mx != -INFINITY) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
-    if (lane == 0) red_sum[warp] = e;
-    __syncthreads();
-    float sum = red_sum[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) sum += red_sum[w];
+        for (int w = 0; w < W; ++w) sum += red_sum[w0 + w] * expf(red_max[w0 + w] - mx);
+    }
     const float total = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-    if (t < S_used) weight[t] = (mx == -INFINITY) ? 0.f : expf(ls - total);
+    float* wt = weight + unit * 32 * W;
+    if (tu < S) wt[tu] = (mx == -INFINITY) ? 0.f : expf(ls - total);
     __syncthreads();
 
     // this warp's run, ascending slice order
@@ -90,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     for (int i = 0; i < kBatch; ++i) {
         const int s = s0 + i;
         if (s < s1) {
-            const float w = weight[s];
+            const float w = wt[s];
             acc.x += w * v[i].x;
             acc.y += w * v[i].y;
             acc.z += w * v[i].z;
@@ -107,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
         for (int i = 0; i < kBatch; ++i) {
             const int s = s0 + kBatch + i;
             if (s < s1) {
-                const float w = weight[s];
+                const float w = wt[s];
                 acc.x += w * v[i].x;
                 acc.y += w * v[i].y;
                 acc.z += w * v[i].z;
@@ -117,11 +134,11 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     }
     part[warp][lane] = acc;
     __syncthreads();
-    if (warp == 0) {
-        float4 o = part[0][lane];
+    if (wl == 0 && live) {
+        float4 o = part[w0][lane];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) {
-            const float4 q = part[w][lane];
+        for (int w = 1; w < W; ++w) {
+            const float4 q = part[w0 + w][lane];
             o.x += q.x;
             o.y += q.y;
             o.z += q.z;
@@ -134,7 +151,20 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
 
 }  // namespace
 
+// Warps per (request, head) for S slices: enough threads for one lse each and
+// about 16 slices per warp (one load batch), rounded up to a power of two so
+// that 8 / W units share a CTA of 8 warps.
+int combine_unit_warps(int splits) {
+    const int need = std::max((splits + 31) / 32, std::min((splits + kBatch - 1) / kBatch, kWarps));
+    int w = 1;
+    while (w < need) w *= 2;
+    return w;
+}
 int combine_block_threads() { return kThreads; }
+int combine_grid_rows(int rows, int splits) {
+    const int per_cta = kWarps / combine_unit_warps(splits);
+    return (rows + per_cta - 1) / per_cta;
+}
 
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -147,7 +177,13 @@ cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pd
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+    const int rows = p.batch * p.heads;
+    switch (combine_unit_warps(p.splits)) {
+        case 1: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<1>, p, rows);
+        case 2: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<2>, p, rows);
+        case 4: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<4>, p, rows);
+        default: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<8>, p, rows);
+    }
 }
 
 }  // namespace mla

@@ -150,6 +150,9 @@ int check_plan(const mla_decode_plan_t* pl) {
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
     if (pl->grid_x < 1 || pl->grid_x > items || pl->grid_y != 1 || pl->grid_z != 1) return MLA_EINVAL;
     if (items > 0x7fffffffLL) return MLA_EINVAL;
+    if (pl->combine_grid_x != mla::combine_grid_rows(pl->shape.batch * pl->shape.heads, pl->splits) ||
+        pl->combine_grid_y != MLA_D_LATENT / mla::kCombineChunk || pl->combine_block != mla::combine_block_threads())
+        return MLA_EINVAL;
     return MLA_OK;
 }
 
@@ -336,7 +339,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.block = pl.variant == kVariantTc ? mla::partial_tc_block_threads() : mla::partial_mma_block_threads();
     pl.smem_bytes = static_cast<int>(pl.variant == kVariantTc ? mla::partial_tc_smem_bytes()
                                                               : mla::partial_mma_smem_bytes());
-    pl.combine_grid_x = s.batch * s.heads;
+    pl.combine_grid_x = mla::combine_grid_rows(s.batch * s.heads, pl.splits);
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
     pl.combine_block = mla::combine_block_threads();
 

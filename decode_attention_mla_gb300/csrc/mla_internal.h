@@ -89,6 +89,7 @@ size_t partial_tc_smem_bytes();
 int partial_tc_block_threads();
 cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
 int combine_block_threads();
+int combine_grid_rows(int rows, int splits);    // combine grid x for B*H rows
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
 
 // Static scratch (mla_static_scratch.cu): its address on `device` once set up

@@ -213,7 +213,12 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
 
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
-        if (it.n_stages == 0) continue;
+        if (it.n_stages == 0) {
+            write_empty_partial(p.o_part, p.lse_part,
+                                (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s,
+                                p.splits, w * 32 + lane, kComputeWarps * 32);
+            continue;
+        }
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
             if (!mbar_wait_bounded(&sh.q_full, q_loads & 1, &sh.abort_flag)) {

@@ -546,7 +546,12 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
-        if (it.n_tiles == 0) continue;
+        if (it.n_tiles == 0) {
+            write_empty_partial(p.o_part, p.lse_part,
+                                (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s,
+                                p.splits, t, kSoftmaxThreads);
+            continue;
+        }
         float m_ref[16], l_part[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {

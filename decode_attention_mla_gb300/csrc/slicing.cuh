@@ -3,6 +3,8 @@
 // combine kernel (which skips the slices that are empty), so both agree.
 #pragma once
 
+#include <cmath>
+
 #include "mla_internal.h"
 
 namespace mla {
@@ -35,6 +37,22 @@ __host__ __device__ __forceinline__ long long slice_entries(long long n, int spl
 __device__ __forceinline__ uint32_t slice_entries_u32(uint32_t n, uint32_t splits, uint32_t granule_pow2) {
     const uint32_t per = (n + splits - 1u) / splits;
     return (per + granule_pow2 - 1u) & ~(granule_pow2 - 1u);
+}
+
+// A slice without entries still gets its partial written: lse_s = -inf and
+// o_s = 0 for the 16 heads of the item, so the combine reads every slice
+// without re-deriving which ones are empty.  row0 = the partial row of head 0
+// ((b * H + first head) * S + s); `tid` / `nthreads` split the stores.
+__device__ __forceinline__ void write_empty_partial(float* o_part, float* lse_part, long long row0, int splits,
+                                                    int tid, int nthreads) {
+    constexpr int kVec = kDLatent / 4;                   // float4 per partial row
+    for (int i = tid; i < kHeadGroup * kVec; i += nthreads) {
+        const int h = i / kVec;
+        const int v = i - h * kVec;
+        reinterpret_cast<float4*>(o_part + (row0 + static_cast<long long>(h) * splits) * kDLatent)[v] =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < kHeadGroup) lse_part[row0 + static_cast<long long>(tid) * splits] = -INFINITY;
 }
 
 }  // namespace mla

@@ -86,7 +86,8 @@ def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
     assert p.n_head_groups == H // 16 and p.ctas_per_sm == 1
     assert p.grid_x == min(B * p.n_head_groups * p.splits, 152) and p.grid_y == 1 and p.grid_z == 1
-    assert p.combine_grid_x == B * H and p.combine_grid_y == 4
+    assert p.combine_grid_x == -(-B * H // (8 // _unit_warps(p.splits))) and p.combine_grid_y == 4
+    assert p.combine_block == 256
     # scratch layout: status word, then o_part, then lse_part, 256-byte aligned
     bh = B * H
     assert p.status_offset == 0 and p.o_part_offset % 256 == 0 and p.lse_part_offset % 256 == 0
@@ -126,6 +127,32 @@ def test_plan_automatic_kernel_choice(rows, batch, heads, sparse):
     v = _model_auto(sparse, rows, batch * heads // 16, heads // 16, 152)
     assert p.variant == v
     assert p.splits == _model_split(rows, batch * heads // 16, 152, v)
+
+
+def _unit_warps(splits):
+    """Warps that merge one (request, head): one lse per thread, about 16
+    slices per warp up to 8 warps, rounded up to a power of two."""
+    need = max(-(-splits // 32), min(-(-splits // 16), 8))
+    w = 1
+    while w < need:
+        w *= 2
+    return w
+
+
+@pytest.mark.parametrize("splits", [1, 2, 16, 17, 32, 33, 100, 128, 149, 256])
+@pytest.mark.parametrize("batch", [1, 3, 64])
+def test_combine_grid_follows_the_split_count(splits, batch):
+    p = _plan(max_ctx=131072, splits=splits, batch=batch)
+    w = _unit_warps(splits)
+    assert 32 * w >= splits and -(-splits // w) <= 32
+    assert p.combine_block == 256
+    assert p.combine_grid_x == -(-batch * 16 // (8 // w))
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.combine_grid_x += 1
+    assert _call("mla_decode_combine", bad, _args(row_offset=0x60000)) == mla.EINVAL
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.combine_block = 128
+    assert _call("mla_decode_combine", bad, _args(row_offset=0x60000)) == mla.EINVAL
 
 
 def test_plan_scales_with_sm_count_and_is_deterministic():

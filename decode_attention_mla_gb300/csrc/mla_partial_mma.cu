@@ -81,19 +81,25 @@ __device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* statu
 
 struct Item {
     int b, hg, s, n_stages;
-    long long base, e0, e1;
+    long long base;
+    uint32_t e0, e1;                      // entries [e0, e1) of the request
 };
 
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     Item it;
-    it.hg = item % p.n_groups;
-    const int rest = item / p.n_groups;
-    it.s = rest % p.splits;
-    it.b = rest / p.splits;
-    const long long n = request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base);
-    const long long per = slice_entries(n, p.splits, p.granule);
-    long long e0 = static_cast<long long>(it.s) * per;
-    long long e1 = e0 + per;
+    const uint32_t ui = static_cast<uint32_t>(item);
+    const uint32_t rest = ui / static_cast<uint32_t>(p.n_groups);
+    it.hg = static_cast<int>(ui - rest * static_cast<uint32_t>(p.n_groups));
+    const uint32_t b = rest / static_cast<uint32_t>(p.splits);
+    it.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
+    it.b = static_cast<int>(b);
+    // entry counts are below 2^31 (d_pos and the list length are int32), so
+    // the slice arithmetic runs in 32 bits (64-bit division is slow)
+    const uint32_t n = static_cast<uint32_t>(
+        request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
+    const uint32_t per = slice_entries_u32(n, static_cast<uint32_t>(p.splits), kStageRows);
+    uint32_t e0 = static_cast<uint32_t>(it.s) * per;
+    uint32_t e1 = e0 + per;
     if (e1 > n) e1 = n;
     if (e0 > e1) e0 = e1;
     it.e0 = e0;
@@ -102,12 +108,34 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     return it;
 }
 
+// Query tile of the CTA's first item: known without the context length.
+__device__ __forceinline__ int first_key(const PartialParams& p) {
+    const int item = static_cast<int>(blockIdx.x);
+    const int rest = item / p.n_groups;
+    return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
+}
+
+__device__ __forceinline__ void load_q(const PartialParams& p, SharedStorage& sh, int key, int lane) {
+    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full, kHeadGroup * kRowBytes);
+    __syncwarp();
+    if (lane < kHeadGroup) {
+        const int b = key / p.n_groups;
+        const int hg = key - b * p.n_groups;
+        const uint16_t* src = p.q + (static_cast<long long>(b) * p.heads + hg * kHeadGroup + lane) * kDRow;
+        bulk_copy_g2s(sh.q[lane], src, kRowBytes, &sh.q_full, l2_policy_evict_normal());
+    }
+}
+
 // ============================== producer ==================================
 __device__ void producer(const PartialParams& p, SharedStorage& sh, int lane) {
     const uint64_t policy = l2_policy_evict_first();
     int stage = 0;            // stages issued so far (ring position)
-    int q_loads = 0;          // query tiles staged so far
-    int q_key = -1;
+    // the first query tile is requested before the context length is read; the
+    // MMA warps follow the same sequence of keys (a new tile whenever a busy
+    // item's key differs) and release a tile through q_empty, read or not
+    int q_key = first_key(p);
+    load_q(p, sh, q_key, lane);
+    int q_loads = 1;          // query tiles staged so far
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
@@ -115,17 +143,11 @@ __device__ void producer(const PartialParams& p, SharedStorage& sh, int lane) {
         const int seg_len = p.sparse ? p.cache_len[it.b] : 0;
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
-            if (q_loads > 0 && !mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
+            if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(&sh.q_full, kHeadGroup * kRowBytes);
-            __syncwarp();
-            if (lane < kHeadGroup) {
-                const uint16_t* src =
-                    p.q + (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup + lane) * kDRow;
-                bulk_copy_g2s(sh.q[lane], src, kRowBytes, &sh.q_full, l2_policy_evict_normal());
-            }
+            load_q(p, sh, key, lane);
             q_key = key;
             ++q_loads;
         }
@@ -207,8 +229,9 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
     uint32_t qa[kKStepsPerWarp][4];
     int stage = 0;
     int red_round = 0;
-    int q_loads = 0;
-    int q_key = -1;
+    int q_phase = 0;                       // query tiles consumed (q_full phases)
+    int q_key = first_key(p);              // key of the tile the producer loaded last
+    bool q_in_regs = false;                // that tile is in registers (and released)
     bool ok = true;
 
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
@@ -221,7 +244,22 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
         }
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
-            if (!mbar_wait_bounded(&sh.q_full, q_loads & 1, &sh.abort_flag)) {
+            // the producer loads another tile over this one: release it, read or
+            // not (it must have landed first)
+            if (!q_in_regs) {
+                if (!mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.q_empty);
+            }
+            ++q_phase;
+            q_key = key;
+            q_in_regs = false;
+        }
+        if (!q_in_regs) {
+            if (!mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
             }
@@ -236,8 +274,7 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.q_empty);
-            q_key = key;
-            ++q_loads;
+            q_in_regs = true;
         }
 
         float o[kPVTiles][4];

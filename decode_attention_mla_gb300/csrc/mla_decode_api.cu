@@ -227,7 +227,12 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
         if (rc != MLA_OK) return rc;
         return launch_status(mla::launch_partial_tc(maps, p, grid, pl->shape.pdl != 0, st));
     }
-    return launch_status(mla::launch_partial_mma(p, grid, pl->shape.pdl != 0, st));
+    // warp-MMA kernel: the query tile by TMA, cache rows by per-row bulk copies
+    mla::TcMaps maps{};
+    rc = encode_bf16_row_chunks(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads, MLA_D_ROW,
+                                mla::kHeadGroup, MLA_D_ROW / 64);
+    if (rc != MLA_OK) return rc;
+    return launch_status(mla::launch_partial_mma(maps, p, grid, pl->shape.pdl != 0, st));
 }
 
 int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void* scratch, size_t bytes,

@@ -73,6 +73,7 @@ struct AppendParams {
 // tensor cores read.  kv: boxes of 64 x 80 rows x 3 chunks (a third of a
 // tile); q: boxes of 64 x 16 heads x 9 chunks (the whole head group).
 constexpr int kTcBoxChunks = 3;
+// The warp-MMA kernel uses the same query map (its cache map is unused).
 struct TcMaps {
     CUtensorMap kv;
     CUtensorMap q;
@@ -83,7 +84,7 @@ cudaError_t partial_mma_prepare(int device);
 size_t partial_mma_smem_bytes();
 int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
-cudaError_t launch_partial_mma(const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
 cudaError_t partial_tc_prepare(int device);
 size_t partial_tc_smem_bytes();
 int partial_tc_block_threads();

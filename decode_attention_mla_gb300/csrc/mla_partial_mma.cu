@@ -40,6 +40,7 @@
 #include "mla_decode.h"
 #include "mla_internal.h"
 #include "slicing.cuh"
+#include "tc_utils.cuh"
 
 namespace mla {
 namespace {
@@ -57,13 +58,20 @@ constexpr int kPVTiles = kFeatPerWarp / 8;                // 8
 constexpr int kPSteps = kStageRows / 16;                  // 2
 constexpr int kIdxPrefetch = 4;                           // sparse index prefetch depth (stages)
 constexpr float kLn2 = 0.6931471805599453f;
+// Cache rows arrive by one 1152-byte bulk copy per row into padded 1168-byte
+// rows (8 consecutive rows hit 8 distinct 16-byte bank groups); the query tile
+// is one TMA box [9 chunks][16 rows][64 bf16], 128-byte swizzled.  (A TMA box
+// for whole dense stages was measured too: faster for single-stage slices,
+// slower for two-stage ones and for the timed T = 8192 shape.)
+constexpr int kChunks = kDRow / 64;                       // 9
+constexpr int kQChunkBytes = kHeadGroup * 128;            // 2048
 
 static_assert(kComputeWarps == 2 * kKGroups, "warp w: k-group w % 4, row half w / 4");
 static_assert(kDRow / 16 % kKGroups == 0, "contraction split");
 
-struct __align__(128) SharedStorage {
-    uint8_t kv[kStages][kStageRows][kSmemRow];
-    uint8_t q[kHeadGroup][kSmemRow];                      // the item's 16 query rows
+struct __align__(1024) SharedStorage {
+    uint8_t q[kChunks * kQChunkBytes];                    // the item's 16 query rows (1024-byte aligned)
+    uint8_t kv[kStages][kStageRows * kSmemRow];           // stage slots
     float4 red[2][kKGroups][kNT][32];                     // per-k-group partial scores
     int valid[kStages][kStageRows];
     uint64_t full[kStages];
@@ -74,6 +82,11 @@ struct __align__(128) SharedStorage {
     int abort_flag;
 };
 
+// Byte offset of byte b of row r in a 128-byte-swizzled chunk-major tile whose
+// 64-column chunks are chunk_bytes apart (b a multiple of 16 for ldmatrix rows).
+__device__ __forceinline__ uint32_t sw_off(int r, int b, int chunk_bytes) {
+    return static_cast<uint32_t>((b >> 7) * chunk_bytes + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15));
+}
 __device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* status) {
     sh.abort_flag = 1;
     if (status) atomicCAS(status, 0, static_cast<int>(MLA_EDEVICE));
@@ -115,26 +128,25 @@ __device__ __forceinline__ int first_key(const PartialParams& p) {
     return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
 }
 
-__device__ __forceinline__ void load_q(const PartialParams& p, SharedStorage& sh, int key, int lane) {
-    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full, kHeadGroup * kRowBytes);
-    __syncwarp();
-    if (lane < kHeadGroup) {
+__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int key,
+                                       int lane) {
+    if (lane == 0) {
         const int b = key / p.n_groups;
         const int hg = key - b * p.n_groups;
-        const uint16_t* src = p.q + (static_cast<long long>(b) * p.heads + hg * kHeadGroup + lane) * kDRow;
-        bulk_copy_g2s(sh.q[lane], src, kRowBytes, &sh.q_full, l2_policy_evict_normal());
+        mbar_arrive_expect_tx(&sh.q_full, kChunks * kQChunkBytes);
+        tma_load_3d(sh.q, &maps.q, 0, b * p.heads + hg * kHeadGroup, 0, &sh.q_full, l2_policy_evict_normal());
     }
 }
 
 // ============================== producer ==================================
-__device__ void producer(const PartialParams& p, SharedStorage& sh, int lane) {
+__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int lane) {
     const uint64_t policy = l2_policy_evict_first();
     int stage = 0;            // stages issued so far (ring position)
     // the first query tile is requested before the context length is read; the
     // MMA warps follow the same sequence of keys (a new tile whenever a busy
     // item's key differs) and release a tile through q_empty, read or not
     int q_key = first_key(p);
-    load_q(p, sh, q_key, lane);
+    load_q(maps, p, sh, q_key, lane);
     int q_loads = 1;          // query tiles staged so far
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
@@ -147,7 +159,7 @@ __device__ void producer(const PartialParams& p, SharedStorage& sh, int lane) {
                 ok = false;
                 break;
             }
-            load_q(p, sh, key, lane);
+            load_q(maps, p, sh, key, lane);
             q_key = key;
             ++q_loads;
         }
@@ -189,7 +201,7 @@ __device__ void producer(const PartialParams& p, SharedStorage& sh, int lane) {
                 const long long en = it.e0 + static_cast<long long>(st + kIdxPrefetch) * kStageRows + lane;
                 idx_pf[kIdxPrefetch - 1] = (en < it.e1) ? idx[en] : -1;
             }
-            uint8_t* dst = sh.kv[slot][lane];
+            uint8_t* dst = sh.kv[slot] + lane * kSmemRow;
             sh.valid[slot][lane] = valid ? 1 : 0;
             if (!valid) {
                 // masked rows still feed P . V (with p = 0): keep them finite
@@ -224,7 +236,7 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
     const int f_base = w * kFeatPerWarp;   // own output features
     const int lrow = lane & 7;
     const int lmat = lane >> 3;
-    const uint32_t q_base = smem_u32(&sh.q[0][0]);
+    const uint32_t q_base = smem_u32(sh.q);
 
     uint32_t qa[kKStepsPerWarp][4];
     int stage = 0;
@@ -267,10 +279,10 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
 #pragma unroll
             for (int kk = 0; kk < kKStepsPerWarp; ++kk) {
                 const int cb = ((kg * kKStepsPerWarp + kk) * 16 + 2 * tq) * 2;
-                qa[kk][0] = ld_shared_u32(q_base + g * kSmemRow + cb);
-                qa[kk][1] = ld_shared_u32(q_base + (g + 8) * kSmemRow + cb);
-                qa[kk][2] = ld_shared_u32(q_base + g * kSmemRow + cb + 16);
-                qa[kk][3] = ld_shared_u32(q_base + (g + 8) * kSmemRow + cb + 16);
+                qa[kk][0] = ld_shared_u32(q_base + sw_off(g, cb, kQChunkBytes));
+                qa[kk][1] = ld_shared_u32(q_base + sw_off(g + 8, cb, kQChunkBytes));
+                qa[kk][2] = ld_shared_u32(q_base + sw_off(g, cb + 16, kQChunkBytes));
+                qa[kk][3] = ld_shared_u32(q_base + sw_off(g + 8, cb + 16, kQChunkBytes));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.q_empty);
@@ -289,7 +301,7 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
                 ok = false;
                 break;
             }
-            const uint32_t kv_base = smem_u32(&sh.kv[slot][0][0]);
+            const uint32_t kv_base = smem_u32(sh.kv[slot]);
 
             // ---- partial scores: rows 16rh..16rh+15, this warp's 144 features
             float acc[2][4];
@@ -428,9 +440,11 @@ __device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int l
     if (!ok && lane == 0) raise_device_error(sh, p.status);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const PartialParams p) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    SharedStorage& sh = *reinterpret_cast<SharedStorage*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __grid_constant__ TcMaps maps,
+                                                                       const PartialParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    SharedStorage& sh =
+        *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -450,38 +464,39 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const Part
     grid_dependency_wait();
     allow_dependent_launch();
     if (warp == kProducerWarp)
-        producer(p, sh, lane);
+        producer(maps, p, sh, lane);
     else
         consumer(p, sh, warp, lane);
 }
 
 }  // namespace
 
-size_t partial_mma_smem_bytes() { return sizeof(SharedStorage); }
+size_t partial_mma_smem_bytes() { return sizeof(SharedStorage) + 1024; }
 int partial_mma_block_threads() { return kThreads; }
 
 cudaError_t partial_mma_prepare(int /*device*/) {
     return cudaFuncSetAttribute(mla_partial_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(sizeof(SharedStorage)));
+                                static_cast<int>(partial_mma_smem_bytes()));
 }
 
 cudaError_t partial_mma_occupancy(int* ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, mla_partial_mma_kernel, kThreads,
-                                                         sizeof(SharedStorage));
+                                                         partial_mma_smem_bytes());
 }
 
-cudaError_t launch_partial_mma(const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream) {
+cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl,
+                               cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(SharedStorage);
+    cfg.dynamicSmemBytes = partial_mma_smem_bytes();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel, p);
+    return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel, maps, p);
 }
 
 }  // namespace mla

@@ -26,9 +26,13 @@ constexpr int kCtasPerSm = 1;
 constexpr size_t kScratchAlign = 256;
 constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 32-row stages
 constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
+constexpr int kVariantTc32 = 3;              // tcgen05 head-group-32 kernel, 64-row tiles (dense)
 
-int variant_tile_rows(int v) { return v == kVariantTc ? mla::kTcTileRows : mla::kStageRows; }
-int variant_granule(int v) { return v == kVariantTc ? mla::kTcGranule : mla::kStageRows; }
+int variant_tile_rows(int v) {
+    return v == kVariantTc ? mla::kTcTileRows : v == kVariantTc32 ? mla::kTcTileRows32 : mla::kStageRows;
+}
+int variant_granule(int v) { return v == kVariantWarpMma ? mla::kStageRows : mla::kTcGranule; }
+int variant_head_group(int v) { return v == kVariantTc32 ? 32 : mla::kHeadGroup; }
 
 // cuTensorMapEncodeTiled, reached through the runtime (no link-time libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -131,13 +135,15 @@ int check_shape(const mla_decode_shape* s) {
     if (s->batch < 1 || s->batch > 65535) return MLA_EINVAL;
     if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
-    if (s->variant < 0 || s->variant > 2) return MLA_EINVAL;
+    if (s->variant < 0 || s->variant > 3) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
     if (!s->sparse && s->max_ctx < 1) return MLA_EINVAL;
     if (s->sparse && s->topk < 1) return MLA_EINVAL;
     if (s->d_latent != MLA_D_LATENT || s->d_rope != MLA_D_ROPE) return MLA_EUNSUPPORTED;
     if (s->heads != 16 && s->heads != 32 && s->heads != 64 && s->heads != 128) return MLA_EUNSUPPORTED;
+    // 32 heads per CTA: dense decode with a multiple of 32 heads
+    if (s->variant == kVariantTc32 && (s->sparse || s->heads % 32 != 0)) return MLA_EUNSUPPORTED;
     return MLA_OK;
 }
 
@@ -145,8 +151,10 @@ int check_plan(const mla_decode_plan_t* pl) {
     if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
     if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
-    if (pl->variant != kVariantWarpMma && pl->variant != kVariantTc) return MLA_EINVAL;
-    if (pl->head_group != mla::kHeadGroup || pl->n_head_groups * pl->head_group != pl->shape.heads) return MLA_EINVAL;
+    if (pl->variant != kVariantWarpMma && pl->variant != kVariantTc && pl->variant != kVariantTc32) return MLA_EINVAL;
+    if (pl->variant == kVariantTc32 && pl->shape.sparse) return MLA_EINVAL;
+    if (pl->head_group != variant_head_group(pl->variant) || pl->n_head_groups * pl->head_group != pl->shape.heads)
+        return MLA_EINVAL;
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
     if (pl->grid_x < 1 || pl->grid_x > items || pl->grid_y != 1 || pl->grid_z != 1) return MLA_EINVAL;
     if (items > 0x7fffffffLL) return MLA_EINVAL;
@@ -216,16 +224,18 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
     const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
-    if (pl->variant == kVariantTc) {
+    if (pl->variant == kVariantTc || pl->variant == kVariantTc32) {
         // TMA coordinates are 32-bit: the cache must be addressable by them
         if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
+        const int hg = variant_head_group(pl->variant);
         mla::TcMaps maps;
-        rc = encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kTcTileRows, mla::kTcBoxChunks);
+        rc = encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride,
+                                    static_cast<uint32_t>(variant_tile_rows(pl->variant)), mla::kTcBoxChunks);
         if (rc == MLA_OK)
             rc = encode_bf16_row_chunks(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads,
-                                        MLA_D_ROW, mla::kHeadGroup, MLA_D_ROW / 64);
+                                        MLA_D_ROW, static_cast<uint32_t>(hg), MLA_D_ROW / 64);
         if (rc != MLA_OK) return rc;
-        return launch_status(mla::launch_partial_tc(maps, p, grid, pl->shape.pdl != 0, st));
+        return launch_status(mla::launch_partial_tc(maps, p, hg, grid, pl->shape.pdl != 0, st));
     }
     // warp-MMA kernel: the query tile by TMA, cache rows by per-row bulk copies
     mla::TcMaps maps{};
@@ -288,17 +298,26 @@ long long derive_splits(long long rows, long long pairs, long long grid_cap, int
 // Kernel choice when the caller leaves it open, from measurements on GB300:
 // the sparse gather moves more rows per SM with the warp-MMA kernel's
 // per-row bulk copies (the tcgen05 kernel's 16-byte gather is bound by the
-// requests an SM keeps in flight); dense decode with four or more head
-// groups, or with long slices (>= 320 rows per item), runs faster on tcgen05;
-// short dense slices are latency chains that the 32-row warp-MMA kernel
-// finishes sooner.
+// requests an SM keeps in flight); dense decode with 64 or more heads runs
+// fastest on the tcgen05 kernel with 32 heads per CTA (half the MMA
+// instructions and cache-row re-reads per head), and so does 32-head decode
+// with long slices (>= 256 rows per item); other dense shapes take the
+// 16-head tcgen05 kernel for long slices (>= 320 rows per item) and the
+// 32-row warp-MMA kernel for short ones (latency chains it finishes sooner).
+constexpr long long kTc32MinRowsPerItem = 256;
 constexpr long long kTcMinRowsPerItem = 320;
-int auto_variant(bool sparse, int head_groups, long long rows, long long pairs, long long grid_cap) {
+long long rows_per_item(long long rows, int batch, int heads, long long grid_cap, int variant) {
+    const long long pairs = static_cast<long long>(batch) * (heads / variant_head_group(variant));
+    const long long S = derive_splits(rows, pairs, grid_cap, variant);
+    return mla::slice_entries(rows, static_cast<int>(S), variant_granule(variant));
+}
+int auto_variant(bool sparse, int batch, int heads, long long rows, long long grid_cap) {
     if (sparse) return kVariantWarpMma;
-    if (head_groups >= 4) return kVariantTc;
-    const long long S = derive_splits(rows, pairs, grid_cap, kVariantTc);
-    const long long per = mla::slice_entries(rows, static_cast<int>(S), variant_granule(kVariantTc));
-    return per >= kTcMinRowsPerItem ? kVariantTc : kVariantWarpMma;
+    if (heads >= 64) return kVariantTc32;
+    if (heads == 32 && rows_per_item(rows, batch, heads, grid_cap, kVariantTc32) >= kTc32MinRowsPerItem)
+        return kVariantTc32;
+    return rows_per_item(rows, batch, heads, grid_cap, kVariantTc) >= kTcMinRowsPerItem ? kVariantTc
+                                                                                        : kVariantWarpMma;
 }
 
 }  // namespace
@@ -323,26 +342,29 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     mla_decode_plan_t pl{};
     pl.shape = s;
     pl.magic = kPlanMagic;
-    pl.head_group = mla::kHeadGroup;
+    pl.head_group = mla::kHeadGroup;                      // set again once the kernel is chosen
     pl.n_head_groups = s.heads / mla::kHeadGroup;
     pl.ctas_per_sm = kCtasPerSm;
     pl.num_sms = sms;
 
     const long long rows = s.sparse ? s.topk : s.max_ctx;
-    const long long pairs = static_cast<long long>(s.batch) * pl.n_head_groups;
     const long long grid_cap = static_cast<long long>(kCtasPerSm) * sms;
-    pl.variant = s.variant != 0 ? s.variant : auto_variant(s.sparse != 0, pl.n_head_groups, rows, pairs, grid_cap);
-    const long long best_s = derive_splits(rows, pairs, grid_cap, pl.variant);
+    pl.variant = s.variant != 0 ? s.variant : auto_variant(s.sparse != 0, s.batch, s.heads, rows, grid_cap);
+    pl.head_group = variant_head_group(pl.variant);
+    pl.n_head_groups = s.heads / pl.head_group;
+    const long long best_s =
+        derive_splits(rows, static_cast<long long>(s.batch) * pl.n_head_groups, grid_cap, pl.variant);
     long long S = best_s;
     if (s.splits_override > 0) S = s.splits_override;
     pl.splits = static_cast<int>(S);
     pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits, variant_granule(pl.variant)));
-    const long long items = pairs * pl.splits;
+    const long long items = static_cast<long long>(s.batch) * pl.n_head_groups * pl.splits;
     pl.grid_x = static_cast<int>(std::min(items, grid_cap));
     pl.grid_y = 1;
     pl.grid_z = 1;
-    pl.block = pl.variant == kVariantTc ? mla::partial_tc_block_threads() : mla::partial_mma_block_threads();
-    pl.smem_bytes = static_cast<int>(pl.variant == kVariantTc ? mla::partial_tc_smem_bytes()
+    const bool tc = pl.variant == kVariantTc || pl.variant == kVariantTc32;
+    pl.block = tc ? mla::partial_tc_block_threads(pl.head_group) : mla::partial_mma_block_threads();
+    pl.smem_bytes = static_cast<int>(tc ? mla::partial_tc_smem_bytes(pl.head_group)
                                                               : mla::partial_mma_smem_bytes());
     pl.combine_grid_x = mla::combine_grid_rows(s.batch * s.heads, pl.splits);
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;

@@ -14,9 +14,10 @@ constexpr int kDRope = 64;
 constexpr int kDRow = kDLatent + kDRope;       // 576 bf16 per cache row
 constexpr int kRowBytes = kDRow * 2;           // 1152
 constexpr int kStageRows = 32;                 // rows per pipeline stage (warp-MMA partial kernel)
-constexpr int kTcTileRows = 80;                // rows per tile (tcgen05 partial kernel)
+constexpr int kTcTileRows = 80;                // rows per tile (tcgen05 partial kernel, 16 heads per CTA)
+constexpr int kTcTileRows32 = 64;              // rows per tile (tcgen05 partial kernel, 32 heads per CTA)
 constexpr int kTcGranule = 16;                 // slice granule of the tcgen05 kernel (one MMA k-step)
-constexpr int kHeadGroup = 16;                 // heads per CTA of the warp-MMA kernel
+constexpr int kHeadGroup = 16;                 // heads per CTA (warp-MMA kernel; tcgen05 kernel: 16 or 32)
 constexpr int kCombineChunk = 128;             // features per combine CTA
 // Size of the library's own scratch array used by mla_decode_forward_static
 // (8 MiB: e.g. 16 heads x 256 slices x 2 KiB partial rows fits with room).
@@ -33,7 +34,7 @@ struct PartialParams {
     const int* cache_len;       // sparse [B]
     const int* indices;         // sparse [B][topk]
     int batch, heads, topk, splits, sparse;
-    int n_groups;               // heads / kHeadGroup
+    int n_groups;               // heads / head group
     int granule;                // slices are whole multiples of this many entries
     int n_items;                // batch * n_groups * splits work items, walked round-robin by the CTAs
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units
@@ -86,9 +87,10 @@ int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
 cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
 cudaError_t partial_tc_prepare(int device);
-size_t partial_tc_smem_bytes();
-int partial_tc_block_threads();
-cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);
+size_t partial_tc_smem_bytes(int head_group);
+int partial_tc_block_threads(int head_group);
+cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int head_group, dim3 grid, bool pdl,
+                              cudaStream_t stream);
 int combine_block_threads();
 int combine_grid_rows(int rows, int splits);    // combine grid x for B*H rows
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);

@@ -1,26 +1,28 @@
 // mla_partial_tc.cu -- split-KV MLA decode partials on the 5th-generation
-// tensor cores (tcgen05 + tensor memory), head group of 16.
+// tensor cores (tcgen05 + tensor memory), head groups of 16 or 32.
 //
 // Same work decomposition as the warp-MMA kernel: work item = (request b,
-// head group hg of 16 heads, context slice s); a persistent grid of at most
-// one CTA per SM walks the items round-robin ("Launch Geometry", Lecture 04,
-// s.1, s.4, s.8); each item yields one online-softmax partial (o_s
+// head group hg, context slice s); a persistent grid of at most one CTA per
+// SM walks the items round-robin ("Launch Geometry", Lecture 04, s.1, s.4,
+// s.8); each item yields one online-softmax partial per head (o_s
 // normalised, lse_s) that a separate kernel merges ("Graph-resident decode",
 // Lecture 08, s.6).
 //
-// A slice is walked in tiles of 80 cache rows, double-buffered in shared
-// memory as 9 column chunks of [80 rows x 64 bf16] in the 128-byte-swizzled
-// layout the tensor cores read; a tile arrives as three TMA boxes of three
-// chunks, each with its own barrier, so the score MMAs start on the first
-// third while the rest is in flight.  With the 16 heads of a group the
-// products are taken "swapped", so the long axis (cache rows, or latent
-// features) is the 128-wide M of the MMA and the 16 heads are N:
-//   S^T[rows x 16]   = K_tile[rows x 576] . Q^T           36 MMAs, M=128 (80 valid rows), N=16
-//   O^T[512 x 32]   += V_tile^T[512 x rows] . [P_hi | P_lo]^T
-//                                                          4 x 5 MMAs, M=128 features, N=32
+// A slice is walked in tiles of TR cache rows (80 for head groups of 16, 64
+// for 32), double-buffered in shared memory as 9 column chunks of
+// [TR rows x 64 bf16] in the 128-byte-swizzled layout the tensor cores read;
+// a tile arrives as three TMA boxes of three chunks, each with its own
+// barrier, so the score MMAs start on the first third while the rest is in
+// flight.  The products are taken "swapped", so the long axis (cache rows,
+// or latent features) is the 128-wide M of the MMA and the HG heads are N:
+//   S^T[rows x HG]   = K_tile[rows x 576] . Q^T         36 MMAs, M=128 (TR valid rows), N=HG
+//   O^T[512 x 2HG]  += V_tile^T[512 x rows] . [P_hi | P_lo]^T
+//                                                        4 x TR/16 MMAs, M=128 features, N=2HG
 // P enters the second product as a bf16 pair P = P_hi + P_lo laid side by
 // side along N (~16 significant bits of P in one MMA); O = O_hi + O_lo at the
-// end.  Scores and O live in tensor memory (fp32).
+// end.  Scores and O live in tensor memory (fp32).  The MMA cost is nearly
+// flat in N up to 64, so 32 heads per CTA halve the instructions per head
+// (and the re-reads of each cache row) of wide-head decode.
 //
 // Online softmax in base 2 with a lazily moved reference m (per head, the
 // same in every thread): a tile whose scores all stay below m + 8 is turned
@@ -29,20 +31,23 @@
 // 2^8) the tile max is taken (warp max instructions and a four-warp exchange
 // through shared memory), m moves to it and O is rescaled.  Row sums stay
 // per thread (each thread owns one tile row) and are added across the 128
-// threads once per slice, in a fixed order.
+// threads of its warpgroup once per slice, in a fixed order.
 //
-// Warp roles (320 threads):
+// Warp roles, head group 16 (320 threads):
 //   warps 0-3  producer.  Dense: one thread issues the TMA boxes (rows past
 //              the cache are zero-filled by the TMA unit).  Sparse top-k
 //              gather ("The Commit That Changed Direction"): 128 threads
 //              copy the indexed rows with 16-byte cp.async straight into the
 //              swizzled layout, one commit group per third of the tile.
-//              Also the item's 16 query rows (one TMA box).
+//              Also the item's query rows (one TMA box).
 //   warps 4-7  softmax: thread t owns tile row t (tensor-memory lane t);
 //              writes P as the bf16 pair; at the end of an item reads O from
 //              tensor memory and writes the partial.
 //   warp 8     score MMA issue and tensor-memory allocation; warp 9 P . V
 //              MMA issue.
+// Head group 32 (384 threads, dense only): warp 0 producer, warp 1 score
+// MMAs and allocation, warp 2 P . V MMAs, warps 4-7 and 8-11 softmax for
+// heads 0-15 and 16-31 of the group (each warpgroup covers the tile's rows).
 // Every wait is bounded (MLA_EDEVICE in the status word on a timeout); the
 // threads of a hardware barrier leave a loop together (the decision to leave
 // is the barrier's own OR-reduction); the CTA drains its copies and its MMAs
@@ -60,45 +65,56 @@
 namespace mla {
 namespace {
 
-constexpr int kTileRows = kTcTileRows;                  // 80 cache rows per tile
 constexpr int kChunks = kDRow / 64;                     // 9 column chunks of 64 bf16
-constexpr int kChunkBytes = kTileRows * 128;            // 10240
-constexpr int kTileBytes = kChunks * kChunkBytes;       // 92160
 constexpr int kGroups = kChunks / kTcBoxChunks;         // 3 TMA boxes (and barriers) per tile
-constexpr int kGroupBytes = kTcBoxChunks * kChunkBytes; // 30720
-constexpr int kQChunkBytes = kHeadGroup * 128;          // 2048
-constexpr int kQBytes = kChunks * kQChunkBytes;         // 18432
-constexpr int kPVHeads = 2 * kHeadGroup;                // [P_hi | P_lo] along N
-constexpr int kPAtomBytes = kPVHeads * 128;             // one 64-row K atom of P^T
-constexpr int kPBytes = 2 * kPAtomBytes;                // 80 rows need two K atoms
-constexpr int kProducerThreads = 128;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kProducerThreads = 128;                   // sparse gather threads (head group 16)
+constexpr int kSoftmaxThreads = 128;                    // one warpgroup per 16 heads
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kMmaWarp = 8;                             // QK issue + TMEM allocation
-constexpr int kPvWarp = 9;                              // P . V issue (its own warp: no divergent waits)
-constexpr int kThreads = 320;
 constexpr int kBarProducer = 1;                         // hardware barrier ids (0 is __syncthreads)
-constexpr int kBarSoftmax = 2;
-constexpr int kBarTmem = 3;                             // softmax + MMA warps: tensor memory allocated
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns 16*buf
-constexpr uint32_t kTmemO = 32;                         // O^T block j at 32 + 32j: hi 0..15, lo 16..31
+constexpr int kBarTmem = 2;                             // softmax + MMA warps: tensor memory allocated
+constexpr int kBarSoftmax0 = 3;                         // + softmax warpgroup
 constexpr float kRescaleLog2 = 8.0f;                    // move the reference when a max grows past 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
-static_assert(kTileRows % 16 == 0 && kTileRows <= 128, "tile rows: whole k-steps, at most M=128");
-static_assert(kChunkBytes % 1024 == 0, "chunks stay 1024-byte aligned for the 128-byte swizzle");
 static_assert(kChunks % kTcBoxChunks == 0, "a tile is a whole number of TMA boxes");
 static_assert((kTcGranule & (kTcGranule - 1)) == 0, "power-of-two granule");
 
+// Everything that follows from the head group HG (16 or 32).
+template <int HG>
+struct Cfg {
+    static constexpr int kTileRows = HG == 16 ? kTcTileRows : kTcTileRows32;
+    static constexpr int kChunkBytes = kTileRows * 128;
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kGroupBytes = kTcBoxChunks * kChunkBytes;
+    static constexpr int kQChunkBytes = HG * 128;
+    static constexpr int kQBytes = kChunks * kQChunkBytes;
+    static constexpr int kPVHeads = 2 * HG;                        // [P_hi | P_lo] along N
+    static constexpr int kPAtomBytes = kPVHeads * 128;             // one 64-row K atom of P^T
+    static constexpr int kPAtoms = (kTileRows + 63) / 64;
+    static constexpr int kPBytes = kPAtoms * kPAtomBytes;
+    static constexpr int kWGs = HG / 16;                           // softmax warpgroups
+    static constexpr int kSoftmaxWarps = 4 * kWGs;
+    static constexpr int kMmaWarp = HG == 16 ? 8 : 1;              // QK issue + TMEM allocation
+    static constexpr int kPvWarp = HG == 16 ? 9 : 2;               // P . V issue (its own warp)
+    static constexpr int kThreads = HG == 16 ? 320 : 384;
+    static constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns HG*buf
+    static constexpr uint32_t kTmemO = 2 * HG;                     // O^T block j at 2HG + 2HG*j
+    static constexpr uint32_t kTmemCols = HG == 16 ? 256 : 512;
+    static_assert(kTileRows % 16 == 0 && kTileRows <= 128, "tile rows: whole k-steps, at most M=128");
+    static_assert(kChunkBytes % 1024 == 0, "chunks stay 1024-byte aligned for the 128-byte swizzle");
+    static_assert(kTmemO + 8 * HG <= kTmemCols, "tensor memory holds S and O");
+};
+
+template <int HG>
 struct __align__(1024) SharedStorage {
-    uint8_t kv[2][kTileBytes];            // double-buffered tile (chunk c of buffer b at kv[b] + c*kChunkBytes)
-    uint8_t q[kQBytes];                   // Q^T: also absorbs the M=128 over-read of the last chunk
-    uint8_t p[2][kPBytes];                // [P_hi | P_lo]^T, K-major, per tile buffer
-    alignas(16) float red_max[2][4][16];
-    alignas(16) float red_sum[4][16];
-    int valid[2][kTileRows];
-    long long rowid[2][kTileRows];        // sparse: the tile's absolute cache rows (-1 = masked)
+    using C = Cfg<HG>;
+    uint8_t kv[2][C::kTileBytes];         // double-buffered tile (chunk c of buffer b at kv[b] + c*kChunkBytes)
+    uint8_t q[C::kQBytes];                // Q^T: also absorbs the M=128 over-read of the last chunk
+    uint8_t p[2][C::kPBytes];             // [P_hi | P_lo]^T, K-major, per tile buffer
+    alignas(16) float red_max[C::kWGs][2][4][16];
+    alignas(16) float red_sum[C::kWGs][4][16];
+    int valid[2][C::kTileRows];
+    long long rowid[2][C::kTileRows];     // sparse: the tile's absolute cache rows (-1 = masked)
     uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
     uint64_t q_full, q_empty, o_free, mma_done[2];
     uint32_t tmem_base;
@@ -111,6 +127,7 @@ struct Item {
     long long base;                       // first cache row of the request
 };
 
+template <int HG>
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     Item it;
     const uint32_t ui = static_cast<uint32_t>(item);
@@ -129,13 +146,15 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     if (e0 > e1) e0 = e1;
     it.e0 = static_cast<int>(e0);
     it.e1 = static_cast<int>(e1);
-    it.n_tiles = static_cast<int>((e1 - e0 + kTileRows - 1) / kTileRows);
+    it.n_tiles = static_cast<int>((e1 - e0 + Cfg<HG>::kTileRows - 1) / Cfg<HG>::kTileRows);
     return it;
 }
 
+template <int HG>
 __device__ __forceinline__ int rows_in_tile(const Item& it, int k) {
-    const int left = it.e1 - (it.e0 + k * kTileRows);
-    return left < kTileRows ? left : kTileRows;
+    constexpr int TR = Cfg<HG>::kTileRows;
+    const int left = it.e1 - (it.e0 + k * TR);
+    return left < TR ? left : TR;
 }
 
 __device__ __forceinline__ int item_key(const PartialParams& p, const Item& it) { return it.b * p.n_groups + it.hg; }
@@ -147,8 +166,8 @@ __device__ __forceinline__ int first_key(const PartialParams& p) {
     return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
 }
 
-__device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* status) {
-    sh.abort_flag = 1;
+__device__ __forceinline__ void raise_device_error(int* abort_flag, int* status) {
+    *abort_flag = 1;
     if (status) atomicCAS(status, 0, static_cast<int>(MLA_EDEVICE));
 }
 
@@ -160,9 +179,10 @@ struct Cursor {
     Item it;
 };
 
+template <int HG>
 __device__ __forceinline__ void cursor_next_item(const PartialParams& p, Cursor& c) {
     for (int i = c.item + static_cast<int>(gridDim.x); i < p.n_items; i += gridDim.x) {
-        const Item it = decode_item(p, i);
+        const Item it = decode_item<HG>(p, i);
         if (it.n_tiles > 0) {
             c.item = i;
             c.it = it;
@@ -173,28 +193,32 @@ __device__ __forceinline__ void cursor_next_item(const PartialParams& p, Cursor&
     }
     c.valid = false;
 }
+template <int HG>
 __device__ __forceinline__ void cursor_init(const PartialParams& p, Cursor& c) {
     c.item = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
     c.g = 0;
     c.k = 0;
-    cursor_next_item(p, c);
+    cursor_next_item<HG>(p, c);
 }
+template <int HG>
 __device__ __forceinline__ void cursor_step(const PartialParams& p, Cursor& c) {
     ++c.g;
-    if (++c.k == c.it.n_tiles) cursor_next_item(p, c);
+    if (++c.k == c.it.n_tiles) cursor_next_item<HG>(p, c);
 }
+template <int HG>
 __device__ __forceinline__ int cursor_row(const Cursor& c) {
-    return static_cast<int>(c.it.base) + c.it.e0 + c.k * kTileRows;
+    return static_cast<int>(c.it.base) + c.it.e0 + c.k * Cfg<HG>::kTileRows;
 }
 
 // Sparse: the request-local id of row t of a tile (or -1 past its rows),
-// with what it is checked against; fetched a tile or two before it is used
-// so the index load is off the gather's critical path.
+// with what it is checked against; fetched a tile ahead of its use so the
+// index load is off the gather's critical path.
 struct IdSlot {
     int id, seg, rows;
     long long base;
     bool valid;
 };
+template <int HG>
 __device__ __forceinline__ IdSlot fetch_id(const PartialParams& p, const Cursor& c, int seg, int t) {
     IdSlot s;
     s.valid = c.valid;
@@ -203,9 +227,10 @@ __device__ __forceinline__ IdSlot fetch_id(const PartialParams& p, const Cursor&
     s.rows = 0;
     s.base = 0;
     if (c.valid) {
-        s.rows = rows_in_tile(c.it, c.k);
+        s.rows = rows_in_tile<HG>(c.it, c.k);
         s.base = c.it.base;
-        if (t < s.rows) s.id = p.indices[static_cast<long long>(c.it.b) * p.topk + c.it.e0 + c.k * kTileRows + t];
+        if (t < s.rows)
+            s.id = p.indices[static_cast<long long>(c.it.b) * p.topk + c.it.e0 + c.k * Cfg<HG>::kTileRows + t];
     }
     return s;
 }
@@ -215,12 +240,13 @@ __device__ __forceinline__ long long id_row(const PartialParams& p, const IdSlot
     return (s.id >= 0 && s.id < s.seg && row >= 0 && row < p.kv_rows) ? row : -1;
 }
 
-__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int key,
+template <int HG>
+__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage<HG>& sh, int key,
                                        uint64_t policy) {
     const int b = key / p.n_groups;
     const int hg = key - b * p.n_groups;
-    mbar_arrive_expect_tx(&sh.q_full, kQBytes);
-    tma_load_3d(sh.q, &maps.q, 0, b * p.heads + hg * kHeadGroup, 0, &sh.q_full, policy);
+    mbar_arrive_expect_tx(&sh.q_full, Cfg<HG>::kQBytes);
+    tma_load_3d(sh.q, &maps.q, 0, b * p.heads + hg * HG, 0, &sh.q_full, policy);
 }
 
 // ============================== producer ==================================
@@ -229,30 +255,33 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 // path); the producer and the score-MMA thread follow the same sequence of
 // keys (a new load whenever the next busy item's key differs), and the MMA
 // thread releases a tile through q_empty before the next one is loaded over it.
-__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int t) {
+template <int HG>
+__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage<HG>& sh, int t) {
+    using C = Cfg<HG>;
+    constexpr int TR = C::kTileRows;
     if (!p.sparse && t != 0) return;
     const uint64_t pol_q = l2_policy_evict_normal();
     int q_key = first_key(p);
     const uint64_t pol_kv = l2_policy_evict_first();
     int q_loads = 1;
     Cursor cur;
-    cursor_init(p, cur);
-    // L2 prefetch runs two tiles ahead of the shared-memory loads: shared memory
-    // holds two tiles, L2 the next two in flight
+    cursor_init<HG>(p, cur);
+    // L2 prefetch runs two tiles ahead of the shared-memory loads (dense); the
+    // sparse gather prefetches the next tile's rows
     Cursor nx = cur;
-    if (nx.valid) cursor_step(p, nx);
+    if (nx.valid) cursor_step<HG>(p, nx);
     Cursor pf = nx;
-    if (pf.valid) cursor_step(p, pf);
+    if (pf.valid) cursor_step<HG>(p, pf);
     // sparse: ids of this tile and the next, the segment length of the item the
     // prefetch cursor is in
     IdSlot id_cur{}, id_nx{};
     int pf_seg = 0;
-    if (p.sparse && t < kTileRows) {
+    if (p.sparse && t < TR) {
         const int seg0 = cur.valid ? p.cache_len[cur.it.b] : 0;
         const int seg1 = nx.valid ? (nx.it.b == cur.it.b ? seg0 : p.cache_len[nx.it.b]) : 0;
         pf_seg = pf.valid ? (pf.it.b == nx.it.b ? seg1 : p.cache_len[pf.it.b]) : 0;
-        id_cur = fetch_id(p, cur, seg0, t);
-        id_nx = fetch_id(p, nx, seg1, t);
+        id_cur = fetch_id<HG>(p, cur, seg0, t);
+        id_nx = fetch_id<HG>(p, nx, seg1, t);
     }
     // `stop` is uniform over the producer threads (sparse: agreed at a barrier)
     bool stop = false;
@@ -265,9 +294,9 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             if (key != q_key) {
                 if (t == 0) {
                     if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag))
-                        raise_device_error(sh, p.status);
+                        raise_device_error(&sh.abort_flag, p.status);
                     else
-                        load_q(maps, p, sh, key, pol_q);
+                        load_q<HG>(maps, p, sh, key, pol_q);
                 }
                 q_key = key;
                 ++q_loads;
@@ -275,30 +304,30 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
         }
         const int buf = g & 1;
         if (t == 0 && g >= 2 && !mbar_wait_bounded(&sh.empty[buf], ((g >> 1) - 1) & 1, &sh.abort_flag))
-            raise_device_error(sh, p.status);
-        const int r0 = it.e0 + k * kTileRows;
-        const int rows = rows_in_tile(it, k);
+            raise_device_error(&sh.abort_flag, p.status);
+        const int r0 = it.e0 + k * TR;
         if (!p.sparse) {
             stop = sh.abort_flag != 0;
             if (stop) break;
             const int y = static_cast<int>(it.base) + r0;
 #pragma unroll
             for (int grp = 0; grp < kGroups; ++grp) {
-                mbar_arrive_expect_tx(&sh.full[buf][grp], kGroupBytes);
-                tma_load_3d(sh.kv[buf] + grp * kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
+                mbar_arrive_expect_tx(&sh.full[buf][grp], C::kGroupBytes);
+                tma_load_3d(sh.kv[buf] + grp * C::kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
                             pol_kv);
             }
             if (pf.valid) {
-                const int yp = cursor_row(pf);
+                const int yp = cursor_row<HG>(pf);
 #pragma unroll
                 for (int grp = 0; grp < kGroups; ++grp) tma_prefetch_3d(&maps.kv, 0, yp, grp * kTcBoxChunks);
             }
-        } else {
+        } else if constexpr (HG == 16) {
+            const int rows = rows_in_tile<HG>(it, k);
             // the buffer is free, or some thread saw the CTA abort
             stop = named_barrier_or(kBarProducer, kProducerThreads, sh.abort_flag != 0);
             if (stop) break;
             // the tile's row ids (fetched a tile ago), resolved once into shared memory
-            if (t < kTileRows) {
+            if (t < TR) {
                 const long long row = id_row(p, id_cur);
                 sh.rowid[buf][t] = row;
                 sh.valid[buf][t] = row >= 0 ? 1 : 0;
@@ -318,7 +347,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                     const int r = piece / kUnits;
                     const int u = grp * kUnits + (piece - r * kUnits);
                     const int c = u >> 3;
-                    const uint32_t dst = dst0 + c * kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
+                    const uint32_t dst = dst0 + c * C::kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
                     const long long row = sh.rowid[buf][r];
                     if (row >= 0)
                         cp_async_16(dst, kvb + row * stride_bytes + u * 16);
@@ -327,13 +356,13 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 }
                 cp_async_commit();
             }
-            if (t < kTileRows) {
+            if (t < TR) {
                 // the next tile's rows into L2 while this tile's copies land, and
                 // the ids of the tile after it
                 const long long nrow = id_nx.valid ? id_row(p, id_nx) : -1;
                 if (nrow >= 0) bulk_prefetch_l2(kvb + nrow * stride_bytes, kRowBytes);
                 id_cur = id_nx;
-                id_nx = fetch_id(p, pf, pf_seg, t);
+                id_nx = fetch_id<HG>(p, pf, pf_seg, t);
             }
             cp_async_wait_group<2>();
             fence_proxy_async_smem();
@@ -347,11 +376,11 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
         }
         if (pf.valid) {
             const int b_before = pf.it.b;
-            cursor_step(p, pf);
-            if (p.sparse && t < kTileRows && pf.valid && pf.it.b != b_before) pf_seg = p.cache_len[pf.it.b];
+            cursor_step<HG>(p, pf);
+            if (p.sparse && t < TR && pf.valid && pf.it.b != b_before) pf_seg = p.cache_len[pf.it.b];
         }
-        if (nx.valid) cursor_step(p, nx);
-        cursor_step(p, cur);
+        if (nx.valid) cursor_step<HG>(p, nx);
+        cursor_step<HG>(p, cur);
     }
     // Never retire the CTA with copies into its shared memory in flight.
     if (t == 0) {
@@ -360,9 +389,10 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
         for (int b = 0; b < 2 && b < g; ++b) {
             const int last = g - 1 - ((g - 1 - b) & 1);    // last tile number that used buffer b
             for (int grp = 0; grp < kGroups; ++grp)
-                if (!mbar_wait_bounded(&sh.full[b][grp], (last >> 1) & 1, &never)) raise_device_error(sh, p.status);
+                if (!mbar_wait_bounded(&sh.full[b][grp], (last >> 1) & 1, &never))
+                    raise_device_error(&sh.abort_flag, p.status);
         }
-        if (!mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never)) raise_device_error(sh, p.status);
+        if (!mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never)) raise_device_error(&sh.abort_flag, p.status);
     }
 }
 
@@ -373,13 +403,15 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
 // waits for each third of its tile and for the softmax of tile g-2 (the
 // owner of its score buffer); P . V of tile g waits for the softmax of tile
 // g, and the first one of an item for the previous item's epilogue.
-__device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
-    const uint32_t idesc_qk = make_idesc_bf16(128, kHeadGroup, 0, 0);
+template <int HG>
+__device__ void mma_issue_qk(const PartialParams& p, SharedStorage<HG>& sh, uint32_t tmem) {
+    using C = Cfg<HG>;
+    const uint32_t idesc_qk = make_idesc_bf16(128, HG, 0, 0);
     // K-major 128-byte-swizzled operands: 8-row groups 1024 bytes apart
     const uint64_t kv_desc0 = make_sdesc(smem_u32(sh.kv[0]), 16, 1024, kLayoutSw128);
     const uint64_t q_desc0 = make_sdesc(smem_u32(sh.q), 16, 1024, kLayoutSw128);
     Cursor qc;
-    cursor_init(p, qc);
+    cursor_init<HG>(p, qc);
     int q_key = first_key(p);
     int q_phase = 0;
     bool q_ready = false;
@@ -410,7 +442,7 @@ __device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t
             ok = false;
             break;
         }
-        const uint64_t kb = kv_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
+        const uint64_t kb = kv_desc0 + ((static_cast<uint32_t>(buf) * C::kTileBytes) >> 4);
         // fully unrolled: every descriptor is a constant offset from kb / q_desc0,
         // so the issuing thread keeps pace with the tensor pipe
 #pragma unroll
@@ -425,29 +457,32 @@ __device__ void mma_issue_qk(const PartialParams& p, SharedStorage& sh, uint32_t
                 const int c = grp * kTcBoxChunks + cc;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t off = (c * kChunkBytes + kk * 32u) >> 4;
-                    const uint32_t qoff = (c * kQChunkBytes + kk * 32u) >> 4;
-                    umma_bf16(tmem + kTmemS + 16 * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
+                    const uint32_t off = (c * C::kChunkBytes + kk * 32u) >> 4;
+                    const uint32_t qoff = (c * C::kQChunkBytes + kk * 32u) >> 4;
+                    umma_bf16(tmem + C::kTmemS + HG * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
                 }
             }
         }
         if (!ok) break;
         umma_commit(&sh.s_full[buf]);
-        cursor_step(p, qc);
+        cursor_step<HG>(p, qc);
     }
-    if (!ok) raise_device_error(sh, p.status);
+    if (!ok) raise_device_error(&sh.abort_flag, p.status);
     umma_commit(&sh.mma_done[0]);
     volatile int never = 0;
-    if (!mbar_wait_bounded(&sh.mma_done[0], 0, &never)) raise_device_error(sh, p.status);
+    if (!mbar_wait_bounded(&sh.mma_done[0], 0, &never)) raise_device_error(&sh.abort_flag, p.status);
 }
 
-__device__ void mma_issue_pv(const PartialParams& p, SharedStorage& sh, uint32_t tmem) {
-    const uint32_t idesc_pv = make_idesc_bf16(128, kPVHeads, 1, 0);
+template <int HG>
+__device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint32_t tmem) {
+    using C = Cfg<HG>;
+    constexpr int TR = C::kTileRows;
+    const uint32_t idesc_pv = make_idesc_bf16(128, C::kPVHeads, 1, 0);
     const uint64_t p_desc0 = make_sdesc(smem_u32(sh.p[0]), 16, 1024, kLayoutSw128);
     // V^T is MN-major: 64-feature atoms one chunk apart, 8-row groups 1024 apart
-    const uint64_t v_desc0 = make_sdesc(smem_u32(sh.kv[0]), kChunkBytes, 1024, kLayoutSw128);
+    const uint64_t v_desc0 = make_sdesc(smem_u32(sh.kv[0]), C::kChunkBytes, 1024, kLayoutSw128);
     Cursor pc;
-    cursor_init(p, pc);
+    cursor_init<HG>(p, pc);
     int items_done = 0;
     bool ok = true;
     while (pc.valid && ok) {
@@ -459,30 +494,31 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage& sh, uint32_t
             break;
         }
         tc_fence_after_sync();
-        const int ksteps = (rows_in_tile(pc.it, pc.k) + 15) >> 4;
-        const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(buf) * kTileBytes) >> 4);
-        const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * kPBytes) >> 4);
+        const int ksteps = (rows_in_tile<HG>(pc.it, pc.k) + 15) >> 4;
+        const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(buf) * C::kTileBytes) >> 4);
+        const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * C::kPBytes) >> 4);
         const uint32_t acc0 = first ? 0u : 1u;
-        if (ksteps == kTileRows / 16) {
+        if (ksteps == TR / 16) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                    const uint64_t a = vb + ((2u * j * kChunkBytes + kk * 2048u) >> 4);
-                    const uint64_t bd = pb + ((static_cast<uint32_t>(kk >> 2) * kPAtomBytes + (kk & 3) * 32u) >> 4);
-                    umma_bf16(tmem + kTmemO + 32 * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                for (int kk = 0; kk < TR / 16; ++kk) {
+                    const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
+                    const uint64_t bd =
+                        pb + ((static_cast<uint32_t>(kk >> 2) * C::kPAtomBytes + (kk & 3) * 32u) >> 4);
+                    umma_bf16(tmem + C::kTmemO + 2 * HG * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
                 }
             }
         } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                for (int kk = 0; kk < TR / 16; ++kk) {
                     if (kk < ksteps) {
-                        const uint64_t a = vb + ((2u * j * kChunkBytes + kk * 2048u) >> 4);
+                        const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
                         const uint64_t bd =
-                            pb + ((static_cast<uint32_t>(kk >> 2) * kPAtomBytes + (kk & 3) * 32u) >> 4);
-                        umma_bf16(tmem + kTmemO + 32 * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                            pb + ((static_cast<uint32_t>(kk >> 2) * C::kPAtomBytes + (kk & 3) * 32u) >> 4);
+                        umma_bf16(tmem + C::kTmemO + 2 * HG * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
                     }
                 }
             }
@@ -490,12 +526,12 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage& sh, uint32_t
         umma_commit(&sh.empty[buf]);
         umma_commit(&sh.o_done[buf]);
         if (pc.k == pc.it.n_tiles - 1) ++items_done;
-        cursor_step(p, pc);
+        cursor_step<HG>(p, pc);
     }
-    if (!ok) raise_device_error(sh, p.status);
+    if (!ok) raise_device_error(&sh.abort_flag, p.status);
     umma_commit(&sh.mma_done[1]);
     volatile int never = 0;
-    if (!mbar_wait_bounded(&sh.mma_done[1], 0, &never)) raise_device_error(sh, p.status);
+    if (!mbar_wait_bounded(&sh.mma_done[1], 0, &never)) raise_device_error(&sh.abort_flag, p.status);
 }
 
 // ============================== softmax warps ==============================
@@ -531,25 +567,31 @@ __device__ __forceinline__ void warp_sum16(float (&v)[16], int lane) {
     v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-// The four softmax warps meet at hardware barrier kBarSoftmax; a bounded wait
-// that ran out in any of them turns the barrier's OR true, and then all 128
-// threads leave together (a thread that left alone would strand the others).
-__device__ __forceinline__ bool softmax_barrier_or(bool pred) {
-    return named_barrier_or(kBarSoftmax, kSoftmaxThreads, pred);
+// The four warps of a softmax warpgroup meet at their own hardware barrier; a
+// bounded wait that ran out in any of them turns the barrier's OR true, and
+// then all 128 threads leave together (a thread that left alone would strand
+// the others).
+__device__ __forceinline__ bool softmax_barrier_or(int wg, bool pred) {
+    return named_barrier_or(kBarSoftmax0 + wg, kSoftmaxThreads, pred);
 }
 
-__device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_t tmem, int q, int lane) {
+// Warpgroup wg handles heads 16 wg .. 16 wg + 15 of the group; warp q of it
+// owns tile rows 32 q .. 32 q + 31 (tensor-memory lanes of warp q mod 4).
+template <int HG>
+__device__ void softmax_warps(const PartialParams& p, SharedStorage<HG>& sh, uint32_t tmem, int wg, int q, int lane) {
+    using C = Cfg<HG>;
+    constexpr int TR = C::kTileRows;
     const int t = q * 32 + lane;                     // tile row / TMEM lane of this thread
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const bool has_rows = q * 32 < kTileRows;        // warp-uniform
+    const bool has_rows = q * 32 < TR;               // warp-uniform
+    const int h_off = 16 * wg;                       // this warpgroup's heads within the group
     int g = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, item);
+        const Item it = decode_item<HG>(p, item);
+        const long long row0 = (static_cast<long long>(it.b) * p.heads + it.hg * HG + h_off) * p.splits + it.s;
         if (it.n_tiles == 0) {
-            write_empty_partial(p.o_part, p.lse_part,
-                                (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s,
-                                p.splits, t, kSoftmaxThreads);
+            write_empty_partial(p.o_part, p.lse_part, row0, p.splits, t, kSoftmaxThreads);
             continue;
         }
         float m_ref[16], l_part[16];
@@ -561,7 +603,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         const int first_g = g;
         for (int k = 0; k < it.n_tiles; ++k, ++g) {
             const int buf = g & 1;
-            const int rows = rows_in_tile(it, k);
+            const int rows = rows_in_tile<HG>(it, k);
             // scores of tile g; sparse: the producer's row flags; P buffer free (P . V of g-2 done)
             bool w = mbar_wait_bounded(&sh.s_full[buf], (g >> 1) & 1, &sh.abort_flag);
             if (p.sparse) w = w && mbar_wait_bounded(&sh.full[buf][0], (g >> 1) & 1, &sh.abort_flag);
@@ -570,7 +612,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             tc_fence_after_sync();
             float s[16];
             if (w && has_rows) {
-                tmem_ld16(tmem + lane_addr + kTmemS + 16 * buf, s);
+                tmem_ld16(tmem + lane_addr + C::kTmemS + HG * buf + h_off, s);
             } else {
 #pragma unroll
                 for (int h = 0; h < 16; ++h) s[h] = 0.f;
@@ -579,7 +621,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             if (p.sparse) {
                 row_ok = t < rows && sh.valid[buf][t] != 0;
             } else {
-                const long long row = it.base + it.e0 + k * kTileRows + t;
+                const long long row = it.base + it.e0 + k * TR + t;
                 row_ok = t < rows && row >= 0 && row < p.kv_rows;
             }
             bool need = !w;
@@ -591,7 +633,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             float alpha[16];
 #pragma unroll
             for (int h = 0; h < 16; ++h) alpha[h] = 1.f;
-            if (softmax_barrier_or(need)) {
+            if (softmax_barrier_or(wg, need)) {
                 // ---- tile max per head: warp max, then the four warps through shared memory
                 float mine = -INFINITY;
 #pragma unroll
@@ -599,13 +641,13 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     const float r = warp_max_f32(s[h]);
                     if (lane == h) mine = r;
                 }
-                if (lane < 16) sh.red_max[buf][q][lane] = mine;
-                if (softmax_barrier_or(!w)) {
+                if (lane < 16) sh.red_max[wg][buf][q][lane] = mine;
+                if (softmax_barrier_or(wg, !w)) {
                     ok = false;
                     break;
                 }
                 bool rescale = false;
-                const float4* rm = reinterpret_cast<const float4*>(&sh.red_max[buf][0][0]);
+                const float4* rm = reinterpret_cast<const float4*>(&sh.red_max[wg][buf][0][0]);
 #pragma unroll
                 for (int h4 = 0; h4 < 4; ++h4) {
                     const float4 a = rm[h4], b = rm[4 + h4], c = rm[8 + h4], d = rm[12 + h4];
@@ -631,24 +673,24 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     const int gp = g - 1;
                     bool w2 = mbar_wait_bounded(&sh.o_done[gp & 1], (gp >> 1) & 1, &sh.abort_flag);
                     w2 = __all_sync(0xffffffffu, w2);
-                    if (softmax_barrier_or(!w2)) {
+                    if (softmax_barrier_or(wg, !w2)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
-                        float o[32];
-                        const uint32_t a = tmem + lane_addr + kTmemO + 32 * j;
-                        tmem_ld32(a, o);
+                        const uint32_t a = tmem + lane_addr + C::kTmemO + 2 * HG * j + h_off;
                         float hi[16], lo[16];
+                        tmem_ld16(a, hi);
+                        tmem_ld16(a + HG, lo);
 #pragma unroll
                         for (int h = 0; h < 16; ++h) {
-                            hi[h] = o[h] * alpha[h];
-                            lo[h] = o[16 + h] * alpha[h];
+                            hi[h] *= alpha[h];
+                            lo[h] *= alpha[h];
                         }
                         tmem_st16(a, hi);
-                        tmem_st16(a + 16, lo);
+                        tmem_st16(a + HG, lo);
                     }
                 }
             }
@@ -657,9 +699,10 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
             float pr[16];
 #pragma unroll
             for (int h = 0; h < 16; ++h) pr[h] = (row_ok && m_ref[h] > -INFINITY) ? ex2_approx(s[h] - m_ref[h]) : 0.f;
-            if (t < kTileRows) {
-                // row t of head h: line h (hi) / 16 + h (lo) of the K atom t / 64, byte 2 * (t % 64)
-                const uint32_t pbase = smem_u32(sh.p[buf]) + (t >> 6) * kPAtomBytes + 2u * (t & 7);
+            if (t < TR) {
+                // row t of head h: line h_off + h (hi) / HG + h_off + h (lo) of the K atom
+                // t / 64, byte 2 * (t % 64); lines are 128 bytes, 8-line groups 1024 apart
+                const uint32_t pbase = smem_u32(sh.p[buf]) + (t >> 6) * C::kPAtomBytes + h_off * 128 + 2u * (t & 7);
                 const uint32_t unit = static_cast<uint32_t>((t & 63) >> 3);
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
@@ -667,18 +710,18 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                     const __nv_bfloat16 lo = __float2bfloat16_rn(pr[h] - __bfloat162float(hi));
                     const uint32_t a = pbase + (h >> 3) * 1024 + (h & 7) * 128 + ((unit ^ (h & 7)) << 4);
                     st_shared_u16(a, __bfloat16_as_ushort(hi));
-                    st_shared_u16(a + 2048, __bfloat16_as_ushort(lo));
+                    st_shared_u16(a + HG * 128, __bfloat16_as_ushort(lo));
                 }
             }
 #pragma unroll
             for (int h = 0; h < 16; ++h) l_part[h] = l_part[h] * alpha[h] + pr[h];
             // ---- dense: masked rows the P . V k-steps read must hold zeros ---------
-            if (!p.sparse && t < kTileRows && !row_ok && t < ((rows + 15) & ~15)) {
+            if (!p.sparse && wg == 0 && t < TR && !row_ok && t < ((rows + 15) & ~15)) {
                 const uint32_t row_base = smem_u32(sh.kv[buf]) + t * 128;
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c)
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) st_shared_v4_zero(row_base + c * kChunkBytes + u * 16);
+                    for (int u = 0; u < 8; ++u) st_shared_v4_zero(row_base + c * C::kChunkBytes + u * 16);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -694,12 +737,12 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
 #pragma unroll
             for (int h = 0; h < 16; ++h) red[h] = l_part[h];
             warp_sum16(red, lane);
-            if ((lane & 1) == 0) sh.red_sum[q][lane >> 1] = red[0];
+            if ((lane & 1) == 0) sh.red_sum[wg][q][lane >> 1] = red[0];
         }
-        named_barrier_sync(kBarSoftmax, kSoftmaxThreads);
+        named_barrier_sync(kBarSoftmax0 + wg, kSoftmaxThreads);
         float l_run[16];
         {
-            const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[0][0]);
+            const float4* rs = reinterpret_cast<const float4*>(&sh.red_sum[wg][0][0]);
 #pragma unroll
             for (int h4 = 0; h4 < 4; ++h4) {
                 const float4 a = rs[h4], b = rs[4 + h4], c = rs[8 + h4], d = rs[12 + h4];
@@ -709,7 +752,6 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
                 l_run[4 * h4 + 3] = ((a.w + b.w) + c.w) + d.w;
             }
         }
-        const long long row0 = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s;
         if (t < 16) {
             float lv = 0.f, mv = 0.f;
 #pragma unroll
@@ -726,7 +768,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         const int gl = g - 1;
         bool w = mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag);
         w = __all_sync(0xffffffffu, w);
-        if (softmax_barrier_or(!w)) {
+        if (softmax_barrier_or(wg, !w)) {
             ok = false;
             break;
         }
@@ -734,23 +776,37 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage& sh, uint32_
         float* o_row = p.o_part + row0 * kDLatent + t;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
-            float o[32];                                  // hi in 0..15, lo in 16..31
-            tmem_ld32(tmem + lane_addr + kTmemO + 32 * j, o);
+            float hi[16], lo[16];                         // features 128 j + t of the 16 heads
+            const uint32_t a = tmem + lane_addr + C::kTmemO + 2 * HG * j + h_off;
+            if constexpr (HG == 16) {
+                float o[32];
+                tmem_ld32(a, o);
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    hi[h] = o[h];
+                    lo[h] = o[16 + h];
+                }
+            } else {
+                tmem_ld16(a, hi);
+                tmem_ld16(a + HG, lo);
+            }
 #pragma unroll
             for (int h = 0; h < 16; ++h)
-                o_row[static_cast<long long>(h) * p.splits * kDLatent + 128 * j] = (o[h] + o[16 + h]) * inv[h];
+                o_row[static_cast<long long>(h) * p.splits * kDLatent + 128 * j] = (hi[h] + lo[h]) * inv[h];
         }
         tc_fence_before_sync();
         mbar_arrive(&sh.o_free);
     }
-    if (!ok && lane == 0) raise_device_error(sh, p.status);
+    if (!ok && lane == 0) raise_device_error(&sh.abort_flag, p.status);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __grid_constant__ TcMaps maps,
-                                                                      const PartialParams p) {
+template <int HG>
+__global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(const __grid_constant__ TcMaps maps,
+                                                                               const PartialParams p) {
+    using C = Cfg<HG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SharedStorage& sh =
-        *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SharedStorage<HG>& sh = *reinterpret_cast<SharedStorage<HG>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -760,12 +816,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
             for (int grp = 0; grp < kGroups; ++grp) mbar_init(&sh.full[i][grp], p.sparse ? kProducerThreads : 1);
             mbar_init(&sh.empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], kSoftmaxThreads);
+            mbar_init(&sh.p_full[i], kSoftmaxThreads * C::kWGs);
             mbar_init(&sh.o_done[i], 1);
         }
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, 1);
-        mbar_init(&sh.o_free, kSoftmaxThreads);
+        mbar_init(&sh.o_free, kSoftmaxThreads * C::kWGs);
         mbar_init(&sh.mma_done[0], 1);
         mbar_init(&sh.mma_done[1], 1);
         sh.abort_flag = 0;
@@ -776,58 +832,68 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_tc_kernel(const __gri
     // before this one on the stream: wait for it before any global read.
     grid_dependency_wait();
     allow_dependent_launch();
-    if (warp == kPvWarp && lane == 1) load_q(maps, p, sh, first_key(p), l2_policy_evict_normal());
+    if (warp == C::kPvWarp && lane == 1) load_q<HG>(maps, p, sh, first_key(p), l2_policy_evict_normal());
+    const bool softmax = warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + C::kSoftmaxWarps;
+    const bool mma = warp == C::kMmaWarp || warp == C::kPvWarp;
     uint32_t tmem = 0;
-    if (warp >= kSoftmaxWarp0) {
+    if (softmax || mma) {
         // the tensor-memory users wait for the allocation; the producer does not
-        if (warp == kMmaWarp) {
-            tmem_alloc(&sh.tmem_base, kTmemCols);
+        if (warp == C::kMmaWarp) {
+            tmem_alloc(&sh.tmem_base, C::kTmemCols);
             tmem_relinquish();
         }
         tc_fence_before_sync();
-        named_barrier_sync(kBarTmem, kThreads - kProducerThreads);
+        named_barrier_sync(kBarTmem, 32 * (C::kSoftmaxWarps + 2));
         tc_fence_after_sync();
         tmem = sh.tmem_base;
     }
-    if (warp < 4) {
-        producer(maps, p, sh, threadIdx.x);
-    } else if (warp < kMmaWarp) {
-        softmax_warps(p, sh, tmem, warp - kSoftmaxWarp0, lane);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issue_qk(p, sh, tmem);
-    } else if (warp == kPvWarp && lane == 0) {
-        mma_issue_pv(p, sh, tmem);
+    if (HG == 16 ? warp < 4 : warp == 0) {
+        producer<HG>(maps, p, sh, threadIdx.x);
+    } else if (softmax) {
+        const int sw = warp - kSoftmaxWarp0;
+        softmax_warps<HG>(p, sh, tmem, sw >> 2, sw & 3, lane);
+    } else if (warp == C::kMmaWarp) {
+        if (lane == 0) mma_issue_qk<HG>(p, sh, tmem);
+    } else if (warp == C::kPvWarp && lane == 0) {
+        mma_issue_pv<HG>(p, sh, tmem);
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
 }  // namespace
 
-size_t partial_tc_smem_bytes() { return sizeof(SharedStorage) + 1024; }
-int partial_tc_block_threads() { return kThreads; }
+size_t partial_tc_smem_bytes(int head_group) {
+    return (head_group == 32 ? sizeof(SharedStorage<32>) : sizeof(SharedStorage<16>)) + 1024;
+}
+int partial_tc_block_threads(int head_group) { return head_group == 32 ? Cfg<32>::kThreads : Cfg<16>::kThreads; }
 
 cudaError_t partial_tc_prepare(int /*device*/) {
-    return cudaFuncSetAttribute(mla_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(partial_tc_smem_bytes()));
+    const cudaError_t e = cudaFuncSetAttribute(mla_partial_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(partial_tc_smem_bytes(16)));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mla_partial_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(partial_tc_smem_bytes(32)));
 }
 
-cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream) {
+cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int head_group, dim3 grid, bool pdl,
+                              cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = partial_tc_smem_bytes();
+    cfg.blockDim = dim3(partial_tc_block_threads(head_group), 1, 1);
+    cfg.dynamicSmemBytes = partial_tc_smem_bytes(head_group);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel, maps, p);
+    return head_group == 32 ? cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<32>, maps, p)
+                            : cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<16>, maps, p);
 }
 
 }  // namespace mla

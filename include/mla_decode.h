@@ -85,10 +85,13 @@ typedef struct {
     float scale;          /* softmax scale, finite and > 0 (1/sqrt(576) for these shapes) */
     int num_sms;          /* SMs to plan for; 0 = query the current device */
     int splits_override;  /* 0 = derive; 1..MLA_MAX_SPLITS = force this split count */
-    int variant;          /* 1 = warp-MMA (mma.sync) kernel, 32-row stages; 2 = tcgen05/TMEM
-                             kernel, 80-row TMA tiles (both: 16 heads per CTA); 0 = auto:
-                             sparse -> 1; dense with >= 4 head groups -> 2; other dense -> 2
-                             when its slices hold >= 320 rows, else 1 (measured crossover) */
+    int variant;          /* 1 = warp-MMA (mma.sync) kernel, 32-row stages, 16 heads per CTA;
+                             2 = tcgen05/TMEM kernel, 80-row TMA tiles, 16 heads per CTA;
+                             3 = tcgen05/TMEM kernel, 64-row tiles, 32 heads per CTA (dense,
+                                 heads a multiple of 32);
+                             0 = auto (measured crossovers): sparse -> 1; dense H >= 64 -> 3;
+                                 H = 32 -> 3 when its slices hold >= 256 rows; otherwise 2
+                                 when its slices hold >= 320 rows, else 1 */
     int pdl;              /* 1 = launch with programmatic dependent launch */
 } mla_decode_shape;
 

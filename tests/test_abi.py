@@ -47,8 +47,9 @@ def _plan(**kw):
     return mla.plan(**base)
 
 
-TILE = {1: 32, 2: 80}        # rows per kernel step: warp-MMA stage, tcgen05 tile
-GRANULE = {1: 32, 2: 16}     # slices are whole multiples of this
+TILE = {1: 32, 2: 80, 3: 64}     # rows per kernel step: warp-MMA stage, tcgen05 tiles (16 / 32 heads)
+GRANULE = {1: 32, 2: 16, 3: 16}  # slices are whole multiples of this
+HEADS = {1: 16, 2: 16, 3: 32}    # heads per CTA
 
 
 def _model_split(rows, pairs, sms, variant=2, max_splits=256):
@@ -71,7 +72,7 @@ def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     (dict(max_ctx=8192), 1, 128, 64),
     (dict(sparse=True, topk=2048), 1, 64, 32),
     (dict(batch=64, sparse=True, topk=2048), 1, 2, 1024),
-    (dict(heads=128, max_ctx=32768 + 64), 2, 19, 1728),
+    (dict(heads=128, max_ctx=32768 + 64), 3, 37, 896),
     (dict(max_ctx=131072), 2, 149, 880),
     (dict(max_ctx=8192, variant=2), 2, 103, 80),
     (dict(sparse=True, topk=2048, variant=2), 2, 26, 80),
@@ -84,7 +85,7 @@ def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     B, H = kw.get("batch", 1), kw.get("heads", 16)
     assert p.splits * p.entries_per_split >= rows
     assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
-    assert p.n_head_groups == H // 16 and p.ctas_per_sm == 1
+    assert p.n_head_groups == H // HEADS[variant] and p.ctas_per_sm == 1
     assert p.grid_x == min(B * p.n_head_groups * p.splits, 152) and p.grid_y == 1 and p.grid_z == 1
     assert p.combine_grid_x == -(-B * H // (8 // _unit_warps(p.splits))) and p.combine_grid_y == 4
     assert p.combine_block == 256
@@ -93,6 +94,20 @@ def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     assert p.status_offset == 0 and p.o_part_offset % 256 == 0 and p.lse_part_offset % 256 == 0
     assert p.lse_part_offset >= p.o_part_offset + bh * p.splits * 512 * 4
     assert p.scratch_bytes >= p.lse_part_offset + bh * p.splits * 4 and p.scratch_bytes % 256 == 0
+
+
+@pytest.mark.parametrize("rows", [1, 100, 8192, 131072])
+@pytest.mark.parametrize("batch,heads", [(1, 32), (2, 64), (1, 128)])
+def test_plan_head_group_32(rows, batch, heads):
+    p = _plan(max_ctx=rows, batch=batch, heads=heads, variant=3)
+    assert p.variant == 3 and p.head_group == 32 and p.n_head_groups == heads // 32
+    assert p.splits == _model_split(rows, batch * heads // 32, 152, 3)
+    assert p.entries_per_split == -(-(-(-rows // p.splits)) // 16) * 16
+    assert p.grid_x == min(batch * (heads // 32) * p.splits, 152)
+    assert p.block == 384 and p.smem_bytes <= 227 * 1024
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.head_group = 16
+    assert _call("mla_decode_run", bad, _args(row_offset=0x60000)) == mla.EINVAL
 
 
 @pytest.mark.parametrize("variant", [1, 2])
@@ -106,16 +121,20 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
     assert ps.splits == p.splits
 
 
-def _model_auto(sparse, rows, pairs, groups, sms):
-    """The automatic kernel choice, restated: sparse -> warp-MMA; >= 4 head
-    groups -> tcgen05; else tcgen05 when its slices hold >= 320 rows."""
+def _model_auto(sparse, rows, batch, heads, sms):
+    """The automatic kernel choice, restated: sparse -> warp-MMA; H >= 64 ->
+    32 heads per CTA; H = 32 -> that too when its slices hold >= 256 rows;
+    otherwise the 16-head tcgen05 kernel when its slices hold >= 320 rows."""
+    def per(v):
+        S = _model_split(rows, batch * heads // HEADS[v], sms, v)
+        return -(-(-(-rows // S)) // GRANULE[v]) * GRANULE[v]
     if sparse:
         return 1
-    if groups >= 4:
-        return 2
-    S = _model_split(rows, pairs, sms, 2)
-    per = -(-(-(-rows // S)) // 16) * 16
-    return 2 if per >= 320 else 1
+    if heads >= 64:
+        return 3
+    if heads == 32 and per(3) >= 256:
+        return 3
+    return 2 if per(2) >= 320 else 1
 
 
 @pytest.mark.parametrize("rows", [1, 100, 256, 8192, 20000, 32768, 65536, 131072])
@@ -124,9 +143,9 @@ def _model_auto(sparse, rows, pairs, groups, sms):
 def test_plan_automatic_kernel_choice(rows, batch, heads, sparse):
     kw = dict(sparse=True, topk=rows) if sparse else dict(max_ctx=rows)
     p = _plan(batch=batch, heads=heads, **kw)
-    v = _model_auto(sparse, rows, batch * heads // 16, heads // 16, 152)
+    v = _model_auto(sparse, rows, batch, heads, 152)
     assert p.variant == v
-    assert p.splits == _model_split(rows, batch * heads // 16, 152, v)
+    assert p.splits == _model_split(rows, batch * heads // HEADS[v], 152, v)
 
 
 def _unit_warps(splits):
@@ -187,7 +206,9 @@ def test_plan_override():
     (dict(max_ctx=16, splits=-1), mla.EINVAL),
     (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
     (dict(max_ctx=16, variant=7), mla.EINVAL),
-    (dict(max_ctx=16, variant=3), mla.EINVAL),
+    (dict(max_ctx=16, variant=4), mla.EINVAL),
+    (dict(max_ctx=16, variant=3), mla.EUNSUPPORTED),                 # 32 heads per CTA: H = 16 is too few
+    (dict(heads=32, sparse=True, topk=64, variant=3), mla.EUNSUPPORTED),  # dense only
 ])
 def test_plan_rejects(kw, status):
     with pytest.raises(mla.MLADecodeError) as e:

@@ -29,7 +29,7 @@ def _setup():
 class Loop:
     """Device state of the multi-step workload and the per-step call sequence."""
 
-    def __init__(self, g: workloads.GraphInputs, H: int, pdl: bool = False, splits: int = 0):
+    def __init__(self, g: workloads.GraphInputs, H: int, pdl: bool = False, splits: int = 0, variant: int = 0):
         d = _gpu.dev()
         self.g = g
         self.H = H
@@ -42,7 +42,8 @@ class Loop:
         self.frozen = self.d_pos.clone()
         self.out = torch.zeros(g.steps, 1, H, 512, device=d)
         self.lse = torch.zeros(g.steps, 1, H, device=d)
-        self.plan = mla.plan(batch=1, heads=H, max_ctx=g.d_pos0 + g.steps, scale=g.scale, pdl=pdl, splits=splits)
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=g.d_pos0 + g.steps, scale=g.scale, pdl=pdl, splits=splits,
+                             variant=variant)
         self.scratch = mla.alloc_scratch(self.plan)
 
     def reset(self):
@@ -121,11 +122,13 @@ def test_graph_frozen_position_fails_from_step_one():
         assert err_o > 10 * _gpu.OUT_ATOL, f"frozen append went unnoticed at step {k}"
 
 
-def test_graph_h128_workload():
+@pytest.mark.parametrize("variant", [0, 3])
+def test_graph_h128_workload(variant):
     """The 64-step, H=128, 32k-context workload: replays byte identical to eager;
-    sampled steps against the oracle; every step finite with lse rising as rows are added."""
+    sampled steps against the oracle; every step finite with lse rising as rows are added.
+    Run with the planner's kernel and with the 32-heads-per-CTA tcgen05 kernel."""
     g = workloads.make("graph_h128")
-    loop = Loop(g, 128)
+    loop = Loop(g, 128, variant=variant)
     loop.reset()
     loop.steps()
     torch.cuda.synchronize()

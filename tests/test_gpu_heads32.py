@@ -1,0 +1,103 @@
+"""GPU parity of the tcgen05 kernel with 32 heads per CTA (variant 3, dense
+decode, H a multiple of 32) against the fp64 oracle; the same bar as every
+other kernel."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import decode_attention_mla_gb300 as mla
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+V32 = 3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from __graft_entry__ import build
+    build()
+    torch.cuda.set_device(0)
+    yield
+
+
+@pytest.mark.parametrize("H", [32, 64, 128])
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 100, 1000, 2049])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_dense_heads32(H, T, splits):
+    x = workloads.dense(1, H, T, seed=T + H)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=splits, variant=V32)
+    assert plan.variant == V32 and plan.head_group == 32
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"H={H} T={T} S={plan.splits}")
+    assert mla.status_word(plan, scratch) == 0
+
+
+def test_heads32_partials_match_oracle_split_emulation():
+    x = workloads.dense(1, 32, 1000, seed=53)
+    out, lse, plan, scratch = _gpu.run_dense(x, splits=5, variant=V32)
+    S = plan.splits
+    _, _, op, lp = oracle.decode_split(x.q, x.kv, scale=x.scale, splits=S, granule=16, d_pos=x.d_pos,
+                                       return_partials=True)
+    o_off, l_off = plan.o_part_offset, plan.lse_part_offset
+    o_gpu = scratch[o_off:o_off + 32 * S * 512 * 4].view(torch.float32).view(1, 32, S, 512).double().cpu().numpy()
+    l_gpu = scratch[l_off:l_off + 32 * S * 4].view(torch.float32).view(1, 32, S).double().cpu().numpy()
+    assert np.abs(o_gpu - op).max() <= _gpu.OUT_ATOL
+    fin = np.isfinite(lp)
+    assert np.array_equal(np.isfinite(l_gpu), fin)
+    assert (np.abs(l_gpu[fin] - lp[fin]) / np.maximum(np.abs(lp[fin]), 1)).max() <= _gpu.LSE_RTOL
+
+
+def test_heads32_batch_ragged_and_many_items():
+    B, H, cap = 3, 64, 1500
+    x = workloads.dense(B, H, cap, seed=54)
+    x.d_pos = torch.tensor([1499, 17, 640], dtype=torch.int32)
+    ro, rl = _gpu.oracle_dense(x)
+    for s in (0, 7, 200):
+        out, lse, plan, _ = _gpu.run_dense(x, max_ctx=cap, splits=s, variant=V32)
+        _gpu.assert_parity(out, lse, ro, rl, f"dense B=3 H=64 ragged S={plan.splits}")
+
+
+def test_heads32_bit_identical_across_runs():
+    x = workloads.dense(1, 128, 3000, seed=55)
+    out0, lse0, plan, scratch = _gpu.run_dense(x, splits=9, variant=V32)
+    for _ in range(5):
+        out, lse, _, _ = _gpu.run_dense(x, plan=plan, scratch=scratch)
+        assert torch.equal(_gpu.bits(out), _gpu.bits(out0)) and torch.equal(_gpu.bits(lse), _gpu.bits(lse0))
+
+
+def test_heads32_agrees_with_heads16():
+    x = workloads.dense(1, 64, 5000, seed=56)
+    a = _gpu.run_dense(x, variant=2)
+    b = _gpu.run_dense(x, variant=V32)
+    assert (a[0] - b[0]).abs().max().item() <= 2 * _gpu.OUT_ATOL
+    assert ((a[1] - b[1]).abs() / a[1].abs().clamp(min=1)).max().item() <= 2 * _gpu.LSE_RTOL
+
+
+def test_heads32_rescale_path():
+    """Scores that grow along the context move the reference (and rescale O in
+    tensor memory) many times within one slice, in both softmax warpgroups."""
+    T = 4000
+    x = workloads.dense(1, 32, T, seed=57)
+    ramp = torch.linspace(0.0, 12.0, T).unsqueeze(1)
+    kv = x.kv.float()
+    kv[:, :512] = kv[:, :512] + ramp * x.q[0, 0, :512].float().sign().unsqueeze(0) * 0.05
+    x.kv = kv.to(torch.bfloat16)
+    x.q = (x.q.float() * 4.0).to(torch.bfloat16)
+    ro, rl = _gpu.oracle_dense(x)
+    out, lse, plan, _ = _gpu.run_dense(x, splits=1, variant=V32)
+    _gpu.assert_parity(out, lse, ro, rl, "growing scores, 32 heads per CTA")
+
+
+def test_heads32_uniform_scores_closed_form():
+    T = 777
+    x = workloads.dense(1, 32, T, seed=58)
+    x.q = torch.zeros_like(x.q)
+    out, lse, _, _ = _gpu.run_dense(x, splits=6, variant=V32)
+    mean = x.kv[:, :512].double().mean(0).numpy()
+    assert np.abs(out.double().cpu().numpy() - mean[None, None]).max() <= _gpu.OUT_ATOL
+    assert np.abs(lse.double().cpu().numpy() - np.log(T)).max() <= _gpu.LSE_RTOL * np.log(T)

@@ -71,8 +71,9 @@ struct AppendParams {
 // swizzle: dimension 0 = 64 bf16 of a row (128 bytes), dimension 1 = rows
 // (stride: the row stride), dimension 2 = the 9 column chunks of a row
 // (stride 128 bytes).  One box lands as [chunk][row][64 bf16], the layout the
-// tensor cores read.  kv: boxes of 64 x 80 rows x 3 chunks (a third of a
-// tile); q: boxes of 64 x 16 heads x 9 chunks (the whole head group).
+// tensor cores read.  kv: boxes of 64 x tile rows x 3 chunks (a third of a
+// tile; one-chunk boxes, nine barriers per tile, measured slower); q: boxes
+// of 64 x head-group rows x 9 chunks (the whole query tile).
 constexpr int kTcBoxChunks = 3;
 // The warp-MMA kernel uses the same query map (its cache map is unused).
 struct TcMaps {

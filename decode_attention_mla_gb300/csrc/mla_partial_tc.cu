@@ -66,7 +66,9 @@ namespace mla {
 namespace {
 
 constexpr int kChunks = kDRow / 64;                     // 9 column chunks of 64 bf16
-constexpr int kGroups = kChunks / kTcBoxChunks;         // 3 TMA boxes (and barriers) per tile
+constexpr int kGroups = kChunks / kTcBoxChunks;         // TMA boxes (and barriers) per tile
+constexpr int kGatherBatches = 3;                       // sparse: cp.async commit groups per tile
+constexpr int kGroupsPerBatch = kGroups / kGatherBatches;
 constexpr int kProducerThreads = 128;                   // sparse gather threads (head group 16)
 constexpr int kSoftmaxThreads = 128;                    // one warpgroup per 16 heads
 constexpr int kSoftmaxWarp0 = 4;
@@ -77,6 +79,7 @@ constexpr float kRescaleLog2 = 8.0f;                    // move the reference wh
 constexpr float kLn2 = 0.6931471805599453f;
 
 static_assert(kChunks % kTcBoxChunks == 0, "a tile is a whole number of TMA boxes");
+static_assert(kGroups % kGatherBatches == 0, "gather batches cover whole boxes");
 static_assert((kTcGranule & (kTcGranule - 1)) == 0, "power-of-two granule");
 
 // Everything that follows from the head group HG (16 or 32).
@@ -339,13 +342,13 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             const uint32_t dst0 = smem_u32(sh.kv[buf]);
             const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
             const long long stride_bytes = p.row_stride * 2;
-            constexpr int kUnits = kTcBoxChunks * 8;                  // 16-byte units of a row in one box
+            constexpr int kUnits = kGroupsPerBatch * kTcBoxChunks * 8;  // 16-byte units of a row per batch
 #pragma unroll
-            for (int grp = 0; grp < kGroups; ++grp) {
+            for (int bt = 0; bt < kGatherBatches; ++bt) {
 #pragma unroll 4
                 for (int piece = t; piece < rows_read * kUnits; piece += kProducerThreads) {
                     const int r = piece / kUnits;
-                    const int u = grp * kUnits + (piece - r * kUnits);
+                    const int u = bt * kUnits + (piece - r * kUnits);
                     const int c = u >> 3;
                     const uint32_t dst = dst0 + c * C::kChunkBytes + r * 128 + ((((u & 7) ^ (r & 7))) << 4);
                     const long long row = sh.rowid[buf][r];
@@ -364,15 +367,19 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 id_cur = id_nx;
                 id_nx = fetch_id<HG>(p, pf, pf_seg, t);
             }
+            static_assert(kGatherBatches == 3, "three commit groups per tile");
             cp_async_wait_group<2>();
             fence_proxy_async_smem();
-            mbar_arrive(&sh.full[buf][0]);
+#pragma unroll
+            for (int i = 0; i < kGroupsPerBatch; ++i) mbar_arrive(&sh.full[buf][i]);
             cp_async_wait_group<1>();
             fence_proxy_async_smem();
-            mbar_arrive(&sh.full[buf][1]);
+#pragma unroll
+            for (int i = 0; i < kGroupsPerBatch; ++i) mbar_arrive(&sh.full[buf][kGroupsPerBatch + i]);
             cp_async_wait_group<0>();
             fence_proxy_async_smem();
-            mbar_arrive(&sh.full[buf][2]);
+#pragma unroll
+            for (int i = 0; i < kGroupsPerBatch; ++i) mbar_arrive(&sh.full[buf][2 * kGroupsPerBatch + i]);
         }
         if (pf.valid) {
             const int b_before = pf.it.b;

@@ -36,7 +36,8 @@ class Shape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("d_latent", ctypes.c_int),
                 ("d_rope", ctypes.c_int), ("sparse", ctypes.c_int), ("max_ctx", ctypes.c_int),
                 ("topk", ctypes.c_int), ("scale", ctypes.c_float), ("num_sms", ctypes.c_int),
-                ("splits_override", ctypes.c_int), ("variant", ctypes.c_int), ("pdl", ctypes.c_int)]
+                ("splits_override", ctypes.c_int), ("variant", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("stall_test", ctypes.c_int)]
 
 
 class Plan(ctypes.Structure):
@@ -137,14 +138,14 @@ def _stream(stream):
 
 
 def plan(*, batch: int, heads: int, scale: float, max_ctx: int = 0, topk: int = 0, sparse: bool = False,
-         num_sms: int = 0, splits: int = 0, variant: int = 0, pdl: bool = False) -> Plan:
+         num_sms: int = 0, splits: int = 0, variant: int = 0, pdl: bool = False, stall_test: bool = False) -> Plan:
     """``mla_decode_plan``: derive the split count, grid and scratch layout.
 
     ``num_sms=0`` queries the current CUDA device and prepares the kernels on it
     (do this before capturing a graph)."""
     s = Shape(batch=batch, heads=heads, d_latent=D_LATENT, d_rope=D_ROPE, sparse=int(bool(sparse)),
               max_ctx=max_ctx, topk=topk, scale=scale, num_sms=num_sms, splits_override=splits,
-              variant=variant, pdl=int(bool(pdl)))
+              variant=variant, pdl=int(bool(pdl)), stall_test=int(bool(stall_test)))
     p = Plan()
     _check(lib().mla_decode_plan(ctypes.byref(s), ctypes.byref(p)), "mla_decode_plan")
     return p

@@ -14,6 +14,10 @@ constexpr unsigned long long kWaitTimeoutNs = 2000ull * 1000ull * 1000ull;  // 2
 // The same bound in SM clock cycles (about 2 s at 2 GHz; longer at lower
 // clocks): waits count cycles, which are cheap to read, not the global timer.
 constexpr long long kWaitTimeoutCycles = 4000ll * 1000ll * 1000ll;
+// The limit of the stall-test wait (about 1 ms): a shape with stall_test set
+// makes one thread of the partial kernel wait this long on a barrier nothing
+// arrives at, so the timeout path (status word, abort, drain) runs for real.
+constexpr long long kStallTestCycles = 2ll * 1000ll * 1000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,7 +69,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // the CTA-wide abort flag is raised or the time limit passes.  The limit is
 // checked every 256 polls against the SM cycle counter (reading the global
 // timer on every wait would put its latency on every hand-off).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  long long limit_cycles = kWaitTimeoutCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
@@ -75,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             const long long now = clock64();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitTimeoutCycles) {
+            } else if (now - t0 > limit_cycles) {
                 return false;
             }
         }

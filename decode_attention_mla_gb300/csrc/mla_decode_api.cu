@@ -135,6 +135,7 @@ int check_shape(const mla_decode_shape* s) {
     if (s->batch < 1 || s->batch > 65535) return MLA_EINVAL;
     if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
+    if (s->stall_test != 0 && s->stall_test != 1) return MLA_EINVAL;
     if (s->variant < 0 || s->variant > 3) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
@@ -223,6 +224,7 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.o_part = reinterpret_cast<float*>(base + pl->o_part_offset);
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
+    p.stall_test = pl->shape.stall_test;
     const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
     if (pl->variant == kVariantTc || pl->variant == kVariantTc32) {
         // TMA coordinates are 32-bit: the cache must be addressable by them

@@ -41,6 +41,7 @@ struct PartialParams {
     float* o_part;              // [B][H][S][512]
     float* lse_part;            // [B][H][S]
     int* status;                // status word
+    int stall_test;             // test hook: run the timeout path (see mla_decode_shape)
 };
 
 struct CombineParams {

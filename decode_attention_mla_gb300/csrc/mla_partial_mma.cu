@@ -79,6 +79,7 @@ struct __align__(1024) SharedStorage {
     uint64_t red_bar[2];
     uint64_t q_full;
     uint64_t q_empty;
+    uint64_t stall_bar;                                   // test hook: a barrier nothing arrives at
     int abort_flag;
 };
 
@@ -148,7 +149,8 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     int q_key = first_key(p);
     load_q(maps, p, sh, q_key, lane);
     int q_loads = 1;          // query tiles staged so far
-    bool ok = true;
+    // test hook: a wait that runs out, so every role takes the abort path
+    bool ok = !(p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
         if (it.n_stages == 0) continue;
@@ -455,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         for (int i = 0; i < 2; ++i) mbar_init(&sh.red_bar[i], kComputeWarps * 32);
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, kComputeWarps);
+        mbar_init(&sh.stall_bar, 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }

@@ -120,6 +120,7 @@ struct __align__(1024) SharedStorage {
     long long rowid[2][C::kTileRows];     // sparse: the tile's absolute cache rows (-1 = masked)
     uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
     uint64_t q_full, q_empty, o_free, mma_done[2];
+    uint64_t stall_bar;                   // test hook: a barrier nothing arrives at
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -422,7 +423,8 @@ __device__ void mma_issue_qk(const PartialParams& p, SharedStorage<HG>& sh, uint
     int q_key = first_key(p);
     int q_phase = 0;
     bool q_ready = false;
-    bool ok = true;
+    // test hook: a wait that runs out, so every role takes the abort path
+    bool ok = !(p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     while (qc.valid && ok) {
         const int key = item_key(p, qc.it);
         const int buf = qc.g & 1;
@@ -831,6 +833,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(co
         mbar_init(&sh.o_free, kSoftmaxThreads * C::kWGs);
         mbar_init(&sh.mma_done[0], 1);
         mbar_init(&sh.mma_done[1], 1);
+        mbar_init(&sh.stall_bar, 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }

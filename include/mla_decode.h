@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 1
+#define MLA_DECODE_ABI_VERSION 2
 #define MLA_D_LATENT 512
 #define MLA_D_ROPE 64
 #define MLA_D_ROW 576        /* elements per cache row */
@@ -93,6 +93,11 @@ typedef struct {
                                  H = 32 -> 3 when its slices hold >= 256 rows; otherwise 2
                                  when its slices hold >= 320 rows, else 1 */
     int pdl;              /* 1 = launch with programmatic dependent launch */
+    int stall_test;       /* test hook, 0 in normal use.  1 = one thread of the partial kernel
+                             waits (about 1 ms) on a barrier nothing arrives at, so the timeout
+                             path runs for real: the CTA aborts, drains its copies and MMAs,
+                             frees its tensor memory and leaves MLA_EDEVICE in the status word;
+                             the outputs of that call are undefined, the context stays usable */
 } mla_decode_shape;
 
 /* Launch plan (plain data; copy freely).  The plan is the capture key of a

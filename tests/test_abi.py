@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     L = ctypes.CDLL(mla.LIB_PATH)
     for n in sorted(names):
         assert hasattr(L, n), f"{n} declared but not exported"
-    assert mla.abi_version() == 1
+    assert mla.abi_version() == 2
     assert "scratch" in mla.strerror(mla.ESCRATCH)
 
 
@@ -214,6 +214,13 @@ def test_plan_rejects(kw, status):
     with pytest.raises(mla.MLADecodeError) as e:
         _plan(**kw)
     assert e.value.status == status
+
+
+def test_plan_rejects_bad_stall_hook():
+    s = mla.Shape(batch=1, heads=16, d_latent=512, d_rope=64, sparse=0, max_ctx=16, topk=0, scale=SCALE,
+                  num_sms=152, splits_override=0, variant=0, pdl=0, stall_test=2)
+    assert mla.lib().mla_decode_plan(ctypes.byref(s), ctypes.byref(mla.Plan())) == mla.EINVAL
+    assert _plan(max_ctx=16, stall_test=True).shape.stall_test == 1
 
 
 def test_plan_rejects_bad_dims():

@@ -24,11 +24,12 @@ constexpr int kMaxDevices = 64;
 // of one CTA overlap them through the ring instead.
 constexpr int kCtasPerSm = 1;
 constexpr size_t kScratchAlign = 256;
-constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 32-row stages
+constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 64-row steps of 32-row slots
 constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
 constexpr int kVariantTc32 = 3;              // tcgen05 head-group-32 kernel, 64-row tiles (dense)
 
 int variant_tile_rows(int v) {
+    // warp-MMA: the model counts 32-row slots (a 64-row step costs about two)
     return v == kVariantTc ? mla::kTcTileRows : v == kVariantTc32 ? mla::kTcTileRows32 : mla::kStageRows;
 }
 int variant_granule(int v) { return v == kVariantWarpMma ? mla::kStageRows : mla::kTcGranule; }
@@ -239,8 +240,14 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
         if (rc != MLA_OK) return rc;
         return launch_status(mla::launch_partial_tc(maps, p, hg, grid, pl->shape.pdl != 0, st));
     }
-    // warp-MMA kernel: the query tile by TMA, cache rows by per-row bulk copies
+    // warp-MMA kernel: the query tile by TMA; dense cache rows by one TMA box
+    // per 32-row slot, sparse rows by per-row bulk copies
     mla::TcMaps maps{};
+    if (!pl->shape.sparse) {
+        if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
+        rc = encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kStageRows, MLA_D_ROW / 64);
+        if (rc != MLA_OK) return rc;
+    }
     rc = encode_bf16_row_chunks(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads, MLA_D_ROW,
                                 mla::kHeadGroup, MLA_D_ROW / 64);
     if (rc != MLA_OK) return rc;

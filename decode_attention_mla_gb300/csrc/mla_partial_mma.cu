@@ -1,4 +1,5 @@
-// mla_partial_mma.cu -- split-KV MLA decode partials, head-group-16 kernel.
+// mla_partial_mma.cu -- split-KV MLA decode partials, head-group-16 kernel on
+// warp-level tensor-core MMA (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 //
 // Work item = (request b, head group of 16 heads, context slice s); item i
 // decodes as hg = i % G, s = (i / G) % S, b = i / (G * S), so the items that
@@ -11,28 +12,33 @@
 // separate kernel).
 //
 // Warp roles:
-//   producer warp : walks the same items and, per 32-row stage, moves one
-//                   1152-byte cache row per lane into a 5-deep shared-memory
-//                   ring with bulk copies (TMA engine); completion is counted
-//                   on the stage's mbarrier.  Dense rows are base + e, sparse
-//                   rows base + indices[b][e] (a gather, "The Commit That
-//                   Changed Direction"); index loads are prefetched a few
-//                   stages ahead.  Rows past the slice or out of range are
-//                   zero-filled and masked.  It also stages the item's 16 query
-//                   rows in shared memory when the (request, head group)
-//                   changes.
-//   8 MMA warps   : scores S[16 heads x 32 rows] = Q . K^T with mma.m16n8k16
-//                   (bf16 in, fp32 accumulate).  Warp w takes k-steps
-//                   9*(w%4) .. 9*(w%4)+8 of the 576-wide contraction for rows
-//                   16*(w/4) .. +15; the four k-group partials are summed in
-//                   fixed order through shared memory.  Every warp applies the
-//                   same online-softmax update (base-2 exponent, quad shuffles
-//                   for row max and row sum) and accumulates its own 64 output
-//                   features: O += P . V with V = the latent c rows and P as a
-//                   bf16 hi + lo pair (two MMAs, ~16 significant bits of P).
+//   producer warp : (one warp of a warpgroup that hands its registers to the
+//                   MMA warps) fills a 4-deep ring of 32-row slots.  Dense slices: one
+//                   TMA box {64, 32 rows, 9 chunks} per slot, landing as
+//                   [chunk][row][128 B], 128-byte swizzled (rows past the end
+//                   of the cache read as zeros).  Sparse lists: one 1152-byte
+//                   bulk copy per row into padded 1168-byte rows, rows taken
+//                   from indices[b][e] (a gather, "The Commit That Changed
+//                   Direction"); masked entries are zero-filled.  It also
+//                   stages the item's 16 query rows (one TMA box) whenever the
+//                   (request, head group) changes.
+//   8 MMA warps   : consume 64-row steps (two slots).  Scores: warp w takes
+//                   rows 16*(w/2) .. +15 of the step and half of the 576-wide
+//                   contraction (k-steps 4c + 2*(w%2) + {0, 1} of each 64-column
+//                   chunk c, its query fragments held in registers); the two
+//                   halves meet through shared
+//                   memory, each warp finishing one 8-row tile.  Softmax keeps
+//                   one base-2 reference per head for the whole CTA and moves
+//                   it only when a score exceeds it by more than 8 (one
+//                   OR-barrier per step decides); each warp turns its 8 rows
+//                   into P = 2^(s - ref) as a bf16 hi + lo pair (about 16
+//                   significant bits) and publishes them.  P . V: warp w owns
+//                   output features 64w .. 64w+63 for all 16 heads and all 64
+//                   rows of the step.
 // No floating-point atomics: the result is a pure function of the inputs and
 // the split count.  Every wait is bounded; a timeout raises MLA_EDEVICE in the
-// status word and the CTA drains its copies before it exits.
+// status word, every warp leaves through the same barrier, and the CTA drains
+// its copies before it exits.
 #include <cfloat>
 #include <cmath>
 
@@ -45,41 +51,59 @@
 namespace mla {
 namespace {
 
-constexpr int kStages = 5;                                // ring depth (32-row stages)
+constexpr int kSlots = 4;                                  // ring depth (32-row slots)
+constexpr int kStepRows = 2 * kStageRows;                  // rows per consumer step (two slots)
 constexpr int kComputeWarps = 8;
-constexpr int kThreads = (kComputeWarps + 1) * 32;        // + one producer warp
+constexpr int kThreads = (kComputeWarps + 4) * 32;         // + a producer warpgroup (one working warp)
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kSmemRow = kRowBytes + 16;                  // padding: 8 rows x 16 B hit 32 distinct banks
-constexpr int kNT = kStageRows / 8;                       // 4 score n-tiles of 8 rows
-constexpr int kKGroups = 4;                               // contraction split across warps
-constexpr int kKStepsPerWarp = kDRow / 16 / kKGroups;     // 9
-constexpr int kFeatPerWarp = kDLatent / kComputeWarps;    // 64 output features per warp
-constexpr int kPVTiles = kFeatPerWarp / 8;                // 8
-constexpr int kPSteps = kStageRows / 16;                  // 2
-constexpr int kIdxPrefetch = 4;                           // sparse index prefetch depth (stages)
+// Register split: the CTA is launched with kLaunchRegs per thread; the
+// producer warpgroup drops to kProducerRegs and the two MMA warpgroups rise to
+// kMmaRegs (the query fragments of a contraction half alone take 72).
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 56;
+constexpr int kMmaRegs = 224;
+static_assert(128 * kProducerRegs + kComputeWarps * 32 * kMmaRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kChunks = kDRow / 64;                        // 9 column chunks of 64 bf16
+constexpr int kKSteps = kDRow / 16;                        // 36 k-steps of the score contraction
+constexpr int kKHalf = kKSteps / 2;                        // 18 per warp
+constexpr int kFeatPerWarp = kDLatent / kComputeWarps;     // 64 output features per warp
+constexpr int kPVTiles = kFeatPerWarp / 8;                 // 8 n-tiles of P . V per warp
+constexpr int kStepTiles = kStepRows / 8;                  // 8 score tiles of 8 rows per step
+constexpr int kIdxPrefetch = 4;                            // sparse index prefetch depth (slots)
 constexpr float kLn2 = 0.6931471805599453f;
-// Cache rows arrive by one 1152-byte bulk copy per row into padded 1168-byte
-// rows (8 consecutive rows hit 8 distinct 16-byte bank groups); the query tile
-// is one TMA box [9 chunks][16 rows][64 bf16], 128-byte swizzled.  (A TMA box
-// for whole dense stages was measured too: faster for single-stage slices,
-// slower for two-stage ones and for the timed T = 8192 shape.)
-constexpr int kChunks = kDRow / 64;                       // 9
-constexpr int kQChunkBytes = kHeadGroup * 128;            // 2048
+constexpr float kRescaleThreshold = 8.f;                   // log2 units: P stays <= 256
+// dense slot: [9 chunks][32 rows][128 B], swizzled; sparse slot: 32 padded rows
+constexpr int kDenseChunkBytes = kStageRows * 128;         // 4096
+constexpr int kDenseSlotBytes = kChunks * kDenseChunkBytes;  // 36,864
+constexpr int kSmemRow = kRowBytes + 16;                   // 8 consecutive rows hit 8 distinct 16-byte groups
+constexpr int kSparseSlotBytes = kStageRows * kSmemRow;    // 37,376
+constexpr int kQChunkBytes = kHeadGroup * 128;             // 2048
+constexpr int kStagePitch = kDLatent + 4;                  // floats per staged partial row (2064 B: 64-bit stores hit distinct banks)
+// named barriers: 0 is __syncthreads, 1..4 the four warp pairs, 5 the MMA warps
+constexpr int kBarPair0 = 1;
+constexpr int kBarMma = 5;
+constexpr int kMmaThreads = kComputeWarps * 32;
 
-static_assert(kComputeWarps == 2 * kKGroups, "warp w: k-group w % 4, row half w / 4");
-static_assert(kDRow / 16 % kKGroups == 0, "contraction split");
+static_assert(kDenseSlotBytes % 1024 == 0, "swizzled slots stay 1024-byte aligned");
+static_assert(kKHalf == 2 * kChunks && kComputeWarps == 2 * (kStepRows / 16),
+              "warp w: rows 16*(w/2), two k-steps of every chunk (half w%2)");
 
+template <bool kDense>
 struct __align__(1024) SharedStorage {
-    uint8_t q[kChunks * kQChunkBytes];                    // the item's 16 query rows (1024-byte aligned)
-    uint8_t kv[kStages][kStageRows * kSmemRow];           // stage slots
-    float4 red[2][kKGroups][kNT][32];                     // per-k-group partial scores
-    int valid[kStages][kStageRows];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t red_bar[2];
+    static constexpr int kSlotBytes = kDense ? kDenseSlotBytes : kSparseSlotBytes;
+    uint8_t q[kChunks * kQChunkBytes];                     // the item's 16 query rows (1024-byte aligned)
+    uint8_t kv[kSlots][kSlotBytes];                        // ring of 32-row slots
+    uint4 p[2][kStepTiles][32];                            // P of a step as mma A fragments, double-buffered
+    float4 red[kComputeWarps / 2][2][32];                  // half-contraction scores exchanged in each pair
+    float mx[kComputeWarps][kHeadGroup];                   // per-warp head maxima (reference moves)
+    float lsum[kComputeWarps][kHeadGroup];                 // per-warp row sums (epilogue)
+    int valid[kSlots][kStageRows];                         // sparse: row holds an attended entry
+    float stage_o[kHeadGroup][kStagePitch];                // the item's normalised partial, written out by bulk copies
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
     uint64_t q_full;
     uint64_t q_empty;
-    uint64_t stall_bar;                                   // test hook: a barrier nothing arrives at
+    uint64_t stall_bar;                                    // test hook: a barrier nothing arrives at
     int abort_flag;
 };
 
@@ -88,15 +112,43 @@ struct __align__(1024) SharedStorage {
 __device__ __forceinline__ uint32_t sw_off(int r, int b, int chunk_bytes) {
     return static_cast<uint32_t>((b >> 7) * chunk_bytes + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15));
 }
-__device__ __forceinline__ void raise_device_error(SharedStorage& sh, int* status) {
+// Lane offsets of the ldmatrix rows inside a slot.  Score operand: row r of
+// the slot (0..31), k-step 4c + 2*kh + j of chunk c; the part that varies with
+// c is added as a constant (c * chunk stride).  P . V operand: row r, features
+// 64w + 16i + 8*hi .. +7 of chunk w.
+template <bool kDense>
+__device__ __forceinline__ uint32_t qk_lane_off(int r, int kh, int j, int lmat) {
+    if constexpr (kDense)
+        return static_cast<uint32_t>(r * 128 + ((((4 * kh + 2 * j + (lmat & 1)) ^ (r & 7))) << 4));
+    else
+        return static_cast<uint32_t>(r * kSmemRow + (2 * kh + j) * 32 + (lmat & 1) * 16);
+}
+template <bool kDense>
+__device__ __forceinline__ uint32_t qk_chunk_stride() {
+    return kDense ? kDenseChunkBytes : 128;
+}
+template <bool kDense>
+__device__ __forceinline__ uint32_t pv_lane_off(int r, int w, int i, int hi) {
+    if constexpr (kDense)
+        return static_cast<uint32_t>(w * kDenseChunkBytes + r * 128 + (((2 * i + hi) ^ (r & 7)) << 4));
+    else
+        return static_cast<uint32_t>(r * kSmemRow + w * 128 + (2 * i + hi) * 16);
+}
+template <bool kDense>
+__host__ __device__ constexpr uint32_t row_pitch() {
+    return kDense ? 128 : kSmemRow;
+}
+
+template <bool kDense>
+__device__ __forceinline__ void raise_device_error(SharedStorage<kDense>& sh, int* status) {
     sh.abort_flag = 1;
     if (status) atomicCAS(status, 0, static_cast<int>(MLA_EDEVICE));
 }
 
 struct Item {
-    int b, hg, s, n_stages;
+    int b, hg, s, n_slots;
     long long base;
-    uint32_t e0, e1;                      // entries [e0, e1) of the request
+    uint32_t e0, e1;                       // entries [e0, e1) of the request
 };
 
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
@@ -108,7 +160,8 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     it.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
     it.b = static_cast<int>(b);
     // entry counts are below 2^31 (d_pos and the list length are int32), so
-    // the slice arithmetic runs in 32 bits (64-bit division is slow)
+    // the slice arithmetic runs in 32 bits (64-bit division is slow); dense
+    // entries are already clamped to the rows that exist in the cache
     const uint32_t n = static_cast<uint32_t>(
         request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
     const uint32_t per = slice_entries_u32(n, static_cast<uint32_t>(p.splits), kStageRows);
@@ -118,7 +171,7 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     if (e0 > e1) e0 = e1;
     it.e0 = e0;
     it.e1 = e1;
-    it.n_stages = static_cast<int>((e1 - e0 + kStageRows - 1) / kStageRows);
+    it.n_slots = static_cast<int>((e1 - e0 + kStageRows - 1) / kStageRows);
     return it;
 }
 
@@ -129,8 +182,9 @@ __device__ __forceinline__ int first_key(const PartialParams& p) {
     return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
 }
 
-__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int key,
-                                       int lane) {
+template <bool kDense>
+__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh,
+                                       int key, int lane) {
     if (lane == 0) {
         const int b = key / p.n_groups;
         const int hg = key - b * p.n_groups;
@@ -140,12 +194,37 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 }
 
 // ============================== producer ==================================
-__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage& sh, int lane) {
+// Dense: while the preceding kernel still runs, bring the first slots of the
+// CTA's first item into L2.  The context length read here may be stale (that
+// kernel may be advancing it): it only aims the prefetch, and every row the
+// kernel uses is loaded again after the grid dependency.
+__device__ void prefetch_first_slots(const TcMaps& maps, const PartialParams& p) {
+    const int item = static_cast<int>(blockIdx.x);
+    if (item >= p.n_items) return;
+    const int rest = item / p.n_groups;
+    const int b = rest / p.splits;
+    const int s = rest - b * p.splits;
+    const long long base = p.row_offset ? ld_relaxed_s64(p.row_offset + b) : 0;
+    if (base < 0 || base >= p.kv_rows) return;
+    long long n = static_cast<long long>(ld_relaxed_s32(p.d_pos + b)) + 1;
+    if (n > p.kv_rows - base) n = p.kv_rows - base;
+    if (n <= 0) return;
+    const long long per = slice_entries(n, p.splits, kStageRows);
+    const long long e0 = static_cast<long long>(s) * per;
+    long long e1 = e0 + per;
+    if (e1 > n) e1 = n;
+    for (long long e = e0, k = 0; e < e1 && k < kSlots; e += kStageRows, ++k)
+        tma_prefetch_3d(&maps.kv, 0, static_cast<int>(base + e), 0);
+}
+
+template <bool kDense>
+__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh, int lane) {
     const uint64_t policy = l2_policy_evict_first();
-    int stage = 0;            // stages issued so far (ring position)
-    // the first query tile is requested before the context length is read; the
-    // MMA warps follow the same sequence of keys (a new tile whenever a busy
-    // item's key differs) and release a tile through q_empty, read or not
+    int stage = 0;            // slots issued so far (ring position)
+    // the first query tile is requested before the item is decoded (its key
+    // needs no context length); the MMA warps follow the same sequence of keys
+    // (a new tile whenever a busy item's key differs) and release a tile
+    // through q_empty, read or not
     int q_key = first_key(p);
     load_q(maps, p, sh, q_key, lane);
     int q_loads = 1;          // query tiles staged so far
@@ -153,8 +232,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     bool ok = !(p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it = decode_item(p, item);
-        if (it.n_stages == 0) continue;
-        const int seg_len = p.sparse ? p.cache_len[it.b] : 0;
+        if (it.n_slots == 0) continue;
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
             if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
@@ -165,63 +243,78 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             q_key = key;
             ++q_loads;
         }
-        // sparse: indices of the next few stages, loaded ahead of their use
-        int idx_pf[kIdxPrefetch];
-        const int* idx = p.sparse ? p.indices + static_cast<long long>(it.b) * p.topk : nullptr;
-        if (p.sparse) {
-#pragma unroll
-            for (int k = 0; k < kIdxPrefetch; ++k) {
-                const long long e = it.e0 + static_cast<long long>(k) * kStageRows + lane;
-                idx_pf[k] = (e < it.e1) ? idx[e] : -1;
-            }
-        }
-        for (int st = 0; st < it.n_stages; ++st, ++stage) {
-            const int slot = stage % kStages;
-            if (stage >= kStages &&
-                !mbar_wait_bounded(&sh.empty[slot], ((stage / kStages) - 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
-            const long long e = it.e0 + static_cast<long long>(st) * kStageRows + lane;
-            bool valid = false;
-            long long row = 0;
-            if (e < it.e1) {
-                if (!p.sparse) {
-                    row = it.base + e;
-                    valid = (row >= 0 && row < p.kv_rows);
-                } else {
-                    const int id = idx_pf[0];
-                    if (id >= 0 && id < seg_len) {
-                        row = it.base + id;
-                        valid = (row >= 0 && row < p.kv_rows);
+        if constexpr (kDense) {
+            // one TMA box per slot from lane 0; rows before the cache (a
+            // negative first row) and past its end read as zeros
+            if (lane == 0) {
+                for (int st = 0; st < it.n_slots; ++st, ++stage) {
+                    const int slot = stage % kSlots;
+                    if (stage >= kSlots &&
+                        !mbar_wait_bounded(&sh.empty[slot], ((stage / kSlots) - 1) & 1, &sh.abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    long long y = it.base + it.e0 + static_cast<long long>(st) * kStageRows;
+                    if (y < -2 * kStageRows) y = -2 * kStageRows;   // a box wholly before row 0 either way
+                    mbar_arrive_expect_tx(&sh.full[slot], kDenseSlotBytes);
+                    tma_load_3d(sh.kv[slot], &maps.kv, 0, static_cast<int>(y), 0, &sh.full[slot], policy);
                 }
             }
-            if (p.sparse) {
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            stage = __shfl_sync(0xffffffffu, stage, 0);
+        } else {
+            // one row per lane per slot; indices of the next few slots are
+            // loaded ahead of their use
+            const int seg_len = p.cache_len[it.b];
+            const int* idx = p.indices + static_cast<long long>(it.b) * p.topk;
+            int idx_pf[kIdxPrefetch];
+#pragma unroll
+            for (int k = 0; k < kIdxPrefetch; ++k) {
+                const uint32_t e = it.e0 + static_cast<uint32_t>(k * kStageRows + lane);
+                idx_pf[k] = (e < it.e1) ? idx[e] : -1;
+            }
+            for (int st = 0; st < it.n_slots; ++st, ++stage) {
+                const int slot = stage % kSlots;
+                if (stage >= kSlots &&
+                    !mbar_wait_bounded(&sh.empty[slot], ((stage / kSlots) - 1) & 1, &sh.abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int id = idx_pf[0];
+                long long row = 0;
+                bool valid = false;
+                if (id >= 0 && id < seg_len) {
+                    row = it.base + id;
+                    valid = (row >= 0 && row < p.kv_rows);
+                }
 #pragma unroll
                 for (int k = 0; k + 1 < kIdxPrefetch; ++k) idx_pf[k] = idx_pf[k + 1];
-                const long long en = it.e0 + static_cast<long long>(st + kIdxPrefetch) * kStageRows + lane;
+                const uint32_t en = it.e0 + static_cast<uint32_t>((st + kIdxPrefetch) * kStageRows + lane);
                 idx_pf[kIdxPrefetch - 1] = (en < it.e1) ? idx[en] : -1;
-            }
-            uint8_t* dst = sh.kv[slot] + lane * kSmemRow;
-            sh.valid[slot][lane] = valid ? 1 : 0;
-            if (!valid) {
-                // masked rows still feed P . V (with p = 0): keep them finite
-                uint4* z = reinterpret_cast<uint4*>(dst);
+
+                uint8_t* dst = sh.kv[slot] + lane * kSmemRow;
+                sh.valid[slot][lane] = valid ? 1 : 0;
+                if (!valid) {
+                    // masked rows still feed P . V (with p = 0): keep them finite
+                    uint4* z = reinterpret_cast<uint4*>(dst);
 #pragma unroll 8
-                for (int i = 0; i < kRowBytes / 16; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int i = 0; i < kRowBytes / 16; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();   // before a later copy lands on these bytes
+                }
+                const uint32_t n_valid = __popc(__ballot_sync(0xffffffffu, valid));
+                __syncwarp();                   // zero rows and flags before the arrival that publishes them
+                if (lane == 0) mbar_arrive_expect_tx(&sh.full[slot], n_valid * static_cast<uint32_t>(kRowBytes));
+                __syncwarp();                   // the byte count is registered before any copy lands
+                if (valid) bulk_copy_g2s(dst, p.kv + row * p.row_stride, kRowBytes, &sh.full[slot], policy);
             }
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sh.full[slot], valid ? static_cast<uint32_t>(kRowBytes) : 0u);
-            if (valid) bulk_copy_g2s(dst, p.kv + row * p.row_stride, kRowBytes, &sh.full[slot], policy);
         }
     }
     if (!ok && lane == 0) raise_device_error(sh, p.status);
     // Never retire the CTA with copies into its shared memory in flight.
     if (lane == 0) {
         volatile int never = 0;
-        for (int slot = 0; slot < kStages && slot < stage; ++slot) {
-            const int last_use = (stage - 1 - slot) / kStages;
+        for (int slot = 0; slot < kSlots && slot < stage; ++slot) {
+            const int last_use = (stage - 1 - slot) / kSlots;
             if (!mbar_wait_bounded(&sh.full[slot], last_use & 1, &never)) raise_device_error(sh, p.status);
         }
         if (q_loads > 0 && !mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never))
@@ -230,261 +323,413 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
 }
 
 // ============================== MMA warps =================================
-__device__ void consumer(const PartialParams& p, SharedStorage& sh, int w, int lane) {
+// Bounded wait whose answer is the same on every lane of the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag));
+}
+__device__ __forceinline__ float4 as_float4(const float (&v)[4]) { return make_float4(v[0], v[1], v[2], v[3]); }
+
+// One k-step (16 rows) of O += P . V for this warp's 64 features: P as the
+// A fragments of the published hi / lo pairs, V by transposing ldmatrix;
+// all eight low-part MMAs first, then the high parts (each accumulator's two
+// MMAs eight instructions apart).
+template <bool kDense>
+__device__ __forceinline__ void pv_kstep(float (&o)[kPVTiles][4], const uint4* pt, int kp, uint32_t vbase,
+                                         const uint32_t (&pv_off)[kPVTiles / 2], int v_hi, int tq, int lane) {
+    const uint4 t0 = pt[(2 * kp) * 32 + lane];
+    const uint4 t1 = pt[(2 * kp + 1) * 32 + lane];
+    const uint32_t a_hi[4] = {t0.x, t0.y, t1.x, t1.y};
+    const uint32_t a_lo[4] = {t0.z, t0.w, t1.z, t1.w};
+    uint32_t v[kPVTiles / 2][4];
+#pragma unroll
+    for (int i = 0; i < kPVTiles / 2; ++i) ldmatrix_x4_trans(v[i], vbase + pv_off[i]);
+    // dense rows past the slice may hold anything (even NaN): zero their V so
+    // that p = 0 really contributes nothing
+    if (kDense && v_hi < 16 * (kp + 1)) {
+        const int k0 = 16 * kp + 2 * tq;
+        const uint32_t m_lo = (k0 < v_hi ? 0x0000ffffu : 0u) | (k0 + 1 < v_hi ? 0xffff0000u : 0u);
+        const uint32_t m_hi = (k0 + 8 < v_hi ? 0x0000ffffu : 0u) | (k0 + 9 < v_hi ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int i = 0; i < kPVTiles / 2; ++i) {
+            v[i][0] &= m_lo;
+            v[i][1] &= m_hi;
+            v[i][2] &= m_lo;
+            v[i][3] &= m_hi;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPVTiles / 2; ++i) {
+        mma_bf16_16816(o[2 * i], a_lo, v[i][0], v[i][1]);
+        mma_bf16_16816(o[2 * i + 1], a_lo, v[i][2], v[i][3]);
+    }
+#pragma unroll
+    for (int i = 0; i < kPVTiles / 2; ++i) {
+        mma_bf16_16816(o[2 * i], a_hi, v[i][0], v[i][1]);
+        mma_bf16_16816(o[2 * i + 1], a_hi, v[i][2], v[i][3]);
+    }
+}
+
+template <bool kDense>
+__device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int w, int lane) {
+    constexpr uint32_t kSlotBytes = SharedStorage<kDense>::kSlotBytes;
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int kg = w % kKGroups;           // contraction k-group
-    const int rh = w / kKGroups;           // row half (n-tiles 2rh, 2rh+1) of the score tile
-    const int f_base = w * kFeatPerWarp;   // own output features
+    const int pr = w >> 1;                  // warp pair: rows 16*pr .. +15 of a step
+    const int kh = w & 1;                   // contraction half, and the pair's 8-row tile this warp finishes
+    const int my_tile = 2 * pr + kh;        // score tile of 8 rows (step rows 8*my_tile ..)
+    const int r_own = 8 * my_tile + 2 * tq; // step rows of this lane's scores: r_own, r_own + 1
+    const int f_base = w * kFeatPerWarp;    // own output features
     const int lrow = lane & 7;
     const int lmat = lane >> 3;
     const uint32_t q_base = smem_u32(sh.q);
+    const uint32_t kv_base = smem_u32(sh.kv[0]);
+    // ldmatrix lane offsets: score rows 16*(pr%2) + lrow + 8*(lmat/2) of the
+    // pair's slot; P . V rows lrow + 8*(lmat%2) (+16 for odd k-steps)
+    const int qk_row = 16 * (pr & 1) + lrow + ((lmat >> 1) << 3);
+    const uint32_t qk_off[2] = {qk_lane_off<kDense>(qk_row, kh, 0, lmat), qk_lane_off<kDense>(qk_row, kh, 1, lmat)};
+    const int pv_row = lrow + ((lmat & 1) << 3);
+    uint32_t pv_off[kPVTiles / 2];
+#pragma unroll
+    for (int i = 0; i < kPVTiles / 2; ++i) pv_off[i] = pv_lane_off<kDense>(pv_row, w, i, lmat >> 1);
 
-    uint32_t qa[kKStepsPerWarp][4];
-    int stage = 0;
-    int red_round = 0;
-    int q_phase = 0;                       // query tiles consumed (q_full phases)
-    int q_key = first_key(p);              // key of the tile the producer loaded last
-    bool q_in_regs = false;                // that tile is in registers (and released)
-    bool ok = true;
+    uint32_t qa[kKHalf][4];                 // query fragments of this warp's contraction half
+    int stage = 0;                          // slots consumed so far (ring position)
+    int pbuf = 0;                           // P buffer of the next step
+    int q_phase = 0;                        // query tiles consumed (q_full phases)
+    int q_key = first_key(p);               // key of the tile the producer loaded last
+    bool q_in_regs = false;                 // that tile is in registers (and released)
+    bool failed = false;                    // a wait of this warp ran out
+    bool stop = false;                      // every warp saw a failure at the same barrier: leave
 
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+    for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
         const Item it = decode_item(p, item);
-        if (it.n_stages == 0) {
+        if (it.n_slots == 0) {
             write_empty_partial(p.o_part, p.lse_part,
                                 (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s,
-                                p.splits, w * 32 + lane, kComputeWarps * 32);
+                                p.splits, w * 32 + lane, kMmaThreads);
             continue;
         }
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
-            // the producer loads another tile over this one: release it, read or
-            // not (it must have landed first)
-            if (!q_in_regs) {
-                if (!mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
-                    ok = false;
-                    break;
+            // the producer loads another tile over this one: release it, read
+            // or not (it must have landed first)
+            if (!q_in_regs && !failed) {
+                if (warp_wait(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
+                    if (lane == 0) mbar_arrive(&sh.q_empty);
+                } else {
+                    failed = true;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.q_empty);
             }
             ++q_phase;
             q_key = key;
             q_in_regs = false;
         }
-        if (!q_in_regs) {
-            if (!mbar_wait_bounded(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
-            // fragments of Q rows g, g+8 for this warp's 9 k-steps
+        if (!q_in_regs && !failed) {
+            if (warp_wait(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
 #pragma unroll
-            for (int kk = 0; kk < kKStepsPerWarp; ++kk) {
-                const int cb = ((kg * kKStepsPerWarp + kk) * 16 + 2 * tq) * 2;
-                qa[kk][0] = ld_shared_u32(q_base + sw_off(g, cb, kQChunkBytes));
-                qa[kk][1] = ld_shared_u32(q_base + sw_off(g + 8, cb, kQChunkBytes));
-                qa[kk][2] = ld_shared_u32(q_base + sw_off(g, cb + 16, kQChunkBytes));
-                qa[kk][3] = ld_shared_u32(q_base + sw_off(g + 8, cb + 16, kQChunkBytes));
+                for (int kk = 0; kk < kKHalf; ++kk)
+                    ldmatrix_x4(qa[kk], q_base + sw_off(lrow + ((lmat & 1) << 3),
+                                                         (4 * (kk >> 1) + 2 * kh + (kk & 1)) * 32 + ((lmat >> 1) << 4),
+                                                         kQChunkBytes));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.q_empty);
+                q_in_regs = true;
+            } else {
+                failed = true;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.q_empty);
-            q_in_regs = true;
         }
 
         float o[kPVTiles][4];
 #pragma unroll
         for (int i = 0; i < kPVTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_run[2] = {-INFINITY, -INFINITY};   // running max, base-2 units
-        float l_run[2] = {0.f, 0.f};               // running sum of 2^(s - m_run)
+        float m_ref[2] = {-INFINITY, -INFINITY};   // heads g, g+8: base-2 reference shared by the CTA
+        float l_own[2] = {0.f, 0.f};               // sums of 2^(s - ref) over this lane's rows
+        const int n_steps = (it.n_slots + 1) >> 1;
+        for (int step = 0; step < n_steps; ++step) {
+            const int halves = min(2, it.n_slots - 2 * step);
+            const int slot_a = stage % kSlots;
+            const int slot_b = (stage + 1) % kSlots;
+            if (!failed && !warp_wait(&sh.full[slot_a], (stage / kSlots) & 1, &sh.abort_flag)) failed = true;
+            if (!failed && halves == 2 && !warp_wait(&sh.full[slot_b], ((stage + 1) / kSlots) & 1, &sh.abort_flag))
+                failed = true;
+            // step rows [v_lo, v_hi) are attended (dense); sparse rows carry flags
+            const uint32_t e_step = it.e0 + static_cast<uint32_t>(step * kStepRows);
+            const int v_hi = static_cast<int>(min(it.e1 - e_step, static_cast<uint32_t>(kStepRows)));
+            const long long first_row = it.base + e_step;
+            const int v_lo = first_row >= 0 ? 0 : first_row <= -kStepRows ? kStepRows : static_cast<int>(-first_row);
+            const bool active = (pr >> 1) < halves;     // this pair's rows are in a loaded slot
+            const int my_slot = (pr >> 1) ? slot_b : slot_a;
 
-        for (int st = 0; st < it.n_stages; ++st, ++stage) {
-            const int slot = stage % kStages;
-            if (!mbar_wait_bounded(&sh.full[slot], (stage / kStages) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
+            // ---- scores of this warp's 8-row tile: two contraction halves ------
+            float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (active) {
+                float acc[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+                if (!failed) {
+                    // two accumulation chains per tile (even / odd k-steps), added once
+                    float acc2[2][4];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) acc2[j][0] = acc2[j][1] = acc2[j][2] = acc2[j][3] = 0.f;
+                    const uint32_t sbase = kv_base + static_cast<uint32_t>(my_slot) * kSlotBytes;
+                    const uint32_t a0 = sbase + qk_off[0];
+                    const uint32_t a1 = sbase + qk_off[1];
+#pragma unroll
+                    for (int kk = 0; kk < kKHalf; ++kk) {
+                        uint32_t bf[4];
+                        ldmatrix_x4(bf, ((kk & 1) ? a1 : a0) + (kk >> 1) * qk_chunk_stride<kDense>());
+                        if (kk & 1) {
+                            mma_bf16_16816(acc2[0], qa[kk], bf[0], bf[1]);
+                            mma_bf16_16816(acc2[1], qa[kk], bf[2], bf[3]);
+                        } else {
+                            mma_bf16_16816(acc[0], qa[kk], bf[0], bf[1]);
+                            mma_bf16_16816(acc[1], qa[kk], bf[2], bf[3]);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[j][c] += acc2[j][c];
+                }
+                // hand the other tile's half to the partner, take ours
+                sh.red[pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
+                named_barrier_sync(kBarPair0 + pr, 64);
+                const float4 other = sh.red[pr][kh][lane];
+                const float4 mine = kh ? as_float4(acc[1]) : as_float4(acc[0]);
+                bool v0, v1;
+                if constexpr (kDense) {
+                    v0 = r_own >= v_lo && r_own < v_hi;
+                    v1 = r_own + 1 >= v_lo && r_own + 1 < v_hi;
+                } else {
+                    v0 = sh.valid[my_slot][r_own & (kStageRows - 1)] != 0;
+                    v1 = sh.valid[my_slot][(r_own + 1) & (kStageRows - 1)] != 0;
+                }
+                if (!failed) {
+                    sc[0] = v0 ? (mine.x + other.x) * p.scale_log2 : -INFINITY;
+                    sc[1] = v1 ? (mine.y + other.y) * p.scale_log2 : -INFINITY;
+                    sc[2] = v0 ? (mine.z + other.z) * p.scale_log2 : -INFINITY;
+                    sc[3] = v1 ? (mine.w + other.w) * p.scale_log2 : -INFINITY;
+                }
             }
-            const uint32_t kv_base = smem_u32(sh.kv[slot]);
+            float mx0 = fmaxf(sc[0], sc[1]);   // head g over this lane's two rows
+            float mx1 = fmaxf(sc[2], sc[3]);   // head g + 8
 
-            // ---- partial scores: rows 16rh..16rh+15, this warp's 144 features
-            float acc[2][4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < kKStepsPerWarp; ++kk) {
-                const int col_bytes = (kg * kKStepsPerWarp + kk) * 32;
-                const int row = 16 * rh + lrow + ((lmat >> 1) << 3);
-                uint32_t bf[4];
-                ldmatrix_x4(bf, kv_base + row * kSmemRow + col_bytes + ((lmat & 1) << 4));
-                mma_bf16_16816(acc[0], qa[kk], bf[0], bf[1]);
-                mma_bf16_16816(acc[1], qa[kk], bf[2], bf[3]);
+            // ---- P against the shared reference; move it only when needed ------
+            float pv[4];
+            bool need = true;                  // the first step of an item sets the reference
+            if (step > 0) {
+                const float ref0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
+                const float ref1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
+                pv[0] = ex2_approx(sc[0] - ref0);
+                pv[1] = ex2_approx(sc[1] - ref0);
+                pv[2] = ex2_approx(sc[2] - ref1);
+                pv[3] = ex2_approx(sc[3] - ref1);
+                uint4 pk;
+                split_bf16x2(pv[0], pv[1], pk.x, pk.z);
+                split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                sh.p[pbuf][my_tile][lane] = pk;
+                const bool over = mx0 > m_ref[0] + kRescaleThreshold || mx1 > m_ref[1] + kRescaleThreshold;
+                need = named_barrier_or(kBarMma, kMmaThreads, over || failed);
             }
+            if (need) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                if (tq == 0) {
+                    sh.mx[w][g] = mx0;
+                    sh.mx[w][g + 8] = mx1;
+                }
+                if (named_barrier_or(kBarMma, kMmaThreads, failed)) {
+                    stop = true;
+                    break;
+                }
+                float n0 = m_ref[0], n1 = m_ref[1];
+#pragma unroll
+                for (int v = 0; v < kComputeWarps; ++v) {
+                    n0 = fmaxf(n0, sh.mx[v][g]);
+                    n1 = fmaxf(n1, sh.mx[v][g + 8]);
+                }
+                if (step > 0) {
+                    // what was accumulated against the old reference, scaled to the new one
+                    const float a0 = m_ref[0] == -INFINITY ? 0.f : ex2_approx(m_ref[0] - n0);
+                    const float a1 = m_ref[1] == -INFINITY ? 0.f : ex2_approx(m_ref[1] - n1);
+#pragma unroll
+                    for (int i = 0; i < kPVTiles; ++i) {
+                        o[i][0] *= a0;
+                        o[i][1] *= a0;
+                        o[i][2] *= a1;
+                        o[i][3] *= a1;
+                    }
+                    l_own[0] *= a0;
+                    l_own[1] *= a1;
+                }
+                m_ref[0] = n0;
+                m_ref[1] = n1;
+                const float ref0 = n0 == -INFINITY ? 0.f : n0;   // nothing attended yet: keep exponents finite
+                const float ref1 = n1 == -INFINITY ? 0.f : n1;
+                pv[0] = ex2_approx(sc[0] - ref0);
+                pv[1] = ex2_approx(sc[1] - ref0);
+                pv[2] = ex2_approx(sc[2] - ref1);
+                pv[3] = ex2_approx(sc[3] - ref1);
+                uint4 pk;
+                split_bf16x2(pv[0], pv[1], pk.x, pk.z);
+                split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                sh.p[pbuf][my_tile][lane] = pk;
+                named_barrier_sync(kBarMma, kMmaThreads);
+            }
+            l_own[0] += pv[0] + pv[1];
+            l_own[1] += pv[2] + pv[3];
 
-            // ---- sum the four k-groups (fixed order) ------------------------
-            const int rb = red_round & 1;
-            sh.red[rb][kg][2 * rh][lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-            sh.red[rb][kg][2 * rh + 1][lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-            mbar_arrive(&sh.red_bar[rb]);
-            if (!mbar_wait_bounded(&sh.red_bar[rb], (red_round >> 1) & 1, &sh.abort_flag)) {
-                ok = false;
-                break;
-            }
-            ++red_round;
-            float sc[kNT][4];
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                const float4 v0 = sh.red[rb][0][j][lane];
-                const float4 v1 = sh.red[rb][1][j][lane];
-                const float4 v2 = sh.red[rb][2][j][lane];
-                const float4 v3 = sh.red[rb][3][j][lane];
-                sc[j][0] = ((v0.x + v1.x) + v2.x) + v3.x;
-                sc[j][1] = ((v0.y + v1.y) + v2.y) + v3.y;
-                sc[j][2] = ((v0.z + v1.z) + v2.z) + v3.z;
-                sc[j][3] = ((v0.w + v1.w) + v2.w) + v3.w;
-            }
-
-            // ---- online softmax (identical in every MMA warp) -----------------
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                const int c0 = 8 * j + 2 * tq;
-                const bool v0 = sh.valid[slot][c0] != 0;
-                const bool v1 = sh.valid[slot][c0 + 1] != 0;
-                sc[j][0] = v0 ? sc[j][0] * p.scale_log2 : -INFINITY;
-                sc[j][1] = v1 ? sc[j][1] * p.scale_log2 : -INFINITY;
-                sc[j][2] = v0 ? sc[j][2] * p.scale_log2 : -INFINITY;
-                sc[j][3] = v1 ? sc[j][3] * p.scale_log2 : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
-                mx1 = fmaxf(mx1, fmaxf(sc[j][2], sc[j][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m_run[0], mx0);
-            const float mn1 = fmaxf(m_run[1], mx1);
-            const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;   // nothing attended yet: keep exponents finite
-            const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float alpha0 = exp2f(m_run[0] - ref0);
-            const float alpha1 = exp2f(m_run[1] - ref1);
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                sc[j][0] = exp2f(sc[j][0] - ref0);
-                sc[j][1] = exp2f(sc[j][1] - ref0);
-                sc[j][2] = exp2f(sc[j][2] - ref1);
-                sc[j][3] = exp2f(sc[j][3] - ref1);
-                ls0 += sc[j][0] + sc[j][1];
-                ls1 += sc[j][2] + sc[j][3];
-            }
-            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
-            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
-            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
-            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
-            l_run[0] = l_run[0] * alpha0 + ls0;
-            l_run[1] = l_run[1] * alpha1 + ls1;
-            m_run[0] = mn0;
-            m_run[1] = mn1;
-#pragma unroll
-            for (int i = 0; i < kPVTiles; ++i) {
-                o[i][0] *= alpha0;
-                o[i][1] *= alpha0;
-                o[i][2] *= alpha1;
-                o[i][3] *= alpha1;
-            }
-
-            // ---- P as a bf16 hi + lo pair (A operand of P . V) ------------------
-            uint32_t pa_hi[kPSteps][4], pa_lo[kPSteps][4];
-#pragma unroll
-            for (int kp = 0; kp < kPSteps; ++kp) {
-                split_bf16x2(sc[2 * kp][0], sc[2 * kp][1], pa_hi[kp][0], pa_lo[kp][0]);
-                split_bf16x2(sc[2 * kp][2], sc[2 * kp][3], pa_hi[kp][1], pa_lo[kp][1]);
-                split_bf16x2(sc[2 * kp + 1][0], sc[2 * kp + 1][1], pa_hi[kp][2], pa_lo[kp][2]);
-                split_bf16x2(sc[2 * kp + 1][2], sc[2 * kp + 1][3], pa_hi[kp][3], pa_lo[kp][3]);
-            }
-            // ---- O[:, own 64 features] += P . V ---------------------------------
-#pragma unroll
-            for (int nt = 0; nt < kPVTiles; nt += 2) {
-#pragma unroll
-                for (int kp = 0; kp < kPSteps; ++kp) {
-                    const int row = 16 * kp + lrow + ((lmat & 1) << 3);
-                    const int fbytes = (f_base + 8 * nt + ((lmat >> 1) << 3)) * 2;
-                    uint32_t vb[4];
-                    ldmatrix_x4_trans(vb, kv_base + row * kSmemRow + fbytes);
-                    mma_bf16_16816(o[nt], pa_lo[kp], vb[0], vb[1]);
-                    mma_bf16_16816(o[nt + 1], pa_lo[kp], vb[2], vb[3]);
-                    mma_bf16_16816(o[nt], pa_hi[kp], vb[0], vb[1]);
-                    mma_bf16_16816(o[nt + 1], pa_hi[kp], vb[2], vb[3]);
+            // ---- O[:, own 64 features] += P . V over the step's rows ------------
+            {
+                const uint4* pt = &sh.p[pbuf][0][0];
+                const uint32_t va = kv_base + static_cast<uint32_t>(slot_a) * kSlotBytes;
+                const uint32_t vb = kv_base + static_cast<uint32_t>(slot_b) * kSlotBytes;
+                const uint32_t kHalfSlot = 16 * row_pitch<kDense>();
+                pv_kstep<kDense>(o, pt, 0, va, pv_off, v_hi, tq, lane);
+                pv_kstep<kDense>(o, pt, 1, va + kHalfSlot, pv_off, v_hi, tq, lane);
+                if (halves == 2) {
+                    pv_kstep<kDense>(o, pt, 2, vb, pv_off, v_hi, tq, lane);
+                    pv_kstep<kDense>(o, pt, 3, vb + kHalfSlot, pv_off, v_hi, tq, lane);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[slot]);
+            if (lane == 0) {
+                mbar_arrive(&sh.empty[slot_a]);
+                if (halves == 2) mbar_arrive(&sh.empty[slot_b]);
+            }
+            stage += halves;
+            pbuf ^= 1;
         }
-        if (!ok) break;
+        if (stop) break;
 
-        // ---- epilogue: normalised partial and its log-sum-exp -------------------
-        const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
-        const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
-        const int h0 = it.hg * kHeadGroup;
-        const long long row0 = (static_cast<long long>(it.b) * p.heads + h0 + g) * p.splits + it.s;
-        const long long row1 = (static_cast<long long>(it.b) * p.heads + h0 + g + 8) * p.splits + it.s;
-        float* op0 = p.o_part + row0 * kDLatent + f_base + 2 * tq;
-        float* op1 = p.o_part + row1 * kDLatent + f_base + 2 * tq;
+        // ---- epilogue: row sums (lane, quad, warps in order), normalised partial
+        // staged in shared memory and written as 16 contiguous 2 KB rows
+        float l0 = l_own[0], l1 = l_own[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (tq == 0) {
+            sh.lsum[w][g] = l0;
+            sh.lsum[w][g + 8] = l1;
+        }
+        if (w == 0) bulk_wait_read_all();      // the previous item's rows have left the staging buffer
+        named_barrier_sync(kBarMma, kMmaThreads);
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < kComputeWarps; ++v) {
+            L0 += sh.lsum[v][g];
+            L1 += sh.lsum[v][g + 8];
+        }
+        const float inv0 = L0 > 0.f ? rcp_approx(L0) : 0.f;
+        const float inv1 = L1 > 0.f ? rcp_approx(L1) : 0.f;
 #pragma unroll
         for (int nt = 0; nt < kPVTiles; ++nt) {
-            *reinterpret_cast<float2*>(op0 + 8 * nt) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-            *reinterpret_cast<float2*>(op1 + 8 * nt) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+            const int f = f_base + 8 * nt + 2 * tq;
+            *reinterpret_cast<float2*>(&sh.stage_o[g][f]) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
+            *reinterpret_cast<float2*>(&sh.stage_o[g + 8][f]) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
         }
-        if (w == 0 && tq == 0) {
-            p.lse_part[row0] = l_run[0] > 0.f ? (m_run[0] + log2f(l_run[0])) * kLn2 : -INFINITY;
-            p.lse_part[row1] = l_run[1] > 0.f ? (m_run[1] + log2f(l_run[1])) * kLn2 : -INFINITY;
+        fence_proxy_async_smem();              // the staged rows, before the bulk copies read them
+        named_barrier_sync(kBarMma, kMmaThreads);
+        const long long row_h0 = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s;
+        if (w == 0 && lane < kHeadGroup) {
+            bulk_store_s2g(p.o_part + (row_h0 + static_cast<long long>(lane) * p.splits) * kDLatent, sh.stage_o[lane],
+                           kDLatent * 4);
+            bulk_commit();
+        }
+        if (w == 1 && tq == 0) {
+            p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
+                L0 > 0.f ? (m_ref[0] + lg2_approx(L0)) * kLn2 : -INFINITY;
+            p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
+                L1 > 0.f ? (m_ref[1] + lg2_approx(L1)) * kLn2 : -INFINITY;
         }
     }
-    if (!ok && lane == 0) raise_device_error(sh, p.status);
+    if (w == 0) bulk_wait_all();               // rows written before the CTA retires
+    if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
 }
 
+template <bool kDense>
 __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __grid_constant__ TcMaps maps,
                                                                        const PartialParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SharedStorage& sh =
-        *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SharedStorage<kDense>& sh = *reinterpret_cast<SharedStorage<kDense>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sh.full[i], 32);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], kComputeWarps);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&sh.red_bar[i], kComputeWarps * 32);
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, kComputeWarps);
         mbar_init(&sh.stall_bar, 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }
+    if (threadIdx.x == kProducerWarp * 32) {
+        // the descriptors are kernel parameters: fetch them while the grid
+        // dependency is pending
+        prefetch_tensormap(&maps.q);
+        if constexpr (kDense) prefetch_tensormap(&maps.kv);
+    }
     __syncthreads();
     // Inputs (d_pos, cache rows, indices, q) may be written by the kernel
-    // before this one on the stream: wait for it before any global read.
-    grid_dependency_wait();
-    allow_dependent_launch();
-    if (warp == kProducerWarp)
-        producer(maps, p, sh, lane);
-    else
-        consumer(p, sh, warp, lane);
+    // before this one on the stream: every read that counts waits for it.
+    // Each role's register share is set right before its code.
+    if (warp >= kComputeWarps) {
+        warpgroup_regs_decrease<kProducerRegs>();
+        if constexpr (kDense) {
+            if (warp == kProducerWarp + 1 && lane == 0) prefetch_first_slots(maps, p);
+        }
+        if (warp == kProducerWarp) {
+            grid_dependency_wait();
+            allow_dependent_launch();
+            producer<kDense>(maps, p, sh, lane);
+        }
+    } else {
+        warpgroup_regs_increase<kMmaRegs>();
+        grid_dependency_wait();
+        allow_dependent_launch();
+        consumer<kDense>(p, sh, warp, lane);
+    }
 }
+
+template <bool kDense>
+size_t smem_bytes() {
+    return sizeof(SharedStorage<kDense>) + 1024;
+}
+static_assert(sizeof(SharedStorage<true>) + 1024 <= 227 * 1024, "dense shared memory");
+static_assert(sizeof(SharedStorage<false>) + 1024 <= 227 * 1024, "sparse shared memory");
 
 }  // namespace
 
-size_t partial_mma_smem_bytes() { return sizeof(SharedStorage) + 1024; }
+size_t partial_mma_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
 int partial_mma_block_threads() { return kThreads; }
 
+template <bool kDense>
+cudaError_t prepare_one() {
+    // the register split assumes kLaunchRegs per thread at launch: with fewer,
+    // the MMA warpgroups' increase could never be granted
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, mla_partial_mma_kernel<kDense>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(mla_partial_mma_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes<kDense>()));
+}
+
 cudaError_t partial_mma_prepare(int /*device*/) {
-    return cudaFuncSetAttribute(mla_partial_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(partial_mma_smem_bytes()));
+    cudaError_t e = prepare_one<true>();
+    if (e != cudaSuccess) return e;
+    return prepare_one<false>();
 }
 
 cudaError_t partial_mma_occupancy(int* ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, mla_partial_mma_kernel, kThreads,
-                                                         partial_mma_smem_bytes());
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, mla_partial_mma_kernel<false>, kThreads,
+                                                         smem_bytes<false>());
 }
 
 cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl,
@@ -492,14 +737,15 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = partial_mma_smem_bytes();
+    cfg.dynamicSmemBytes = p.sparse ? smem_bytes<false>() : smem_bytes<true>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel, maps, p);
+    if (p.sparse) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<false>, maps, p);
+    return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true>, maps, p);
 }
 
 }  // namespace mla

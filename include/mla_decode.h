@@ -64,7 +64,8 @@ typedef enum {
     MLA_OK = 0,
     MLA_EINVAL = -1,        /* null pointer, bad shape, size or plan */
     MLA_EUNSUPPORTED = -2,  /* shape the kernels do not implement (d_c != 512, d_r != 64, H,
-                               or a cache of 2^31 rows or more for the tcgen05 kernel) */
+                               or a dense cache of 2^31 rows or more: TMA row coordinates
+                               are 32-bit) */
     MLA_ESCRATCH = -3,      /* scratch missing, misaligned or smaller than plan->scratch_bytes */
     MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 */
     MLA_ECUDA = -5,         /* the CUDA runtime reported an error for a launch or query */
@@ -85,7 +86,7 @@ typedef struct {
     float scale;          /* softmax scale, finite and > 0 (1/sqrt(576) for these shapes) */
     int num_sms;          /* SMs to plan for; 0 = query the current device */
     int splits_override;  /* 0 = derive; 1..MLA_MAX_SPLITS = force this split count */
-    int variant;          /* 1 = warp-MMA (mma.sync) kernel, 32-row stages, 16 heads per CTA;
+    int variant;          /* 1 = warp-MMA (mma.sync) kernel, 64-row steps, 16 heads per CTA;
                              2 = tcgen05/TMEM kernel, 80-row TMA tiles, 16 heads per CTA;
                              3 = tcgen05/TMEM kernel, 64-row tiles, 32 heads per CTA (dense,
                                  heads a multiple of 32);
@@ -145,7 +146,8 @@ MLA_API int mla_decode_abi_version(void);
  * grid of min(items, num_sms) CTAs (one per SM) that walk the
  * B * n_head_groups * S work items round-robin; S is the split count that
  * minimises the modelled time ceil(items / grid) * (tiles per slice + 1),
- * a tile being the kernel's row step (80 rows for tcgen05, 32 for warp-MMA)
+ * a tile being the kernel's row step (80 or 64 rows for tcgen05; for warp-MMA
+ * its 32-row slot, two of which make one 64-row step)
  * and the +1 the item's partial write, the smallest such S on ties; slices
  * are whole multiples of 16 (tcgen05) or 32 (warp-MMA) rows and
  * S <= MLA_MAX_SPLITS.  With num_sms == 0 it queries the

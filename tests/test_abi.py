@@ -47,7 +47,7 @@ def _plan(**kw):
     return mla.plan(**base)
 
 
-TILE = {1: 32, 2: 80, 3: 64}     # rows per kernel step: warp-MMA stage, tcgen05 tiles (16 / 32 heads)
+TILE = {1: 32, 2: 80, 3: 64}     # rows per modelled step: warp-MMA slot, tcgen05 tiles (16 / 32 heads)
 GRANULE = {1: 32, 2: 16, 3: 16}  # slices are whole multiples of this
 HEADS = {1: 16, 2: 16, 3: 32}    # heads per CTA
 

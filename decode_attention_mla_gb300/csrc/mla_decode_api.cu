@@ -305,28 +305,22 @@ long long derive_splits(long long rows, long long pairs, long long grid_cap, int
 }
 
 // Kernel choice when the caller leaves it open, from measurements on GB300:
-// the sparse gather moves more rows per SM with the warp-MMA kernel's
-// per-row bulk copies (the tcgen05 kernel's 16-byte gather is bound by the
-// requests an SM keeps in flight); dense decode with 64 or more heads runs
-// fastest on the tcgen05 kernel with 32 heads per CTA (half the MMA
-// instructions and cache-row re-reads per head), and so does 32-head decode
-// with long slices (>= 256 rows per item); other dense shapes take the
-// 16-head tcgen05 kernel for long slices (>= 320 rows per item) and the
-// 32-row warp-MMA kernel for short ones (latency chains it finishes sooner).
-constexpr long long kTc32MinRowsPerItem = 256;
-constexpr long long kTcMinRowsPerItem = 320;
+// the warp-MMA kernel wins every sparse shape (per-row bulk copies gather
+// more rows per SM than the tcgen05 kernel's 16-byte cp.async) and every
+// dense shape with 16 heads (T = 256 .. 131072).  With 32 or more heads it
+// reads each cache row once per 16-head group, so once its slices grow past
+// 512 rows per item the tcgen05 kernel with 32 heads per CTA (one read per
+// 32 heads) is faster; below that the warp-MMA kernel's shorter chain wins.
+constexpr long long kMmaMaxRowsPerItemWide = 512;
 long long rows_per_item(long long rows, int batch, int heads, long long grid_cap, int variant) {
     const long long pairs = static_cast<long long>(batch) * (heads / variant_head_group(variant));
     const long long S = derive_splits(rows, pairs, grid_cap, variant);
     return mla::slice_entries(rows, static_cast<int>(S), variant_granule(variant));
 }
 int auto_variant(bool sparse, int batch, int heads, long long rows, long long grid_cap) {
-    if (sparse) return kVariantWarpMma;
-    if (heads >= 64) return kVariantTc32;
-    if (heads == 32 && rows_per_item(rows, batch, heads, grid_cap, kVariantTc32) >= kTc32MinRowsPerItem)
-        return kVariantTc32;
-    return rows_per_item(rows, batch, heads, grid_cap, kVariantTc) >= kTcMinRowsPerItem ? kVariantTc
-                                                                                        : kVariantWarpMma;
+    if (sparse || heads == mla::kHeadGroup) return kVariantWarpMma;
+    return rows_per_item(rows, batch, heads, grid_cap, kVariantWarpMma) <= kMmaMaxRowsPerItemWide ? kVariantWarpMma
+                                                                                                 : kVariantTc32;
 }
 
 }  // namespace

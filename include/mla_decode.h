@@ -90,9 +90,8 @@ typedef struct {
                              2 = tcgen05/TMEM kernel, 80-row TMA tiles, 16 heads per CTA;
                              3 = tcgen05/TMEM kernel, 64-row tiles, 32 heads per CTA (dense,
                                  heads a multiple of 32);
-                             0 = auto (measured crossovers): sparse -> 1; dense H >= 64 -> 3;
-                                 H = 32 -> 3 when its slices hold >= 256 rows; otherwise 2
-                                 when its slices hold >= 320 rows, else 1 */
+                             0 = auto (measured crossovers): sparse or H = 16 -> 1; dense
+                                 H >= 32 -> 1 while its slices hold <= 512 rows, else 3 */
     int pdl;              /* 1 = launch with programmatic dependent launch */
     int stall_test;       /* test hook, 0 in normal use.  1 = one thread of the partial kernel
                              waits (about 1 ms) on a barrier nothing arrives at, so the timeout

@@ -21,7 +21,8 @@ VARIANTS = [1, 2]      # warp-MMA kernel, tcgen05 kernel
 GRANULE = {1: 32, 2: 16}
 
 
-def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, plan=None, max_ctx=None, variant=0):
+def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, plan=None, max_ctx=None, variant=0,
+              kv_dev=None):
     """Dense decode of workloads.DenseInputs on the GPU; returns (out, lse, plan, scratch)."""
     d = dev()
     B, H, _ = x.q.shape
@@ -33,7 +34,8 @@ def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, pl
         scratch = mla.alloc_scratch(plan)
     out = torch.full((B, H, 512), float("nan"), device=d)
     lse = torch.full((B, H), float("nan"), device=d)
-    mla.forward(plan, x.q.to(d), x.kv.to(d), out, lse, scratch, d_pos=x.d_pos.to(d),
+    kv = kv_dev if kv_dev is not None else x.kv.to(d)
+    mla.forward(plan, x.q.to(d), kv, out, lse, scratch, d_pos=x.d_pos.to(d),
                 row_offset=x.row_offset.to(d) if B > 1 else None)
     torch.cuda.synchronize()
     return out, lse, plan, scratch

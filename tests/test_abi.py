@@ -73,7 +73,10 @@ def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     (dict(sparse=True, topk=2048), 1, 64, 32),
     (dict(batch=64, sparse=True, topk=2048), 1, 2, 1024),
     (dict(heads=128, max_ctx=32768 + 64), 3, 37, 896),
-    (dict(max_ctx=131072), 2, 149, 880),
+    (dict(max_ctx=131072), 1, 152, 864),
+    (dict(max_ctx=131072, variant=2), 2, 149, 880),
+    (dict(heads=32, max_ctx=32768), 1, 74, 448),
+    (dict(heads=32, max_ctx=131072), 3, 147, 896),
     (dict(max_ctx=8192, variant=2), 2, 103, 80),
     (dict(sparse=True, topk=2048, variant=2), 2, 26, 80),
     (dict(batch=64, sparse=True, topk=2048, variant=2), 2, 2, 1024),
@@ -122,19 +125,15 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
 
 
 def _model_auto(sparse, rows, batch, heads, sms):
-    """The automatic kernel choice, restated: sparse -> warp-MMA; H >= 64 ->
-    32 heads per CTA; H = 32 -> that too when its slices hold >= 256 rows;
-    otherwise the 16-head tcgen05 kernel when its slices hold >= 320 rows."""
+    """The automatic kernel choice, restated: sparse or 16 heads -> warp-MMA;
+    more heads -> warp-MMA while its slices hold <= 512 rows, else 32 heads
+    per CTA on tcgen05."""
     def per(v):
         S = _model_split(rows, batch * heads // HEADS[v], sms, v)
         return -(-(-(-rows // S)) // GRANULE[v]) * GRANULE[v]
-    if sparse:
+    if sparse or heads == 16:
         return 1
-    if heads >= 64:
-        return 3
-    if heads == 32 and per(3) >= 256:
-        return 3
-    return 2 if per(2) >= 320 else 1
+    return 1 if per(1) <= 512 else 3
 
 
 @pytest.mark.parametrize("rows", [1, 100, 256, 8192, 20000, 32768, 65536, 131072])

@@ -101,3 +101,14 @@ def test_heads32_uniform_scores_closed_form():
     mean = x.kv[:, :512].double().mean(0).numpy()
     assert np.abs(out.double().cpu().numpy() - mean[None, None]).max() <= _gpu.OUT_ATOL
     assert np.abs(lse.double().cpu().numpy() - np.log(T)).max() <= _gpu.LSE_RTOL * np.log(T)
+
+
+@pytest.mark.parametrize("T", [37, 1000, 4097])
+def test_heads32_rows_past_the_context_may_hold_nan(T):
+    x = workloads.dense(1, 32, T, seed=95 + T)
+    d = _gpu.dev()
+    kv = torch.full((T + 300, 576), float("nan"), dtype=torch.bfloat16)
+    kv[:T] = x.kv
+    out, lse, plan, _ = _gpu.run_dense(x, max_ctx=T + 300, variant=V32, kv_dev=kv.to(d))
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"NaN past the context, 32 heads per CTA, T={T}")

@@ -299,3 +299,40 @@ def test_tcgen05_rescale_path():
     for variant in _gpu.VARIANTS:
         out, lse, plan, _ = _gpu.run_dense(x, splits=1, variant=variant)
         _gpu.assert_parity(out, lse, ro, rl, f"growing scores, variant {variant}")
+
+
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("T,splits", [(37, 0), (100, 3), (1000, 0), (1000, 7), (4097, 0)])
+def test_dense_rows_past_the_context_may_hold_nan(T, splits, variant):
+    """A cache allocated for max_ctx rows holds anything past the context
+    (here NaN): the attended rows alone decide the result, including the rows
+    a kernel loads past a slice's end inside its last tile."""
+    x = workloads.dense(1, 16, T, seed=90 + T)
+    d = _gpu.dev()
+    cap = T + 300
+    kv = torch.full((cap, 576), float("nan"), dtype=torch.bfloat16)
+    kv[:T] = x.kv
+    out, lse, plan, _ = _gpu.run_dense(x, splits=splits, max_ctx=cap, variant=variant, kv_dev=kv.to(d))
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"NaN past the context, T={T} S={plan.splits}")
+
+
+@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("topk", [17, 81, 300])
+def test_sparse_unlisted_rows_may_hold_nan(topk, variant):
+    """Rows no list names (and the rows masked ids would point at) hold NaN:
+    only the listed rows may reach the result."""
+    x = workloads.sparse(2, 16, [5000, 300], topk, seed=200 + topk)
+    idx = x.indices.clone()
+    idx[0, 0] = -1
+    idx[1, topk - 1] = 300           # == cache_len: masked
+    x.indices = idx
+    kv = torch.full_like(x.kv, float("nan"))
+    for b in range(2):
+        ids = x.indices[b]
+        ok = (ids >= 0) & (ids < x.cache_len[b])
+        rows = x.row_offset[b] + ids[ok].long()
+        kv[rows] = x.kv[rows]
+    out, lse, plan, _ = _gpu.run_sparse(x, splits=3, variant=variant, kv_dev=kv.to(_gpu.dev()))
+    ro, rl = _gpu.oracle_sparse(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"sparse k={topk}, NaN outside the lists")

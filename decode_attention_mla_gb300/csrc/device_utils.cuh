@@ -157,6 +157,12 @@ __device__ __forceinline__ void warpgroup_regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Bring the line holding p into L2 (and its translation into the TLBs); a
+// hint only, safe on memory another kernel is still writing.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Relaxed (atomic, unordered) loads: for values another kernel may be writing
 // at the same time, read only as a hint (e.g. to aim an L2 prefetch).
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {

@@ -40,8 +40,6 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     __shared__ float red_max[kWarps];
     __shared__ float red_sum[kWarps];
     __shared__ float4 part[kWarps][32];
-    grid_dependency_wait();          // the partials come from the preceding kernel
-    allow_dependent_launch();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // W = warps per (request, head): 1, 2, 4 or 8
@@ -51,6 +49,16 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     const bool live = bh < rows;
     const int chunk = blockIdx.y;
     const int S = p.splits;
+    // while the partial kernel finishes: the lines (and address translations)
+    // this thread reads first
+    if (live) {
+        if (threadIdx.x % 32 == 0) prefetch_l2(p.lse_part + static_cast<long long>(bh) * S);
+        const int s = (S + W - 1) / W * wl;
+        if (s < S)
+            prefetch_l2(p.o_part + (static_cast<long long>(bh) * S + s) * kDLatent + chunk * kCombineChunk + 4 * lane);
+    }
+    grid_dependency_wait();          // the partials come from the preceding kernel
+    allow_dependent_launch();
     // Every slice holds a partial (the partial kernels write lse = -inf, o = 0
     // for slices without entries), so nothing here depends on the context length.
     const int tu = wl * 32 + lane;                     // thread within the unit: 32 * W >= S
@@ -166,11 +174,28 @@ int combine_grid_rows(int rows, int splits) {
     return (rows + per_cta - 1) / per_cta;
 }
 
-cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream) {
+// Shared memory reserved (unused) by each combine CTA of a grid no larger than
+// the GPU, so that no two share an SM: launched early (programmatic dependent
+// launch) while the partial kernel holds most SMs, the CTAs would otherwise
+// pile onto the few idle ones and load the partials through a fraction of
+// the GPU.  Larger grids run in waves anyway and are launched without it.
+constexpr int kSpreadSmemBytes = 120 * 1024;
+
+cudaError_t combine_prepare() {
+    for (auto fn : {mla_combine_kernel<1>, mla_combine_kernel<2>, mla_combine_kernel<4>, mla_combine_kernel<8>}) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, bool spread,
+                           cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(block, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = spread ? kSpreadSmemBytes : 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -109,7 +109,8 @@ int prepare_device(int dev) {
     if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
     std::lock_guard<std::mutex> lock(g_prepare_mutex);
     if (g_prepared[dev].load(std::memory_order_acquire)) return MLA_OK;
-    if (mla::partial_mma_prepare(dev) != cudaSuccess || mla::partial_tc_prepare(dev) != cudaSuccess) {
+    if (mla::partial_mma_prepare(dev) != cudaSuccess || mla::partial_tc_prepare(dev) != cudaSuccess ||
+        mla::combine_prepare() != cudaSuccess) {
         cudaGetLastError();
         return MLA_ECUDA;
     }
@@ -276,8 +277,9 @@ int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void
     c.row_offset = a->row_offset;
     c.kv_rows = a->kv_rows;
     c.granule = variant_granule(pl->variant);
+    const bool spread = static_cast<long long>(pl->combine_grid_x) * pl->combine_grid_y <= pl->num_sms;
     return launch_status(mla::launch_combine(c, dim3(pl->combine_grid_x, pl->combine_grid_y, 1), pl->combine_block,
-                                             pl->shape.pdl != 0, static_cast<cudaStream_t>(stream)));
+                                             pl->shape.pdl != 0, spread, static_cast<cudaStream_t>(stream)));
 }
 
 // Split count derived from the shape ("Launch Geometry", Lecture 04, s.4:

@@ -95,7 +95,10 @@ cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int he
                               cudaStream_t stream);
 int combine_block_threads();
 int combine_grid_rows(int rows, int splits);    // combine grid x for B*H rows
-cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, cudaStream_t stream);
+cudaError_t combine_prepare();
+// spread: one CTA per SM (for grids no larger than the SM count)
+cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, bool spread,
+                           cudaStream_t stream);
 
 // Static scratch (mla_static_scratch.cu): its address on `device` once set up
 // there (nullptr before), and the one-time set-up with `device` current.

@@ -151,7 +151,24 @@ struct Item {
     uint32_t e0, e1;                       // entries [e0, e1) of the request
 };
 
-__device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
+// The request fields an item's slice depends on (dense: d_pos[b] and the
+// segment's first row), read ahead of their use by the caller.
+struct RequestRead {
+    int d_pos;
+    long long base;
+};
+__device__ __forceinline__ RequestRead read_request(const PartialParams& p, int b) {
+    RequestRead r;
+    r.d_pos = p.sparse ? 0 : p.d_pos[b];
+    r.base = p.row_offset ? p.row_offset[b] : 0;
+    return r;
+}
+__device__ __forceinline__ int request_of(const PartialParams& p, int item) {
+    return static_cast<int>(static_cast<uint32_t>(item) / static_cast<uint32_t>(p.n_groups) /
+                            static_cast<uint32_t>(p.splits));
+}
+
+__device__ __forceinline__ Item decode_item(const PartialParams& p, int item, const RequestRead* pre = nullptr) {
     Item it;
     const uint32_t ui = static_cast<uint32_t>(item);
     const uint32_t rest = ui / static_cast<uint32_t>(p.n_groups);
@@ -162,8 +179,20 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item) {
     // entry counts are below 2^31 (d_pos and the list length are int32), so
     // the slice arithmetic runs in 32 bits (64-bit division is slow); dense
     // entries are already clamped to the rows that exist in the cache
-    const uint32_t n = static_cast<uint32_t>(
-        request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
+    uint32_t n;
+    if (pre) {
+        // the same count as request_entries, from values read earlier
+        it.base = pre->base;
+        long long m = p.sparse ? p.topk : static_cast<long long>(pre->d_pos) + 1;
+        if (!p.sparse) {
+            const long long cap = p.kv_rows - it.base;
+            if (m > cap) m = cap;
+            if (m < 0) m = 0;
+        }
+        n = static_cast<uint32_t>(m);
+    } else {
+        n = static_cast<uint32_t>(request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
+    }
     const uint32_t per = slice_entries_u32(n, static_cast<uint32_t>(p.splits), kStageRows);
     uint32_t e0 = static_cast<uint32_t>(it.s) * per;
     uint32_t e1 = e0 + per;
@@ -194,6 +223,29 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 }
 
 // ============================== producer ==================================
+// While the preceding kernel still runs: the first item's query tile, its
+// request fields and the first row of its partial output into L2 (with their
+// address translations).  Hints only: everything is read again after the
+// grid dependency.
+__device__ void prefetch_first_inputs(const TcMaps& maps, const PartialParams& p) {
+    const int item = static_cast<int>(blockIdx.x);
+    if (item >= p.n_items) return;
+    const int rest = item / p.n_groups;
+    const int hg = item - rest * p.n_groups;
+    const int b = rest / p.splits;
+    const int s = rest - b * p.splits;
+    tma_prefetch_3d(&maps.q, 0, b * p.heads + hg * kHeadGroup, 0);
+    if (!p.sparse) prefetch_l2(p.d_pos + b);
+    if (p.row_offset) prefetch_l2(p.row_offset + b);
+    if (p.sparse) {
+        prefetch_l2(p.cache_len + b);
+        prefetch_l2(p.indices + static_cast<long long>(b) * p.topk);
+    }
+    const long long row0 = (static_cast<long long>(b) * p.heads + hg * kHeadGroup) * p.splits + s;
+    prefetch_l2(p.o_part + row0 * kDLatent);
+    prefetch_l2(p.lse_part + row0);
+}
+
 // Dense: while the preceding kernel still runs, bring the first slots of the
 // CTA's first item into L2.  The context length read here may be stale (that
 // kernel may be advancing it): it only aims the prefetch, and every row the
@@ -226,12 +278,15 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     // (a new tile whenever a busy item's key differs) and release a tile
     // through q_empty, read or not
     int q_key = first_key(p);
+    // the first item's request fields are read before the query tile is
+    // requested, so that the two latencies overlap
+    const RequestRead first = read_request(p, blockIdx.x < p.n_items ? request_of(p, blockIdx.x) : 0);
     load_q(maps, p, sh, q_key, lane);
     int q_loads = 1;          // query tiles staged so far
     // test hook: a wait that runs out, so every role takes the abort path
     bool ok = !(p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, item);
+        const Item it = decode_item(p, item, item == static_cast<int>(blockIdx.x) ? &first : nullptr);
         if (it.n_slots == 0) continue;
         const int key = it.b * p.n_groups + it.hg;
         if (key != q_key) {
@@ -646,7 +701,9 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 L1 > 0.f ? (m_ref[1] + lg2_approx(L1)) * kLn2 : -INFINITY;
         }
     }
-    if (w == 0) bulk_wait_all();               // rows written before the CTA retires
+    // the staged rows must have left shared memory before the CTA retires; the
+    // writes themselves are visible to the next kernel once this grid completes
+    if (w == 0) bulk_wait_read_all();
     if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
 }
 
@@ -684,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         if constexpr (kDense) {
             if (warp == kProducerWarp + 1 && lane == 0) prefetch_first_slots(maps, p);
         }
+        if (warp == kProducerWarp + 2 && lane == 0) prefetch_first_inputs(maps, p);
         if (warp == kProducerWarp) {
             grid_dependency_wait();
             allow_dependent_launch();

@@ -564,9 +564,11 @@ def ncu_case(args):
     from decode_attention_mla_gb300 import build as mla_build
     mla_build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    if args.ncu_case.startswith("dense_t"):
-        T = int(args.ncu_case[len("dense_t"):])
-        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
+    if args.ncu_case.startswith("dense_"):
+        # dense_t<T> (16 heads) or dense_h<H>_t<T>
+        fields = dict((f[0], int(f[1:])) for f in args.ncu_case[len("dense_"):].split("_"))
+        T, H = fields["t"], fields.get("h", 16)
+        b = DenseBench(T, H, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
     elif args.ncu_case == "sparse_k2048":
         b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl),
                         variant=args.variant)
@@ -592,7 +594,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--details", default=None)
     ap.add_argument("--ncu-case", default=None,
-                    help="profiling helper: dense_t<T> | sparse_k2048 | sparse_b64: run --calls eager calls of "
+                    help="profiling helper: dense_t<T> | dense_h<H>_t<T> | sparse_k2048 | sparse_b64: run --calls eager calls of "
                          "that workload and exit (no JSON)")
     ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()

@@ -22,19 +22,24 @@
 //                   Direction"); masked entries are zero-filled.  It also
 //                   stages the item's 16 query rows (one TMA box) whenever the
 //                   (request, head group) changes.
-//   8 MMA warps   : consume 64-row steps (two slots).  Scores: warp w takes
-//                   rows 16*(w/2) .. +15 of the step and half of the 576-wide
-//                   contraction (k-steps 4c + 2*(w%2) + {0, 1} of each 64-column
-//                   chunk c, its query fragments held in registers); the two
-//                   halves meet through shared
-//                   memory, each warp finishing one 8-row tile.  Softmax keeps
-//                   one base-2 reference per head for the whole CTA and moves
-//                   it only when a score exceeds it by more than 8 (one
-//                   OR-barrier per step decides); each warp turns its 8 rows
-//                   into P = 2^(s - ref) as a bf16 hi + lo pair (about 16
-//                   significant bits) and publishes them.  P . V: warp w owns
-//                   output features 64w .. 64w+63 for all 16 heads and all 64
-//                   rows of the step.
+//   8 MMA warps   : two groups of four (one warp of each group on every SM
+//                   sub-partition) take alternate 32-row slots of an item, each
+//                   group with its own online softmax, so one group's
+//                   exchanges, barriers and softmax overlap the other's MMAs.
+//                   Scores: in a group, warp pair p takes rows 16p .. +15 of
+//                   the slot and each warp half of the 576-wide contraction
+//                   (k-steps 4c + 2h + {0, 1} of each 64-column chunk c, its
+//                   query fragments held in registers); the halves meet
+//                   through shared memory, each warp finishing one 8-row
+//                   tile.  Softmax keeps one base-2 reference per head for the
+//                   group and moves it only when a score exceeds it by more
+//                   than 8 (one OR-barrier per slot decides); each warp turns
+//                   its 8 rows into P = 2^(s - ref) as a bf16 hi + lo pair
+//                   (about 16 significant bits) and publishes them.  P . V:
+//                   warp w of a group owns output features 128w .. 128w+127
+//                   for all 16 heads and all 32 rows of the slot.  At the end
+//                   of an item group 1 stages its O, reference and row sums in
+//                   its last slot and group 0 merges the two states.
 // No floating-point atomics: the result is a pure function of the inputs and
 // the split count.  Every wait is bounded; a timeout raises MLA_EDEVICE in the
 // status word, every warp leaves through the same barrier, and the CTA drains
@@ -52,8 +57,10 @@ namespace mla {
 namespace {
 
 constexpr int kSlots = 4;                                  // ring depth (32-row slots)
-constexpr int kStepRows = 2 * kStageRows;                  // rows per consumer step (two slots)
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 8;                           // two groups of four MMA warps
+constexpr int kGroups = 2;
+constexpr int kGroupWarps = kComputeWarps / kGroups;       // 4: one per SM sub-partition
+constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kThreads = (kComputeWarps + 4) * 32;         // + a producer warpgroup (one working warp)
 constexpr int kProducerWarp = kComputeWarps;
 // Register split: the CTA is launched with kLaunchRegs per thread; the
@@ -66,9 +73,9 @@ static_assert(128 * kProducerRegs + kComputeWarps * 32 * kMmaRegs <= kThreads * 
 constexpr int kChunks = kDRow / 64;                        // 9 column chunks of 64 bf16
 constexpr int kKSteps = kDRow / 16;                        // 36 k-steps of the score contraction
 constexpr int kKHalf = kKSteps / 2;                        // 18 per warp
-constexpr int kFeatPerWarp = kDLatent / kComputeWarps;     // 64 output features per warp
-constexpr int kPVTiles = kFeatPerWarp / 8;                 // 8 n-tiles of P . V per warp
-constexpr int kStepTiles = kStepRows / 8;                  // 8 score tiles of 8 rows per step
+constexpr int kFeatPerWarp = kDLatent / kGroupWarps;       // 128 output features per warp
+constexpr int kPVTiles = kFeatPerWarp / 8;                 // 16 n-tiles of P . V per warp
+constexpr int kSlotTiles = kStageRows / 8;                 // 4 score tiles of 8 rows per slot
 constexpr int kIdxPrefetch = 4;                            // sparse index prefetch depth (slots)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;                   // log2 units: P stays <= 256
@@ -78,24 +85,30 @@ constexpr int kDenseSlotBytes = kChunks * kDenseChunkBytes;  // 36,864
 constexpr int kSmemRow = kRowBytes + 16;                   // 8 consecutive rows hit 8 distinct 16-byte groups
 constexpr int kSparseSlotBytes = kStageRows * kSmemRow;    // 37,376
 constexpr int kQChunkBytes = kHeadGroup * 128;             // 2048
-// named barriers: 0 is __syncthreads, 1..4 the four warp pairs, 5 the MMA warps
+constexpr int kStagePitch = kDLatent + 4;                  // floats per staged row of group 1's O (2064 B)
+// named barriers: 0 is __syncthreads, 1..4 the warp pairs (two per group),
+// 5 and 6 the groups, 7 all MMA warps
 constexpr int kBarPair0 = 1;
-constexpr int kBarMma = 5;
+constexpr int kBarGroup0 = 5;
+constexpr int kBarMma = 7;
 constexpr int kMmaThreads = kComputeWarps * 32;
 
 static_assert(kDenseSlotBytes % 1024 == 0, "swizzled slots stay 1024-byte aligned");
-static_assert(kKHalf == 2 * kChunks && kComputeWarps == 2 * (kStepRows / 16),
-              "warp w: rows 16*(w/2), two k-steps of every chunk (half w%2)");
+static_assert(kKHalf == 2 * kChunks && kGroupWarps == 2 * (kStageRows / 16),
+              "a group's warp pairs cover a slot 16 rows each, a contraction half per warp");
+static_assert(kHeadGroup * kStagePitch * 4 <= kDenseSlotBytes, "group 1's O fits in one slot");
 
 template <bool kDense>
 struct __align__(1024) SharedStorage {
     static constexpr int kSlotBytes = kDense ? kDenseSlotBytes : kSparseSlotBytes;
     uint8_t q[kChunks * kQChunkBytes];                     // the item's 16 query rows (1024-byte aligned)
     uint8_t kv[kSlots][kSlotBytes];                        // ring of 32-row slots
-    uint4 p[2][kStepTiles][32];                            // P of a step as mma A fragments, double-buffered
-    float4 red[kComputeWarps / 2][2][32];                  // half-contraction scores exchanged in each pair
-    float mx[kComputeWarps][kHeadGroup];                   // per-warp head maxima (reference moves)
-    float lsum[kComputeWarps][kHeadGroup];                 // per-warp row sums (epilogue)
+    uint4 p[kGroups][2][kSlotTiles][32];                   // P of a group's slot as mma A fragments, double-buffered
+    float4 red[kGroups][2][2][32];                         // half-contraction scores exchanged in each pair
+    float mx[kGroups][kGroupWarps][kHeadGroup];            // per-warp head maxima (reference moves)
+    float lsum[kGroups][kGroupWarps][kHeadGroup];          // per-warp row sums (epilogue)
+    float merge_m[kHeadGroup];                             // group 1's reference and row sum, for the merge
+    float merge_l[kHeadGroup];
     int valid[kSlots][kStageRows];                         // sparse: row holds an attended entry
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
@@ -113,7 +126,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int b, int chunk_bytes) {
 // Lane offsets of the ldmatrix rows inside a slot.  Score operand: row r of
 // the slot (0..31), k-step 4c + 2*kh + j of chunk c; the part that varies with
 // c is added as a constant (c * chunk stride).  P . V operand: row r, features
-// 64w + 16i + 8*hi .. +7 of chunk w.
+// 128gw + 16i + 8*hi .. +7 (chunk 2gw + i/4).
 template <bool kDense>
 __device__ __forceinline__ uint32_t qk_lane_off(int r, int kh, int j, int lmat) {
     if constexpr (kDense)
@@ -126,11 +139,12 @@ __device__ __forceinline__ uint32_t qk_chunk_stride() {
     return kDense ? kDenseChunkBytes : 128;
 }
 template <bool kDense>
-__device__ __forceinline__ uint32_t pv_lane_off(int r, int w, int i, int hi) {
+__device__ __forceinline__ uint32_t pv_lane_off(int r, int gw, int i, int hi) {
     if constexpr (kDense)
-        return static_cast<uint32_t>(w * kDenseChunkBytes + r * 128 + (((2 * i + hi) ^ (r & 7)) << 4));
+        return static_cast<uint32_t>((2 * gw + (i >> 2)) * kDenseChunkBytes + r * 128 +
+                                     (((2 * (i & 3) + hi) ^ (r & 7)) << 4));
     else
-        return static_cast<uint32_t>(r * kSmemRow + w * 128 + (2 * i + hi) * 16);
+        return static_cast<uint32_t>(r * kSmemRow + gw * 256 + (2 * i + hi) * 16);
 }
 template <bool kDense>
 __host__ __device__ constexpr uint32_t row_pitch() {
@@ -376,16 +390,55 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
 }
 
 // ============================== MMA warps =================================
+// Two groups of four warps (one warp of each on every SM sub-partition) take
+// alternate 32-row slots of an item: group 0 slots 0, 2, 4, ..., group 1
+// slots 1, 3, 5, ...  Each group runs its own online softmax (its own
+// reference, row sums and O), so one group's exchanges, barriers and softmax
+// overlap the other group's MMAs; the two partials meet once per item, in
+// shared memory, before the normalised partial is stored.
+//
 // Bounded wait whose answer is the same on every lane of the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag));
 }
 __device__ __forceinline__ float4 as_float4(const float (&v)[4]) { return make_float4(v[0], v[1], v[2], v[3]); }
 
-// One k-step (16 rows) of O += P . V for this warp's 64 features: P as the
-// A fragments of the published hi / lo pairs, V by transposing ldmatrix;
-// all eight low-part MMAs first, then the high parts (each accumulator's two
-// MMAs eight instructions apart).
+// This warp's half of the score contraction for its pair's 16 rows of a slot
+// (two 8-row tiles), in two accumulation chains per tile (even / odd k-steps)
+// added once; zeros when `run` is false.
+template <bool kDense>
+__device__ __forceinline__ void qk_scores(float (&acc)[2][4], const uint32_t (&qa)[kKHalf][4], uint32_t sbase,
+                                          const uint32_t (&qk_off)[2], bool run) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    if (!run) return;
+    float acc2[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) acc2[j][0] = acc2[j][1] = acc2[j][2] = acc2[j][3] = 0.f;
+    const uint32_t a0 = sbase + qk_off[0];
+    const uint32_t a1 = sbase + qk_off[1];
+#pragma unroll
+    for (int kk = 0; kk < kKHalf; ++kk) {
+        uint32_t bf[4];
+        ldmatrix_x4(bf, ((kk & 1) ? a1 : a0) + (kk >> 1) * qk_chunk_stride<kDense>());
+        if (kk & 1) {
+            mma_bf16_16816(acc2[0], qa[kk], bf[0], bf[1]);
+            mma_bf16_16816(acc2[1], qa[kk], bf[2], bf[3]);
+        } else {
+            mma_bf16_16816(acc[0], qa[kk], bf[0], bf[1]);
+            mma_bf16_16816(acc[1], qa[kk], bf[2], bf[3]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][c] += acc2[j][c];
+}
+
+// One k-step (16 rows of a slot) of O += P . V for this warp's 128 features:
+// P as the A fragments of the group's published hi / lo pairs, V by
+// transposing ldmatrix, in two halves of eight n-tiles (low-part MMAs first,
+// then the high parts: each accumulator's two MMAs eight instructions apart).
 template <bool kDense>
 __device__ __forceinline__ void pv_kstep(float (&o)[kPVTiles][4], const uint4* pt, int kp, uint32_t vbase,
                                          const uint32_t (&pv_off)[kPVTiles / 2], int v_hi, int tq, int lane) {
@@ -393,32 +446,35 @@ __device__ __forceinline__ void pv_kstep(float (&o)[kPVTiles][4], const uint4* p
     const uint4 t1 = pt[(2 * kp + 1) * 32 + lane];
     const uint32_t a_hi[4] = {t0.x, t0.y, t1.x, t1.y};
     const uint32_t a_lo[4] = {t0.z, t0.w, t1.z, t1.w};
-    uint32_t v[kPVTiles / 2][4];
-#pragma unroll
-    for (int i = 0; i < kPVTiles / 2; ++i) ldmatrix_x4_trans(v[i], vbase + pv_off[i]);
     // dense rows past the slice may hold anything (even NaN): zero their V so
     // that p = 0 really contributes nothing
+    uint32_t m_lo = 0xffffffffu, m_hi = 0xffffffffu;
     if (kDense && v_hi < 16 * (kp + 1)) {
         const int k0 = 16 * kp + 2 * tq;
-        const uint32_t m_lo = (k0 < v_hi ? 0x0000ffffu : 0u) | (k0 + 1 < v_hi ? 0xffff0000u : 0u);
-        const uint32_t m_hi = (k0 + 8 < v_hi ? 0x0000ffffu : 0u) | (k0 + 9 < v_hi ? 0xffff0000u : 0u);
+        m_lo = (k0 < v_hi ? 0x0000ffffu : 0u) | (k0 + 1 < v_hi ? 0xffff0000u : 0u);
+        m_hi = (k0 + 8 < v_hi ? 0x0000ffffu : 0u) | (k0 + 9 < v_hi ? 0xffff0000u : 0u);
+    }
 #pragma unroll
-        for (int i = 0; i < kPVTiles / 2; ++i) {
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ldmatrix_x4_trans(v[i], vbase + pv_off[4 * hh + i]);
             v[i][0] &= m_lo;
             v[i][1] &= m_hi;
             v[i][2] &= m_lo;
             v[i][3] &= m_hi;
         }
-    }
 #pragma unroll
-    for (int i = 0; i < kPVTiles / 2; ++i) {
-        mma_bf16_16816(o[2 * i], a_lo, v[i][0], v[i][1]);
-        mma_bf16_16816(o[2 * i + 1], a_lo, v[i][2], v[i][3]);
-    }
+        for (int i = 0; i < 4; ++i) {
+            mma_bf16_16816(o[8 * hh + 2 * i], a_lo, v[i][0], v[i][1]);
+            mma_bf16_16816(o[8 * hh + 2 * i + 1], a_lo, v[i][2], v[i][3]);
+        }
 #pragma unroll
-    for (int i = 0; i < kPVTiles / 2; ++i) {
-        mma_bf16_16816(o[2 * i], a_hi, v[i][0], v[i][1]);
-        mma_bf16_16816(o[2 * i + 1], a_hi, v[i][2], v[i][3]);
+        for (int i = 0; i < 4; ++i) {
+            mma_bf16_16816(o[8 * hh + 2 * i], a_hi, v[i][0], v[i][1]);
+            mma_bf16_16816(o[8 * hh + 2 * i + 1], a_hi, v[i][2], v[i][3]);
+        }
     }
 }
 
@@ -427,32 +483,36 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
     constexpr uint32_t kSlotBytes = SharedStorage<kDense>::kSlotBytes;
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int pr = w >> 1;                  // warp pair: rows 16*pr .. +15 of a step
-    const int kh = w & 1;                   // contraction half, and the pair's 8-row tile this warp finishes
-    const int my_tile = 2 * pr + kh;        // score tile of 8 rows (step rows 8*my_tile ..)
-    const int r_own = 8 * my_tile + 2 * tq; // step rows of this lane's scores: r_own, r_own + 1
-    const int f_base = w * kFeatPerWarp;    // own output features
+    const int grp = w / kGroupWarps;        // group: the item's slots grp, grp + 2, ...
+    const int gw = w % kGroupWarps;         // warp within the group
+    const int pr = gw >> 1;                 // warp pair: rows 16*pr .. +15 of a slot
+    const int kh = gw & 1;                  // contraction half, and the pair's 8-row tile this warp finishes
+    const int my_tile = 2 * pr + kh;        // score tile of 8 rows (slot rows 8*my_tile ..)
+    const int r_own = 8 * my_tile + 2 * tq; // slot rows of this lane's scores: r_own, r_own + 1
+    const int f_base = gw * kFeatPerWarp;   // own output features
     const int lrow = lane & 7;
     const int lmat = lane >> 3;
+    const int bar_pair = kBarPair0 + 2 * grp + pr;
+    const int bar_group = kBarGroup0 + grp;
     const uint32_t q_base = smem_u32(sh.q);
     const uint32_t kv_base = smem_u32(sh.kv[0]);
-    // ldmatrix lane offsets: score rows 16*(pr%2) + lrow + 8*(lmat/2) of the
-    // pair's slot; P . V rows lrow + 8*(lmat%2) (+16 for odd k-steps)
-    const int qk_row = 16 * (pr & 1) + lrow + ((lmat >> 1) << 3);
+    // ldmatrix lane offsets: score rows 16*pr + lrow + 8*(lmat/2) of the slot;
+    // P . V rows lrow + 8*(lmat%2) (+16 for the second k-step)
+    const int qk_row = 16 * pr + lrow + ((lmat >> 1) << 3);
     const uint32_t qk_off[2] = {qk_lane_off<kDense>(qk_row, kh, 0, lmat), qk_lane_off<kDense>(qk_row, kh, 1, lmat)};
     const int pv_row = lrow + ((lmat & 1) << 3);
     uint32_t pv_off[kPVTiles / 2];
 #pragma unroll
-    for (int i = 0; i < kPVTiles / 2; ++i) pv_off[i] = pv_lane_off<kDense>(pv_row, w, i, lmat >> 1);
+    for (int i = 0; i < kPVTiles / 2; ++i) pv_off[i] = pv_lane_off<kDense>(pv_row, gw, i, lmat >> 1);
 
     uint32_t qa[kKHalf][4];                 // query fragments of this warp's contraction half
-    int stage = 0;                          // slots consumed so far (ring position)
-    int pbuf = 0;                           // P buffer of the next step
+    int stage = 0;                          // slots of earlier items (ring position of this item's slot 0)
+    int pbuf = 0;                           // this group's P buffer for its next slot
     int q_phase = 0;                        // query tiles consumed (q_full phases)
     int q_key = first_key(p);               // key of the tile the producer loaded last
     bool q_in_regs = false;                 // that tile is in registers (and released)
     bool failed = false;                    // a wait of this warp ran out
-    bool stop = false;                      // every warp saw a failure at the same barrier: leave
+    bool stop = false;                      // every MMA warp saw a failure at the same barrier: leave
 
     for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
         const Item it = decode_item(p, item);
@@ -495,82 +555,52 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
         float o[kPVTiles][4];
 #pragma unroll
         for (int i = 0; i < kPVTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_ref[2] = {-INFINITY, -INFINITY};   // heads g, g+8: base-2 reference shared by the CTA
+        float m_ref[2] = {-INFINITY, -INFINITY};   // heads g, g+8: base-2 reference shared by the group
         float l_own[2] = {0.f, 0.f};               // sums of 2^(s - ref) over this lane's rows
-        const int n_steps = (it.n_slots + 1) >> 1;
-        for (int step = 0; step < n_steps; ++step) {
-            const int halves = min(2, it.n_slots - 2 * step);
-            const int slot_a = stage % kSlots;
-            const int slot_b = (stage + 1) % kSlots;
-            if (!failed && !warp_wait(&sh.full[slot_a], (stage / kSlots) & 1, &sh.abort_flag)) failed = true;
-            if (!failed && halves == 2 && !warp_wait(&sh.full[slot_b], ((stage + 1) / kSlots) & 1, &sh.abort_flag))
-                failed = true;
-            // step rows [v_lo, v_hi) are attended (dense); sparse rows carry flags
-            const uint32_t e_step = it.e0 + static_cast<uint32_t>(step * kStepRows);
-            const int v_hi = static_cast<int>(min(it.e1 - e_step, static_cast<uint32_t>(kStepRows)));
-            const long long first_row = it.base + e_step;
-            const int v_lo = first_row >= 0 ? 0 : first_row <= -kStepRows ? kStepRows : static_cast<int>(-first_row);
-            const bool active = (pr >> 1) < halves;     // this pair's rows are in a loaded slot
-            const int my_slot = (pr >> 1) ? slot_b : slot_a;
+        const int my_slots = it.n_slots > grp ? (it.n_slots - grp + 1) / 2 : 0;
+        bool gstop = false;                        // the group saw a failure at one of its barriers
+        for (int k = 0; k < my_slots && !gstop; ++k) {
+            const int j = grp + 2 * k;                      // slot of the item
+            const int st = stage + j;                       // its ring position
+            const int slot = st % kSlots;
+            if (!failed && !warp_wait(&sh.full[slot], (st / kSlots) & 1, &sh.abort_flag)) failed = true;
+            // slot rows [v_lo, v_hi) are attended (dense); sparse rows carry flags
+            const uint32_t e_slot = it.e0 + static_cast<uint32_t>(j * kStageRows);
+            const int v_hi = static_cast<int>(min(it.e1 - e_slot, static_cast<uint32_t>(kStageRows)));
+            const long long first_row = it.base + e_slot;
+            const int v_lo =
+                first_row >= 0 ? 0 : first_row <= -kStageRows ? kStageRows : static_cast<int>(-first_row);
+            const uint32_t sbase = kv_base + static_cast<uint32_t>(slot) * kSlotBytes;
 
             // ---- scores of this warp's 8-row tile: two contraction halves ------
+            float acc[2][4];
+            qk_scores<kDense>(acc, qa, sbase, qk_off, !failed);
+            sh.red[grp][pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
+            named_barrier_sync(bar_pair, 64);
+            const float4 other = sh.red[grp][pr][kh][lane];
+            const float4 mine = kh ? as_float4(acc[1]) : as_float4(acc[0]);
+            bool v0, v1;
+            if constexpr (kDense) {
+                v0 = r_own >= v_lo && r_own < v_hi;
+                v1 = r_own + 1 >= v_lo && r_own + 1 < v_hi;
+            } else {
+                v0 = sh.valid[slot][r_own] != 0;
+                v1 = sh.valid[slot][r_own + 1] != 0;
+            }
             float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (active) {
-                float acc[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-                if (!failed) {
-                    // two accumulation chains per tile (even / odd k-steps), added once
-                    float acc2[2][4];
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) acc2[j][0] = acc2[j][1] = acc2[j][2] = acc2[j][3] = 0.f;
-                    const uint32_t sbase = kv_base + static_cast<uint32_t>(my_slot) * kSlotBytes;
-                    const uint32_t a0 = sbase + qk_off[0];
-                    const uint32_t a1 = sbase + qk_off[1];
-#pragma unroll
-                    for (int kk = 0; kk < kKHalf; ++kk) {
-                        uint32_t bf[4];
-                        ldmatrix_x4(bf, ((kk & 1) ? a1 : a0) + (kk >> 1) * qk_chunk_stride<kDense>());
-                        if (kk & 1) {
-                            mma_bf16_16816(acc2[0], qa[kk], bf[0], bf[1]);
-                            mma_bf16_16816(acc2[1], qa[kk], bf[2], bf[3]);
-                        } else {
-                            mma_bf16_16816(acc[0], qa[kk], bf[0], bf[1]);
-                            mma_bf16_16816(acc[1], qa[kk], bf[2], bf[3]);
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[j][c] += acc2[j][c];
-                }
-                // hand the other tile's half to the partner, take ours
-                sh.red[pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
-                named_barrier_sync(kBarPair0 + pr, 64);
-                const float4 other = sh.red[pr][kh][lane];
-                const float4 mine = kh ? as_float4(acc[1]) : as_float4(acc[0]);
-                bool v0, v1;
-                if constexpr (kDense) {
-                    v0 = r_own >= v_lo && r_own < v_hi;
-                    v1 = r_own + 1 >= v_lo && r_own + 1 < v_hi;
-                } else {
-                    v0 = sh.valid[my_slot][r_own & (kStageRows - 1)] != 0;
-                    v1 = sh.valid[my_slot][(r_own + 1) & (kStageRows - 1)] != 0;
-                }
-                if (!failed) {
-                    sc[0] = v0 ? (mine.x + other.x) * p.scale_log2 : -INFINITY;
-                    sc[1] = v1 ? (mine.y + other.y) * p.scale_log2 : -INFINITY;
-                    sc[2] = v0 ? (mine.z + other.z) * p.scale_log2 : -INFINITY;
-                    sc[3] = v1 ? (mine.w + other.w) * p.scale_log2 : -INFINITY;
-                }
+            if (!failed) {
+                sc[0] = v0 ? (mine.x + other.x) * p.scale_log2 : -INFINITY;
+                sc[1] = v1 ? (mine.y + other.y) * p.scale_log2 : -INFINITY;
+                sc[2] = v0 ? (mine.z + other.z) * p.scale_log2 : -INFINITY;
+                sc[3] = v1 ? (mine.w + other.w) * p.scale_log2 : -INFINITY;
             }
             float mx0 = fmaxf(sc[0], sc[1]);   // head g over this lane's two rows
             float mx1 = fmaxf(sc[2], sc[3]);   // head g + 8
 
-            // ---- P against the shared reference; move it only when needed ------
+            // ---- P against the group's reference; move it only when needed ----
             float pv[4];
-            bool need = true;                  // the first step of an item sets the reference
-            if (step > 0) {
+            bool need = true;                  // the group's first slot of an item sets the reference
+            if (k > 0) {
                 const float ref0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
                 const float ref1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
                 pv[0] = ex2_approx(sc[0] - ref0);
@@ -580,9 +610,9 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 uint4 pk;
                 split_bf16x2(pv[0], pv[1], pk.x, pk.z);
                 split_bf16x2(pv[2], pv[3], pk.y, pk.w);
-                sh.p[pbuf][my_tile][lane] = pk;
+                sh.p[grp][pbuf][my_tile][lane] = pk;
                 const bool over = mx0 > m_ref[0] + kRescaleThreshold || mx1 > m_ref[1] + kRescaleThreshold;
-                need = named_barrier_or(kBarMma, kMmaThreads, over || failed);
+                need = named_barrier_or(bar_group, kGroupThreads, over || failed);
             }
             if (need) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -590,20 +620,20 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
                 if (tq == 0) {
-                    sh.mx[w][g] = mx0;
-                    sh.mx[w][g + 8] = mx1;
+                    sh.mx[grp][gw][g] = mx0;
+                    sh.mx[grp][gw][g + 8] = mx1;
                 }
-                if (named_barrier_or(kBarMma, kMmaThreads, failed)) {
-                    stop = true;
+                if (named_barrier_or(bar_group, kGroupThreads, failed)) {
+                    gstop = true;
                     break;
                 }
                 float n0 = m_ref[0], n1 = m_ref[1];
 #pragma unroll
-                for (int v = 0; v < kComputeWarps; ++v) {
-                    n0 = fmaxf(n0, sh.mx[v][g]);
-                    n1 = fmaxf(n1, sh.mx[v][g + 8]);
+                for (int v = 0; v < kGroupWarps; ++v) {
+                    n0 = fmaxf(n0, sh.mx[grp][v][g]);
+                    n1 = fmaxf(n1, sh.mx[grp][v][g + 8]);
                 }
-                if (step > 0) {
+                if (k > 0) {
                     // what was accumulated against the old reference, scaled to the new one
                     const float a0 = m_ref[0] == -INFINITY ? 0.f : ex2_approx(m_ref[0] - n0);
                     const float a1 = m_ref[1] == -INFINITY ? 0.f : ex2_approx(m_ref[1] - n1);
@@ -628,70 +658,120 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 uint4 pk;
                 split_bf16x2(pv[0], pv[1], pk.x, pk.z);
                 split_bf16x2(pv[2], pv[3], pk.y, pk.w);
-                sh.p[pbuf][my_tile][lane] = pk;
-                named_barrier_sync(kBarMma, kMmaThreads);
+                sh.p[grp][pbuf][my_tile][lane] = pk;
+                named_barrier_sync(bar_group, kGroupThreads);
             }
             l_own[0] += pv[0] + pv[1];
             l_own[1] += pv[2] + pv[3];
 
-            // ---- O[:, own 64 features] += P . V over the step's rows ------------
-            {
-                const uint4* pt = &sh.p[pbuf][0][0];
-                const uint32_t va = kv_base + static_cast<uint32_t>(slot_a) * kSlotBytes;
-                const uint32_t vb = kv_base + static_cast<uint32_t>(slot_b) * kSlotBytes;
-                const uint32_t kHalfSlot = 16 * row_pitch<kDense>();
-                pv_kstep<kDense>(o, pt, 0, va, pv_off, v_hi, tq, lane);
-                pv_kstep<kDense>(o, pt, 1, va + kHalfSlot, pv_off, v_hi, tq, lane);
-                if (halves == 2) {
-                    pv_kstep<kDense>(o, pt, 2, vb, pv_off, v_hi, tq, lane);
-                    pv_kstep<kDense>(o, pt, 3, vb + kHalfSlot, pv_off, v_hi, tq, lane);
-                }
-            }
+            // ---- O[:, own 128 features] += P . V over the slot's 32 rows --------
+            const uint4* pt = &sh.p[grp][pbuf][0][0];
+            pv_kstep<kDense>(o, pt, 0, sbase, pv_off, v_hi, tq, lane);
+            pv_kstep<kDense>(o, pt, 1, sbase + 16 * row_pitch<kDense>(), pv_off, v_hi, tq, lane);
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sh.empty[slot_a]);
-                if (halves == 2) mbar_arrive(&sh.empty[slot_b]);
-            }
-            stage += halves;
+            // group 1 keeps its last slot of the item: its O is staged there
+            const bool keep = grp == 1 && k + 1 == my_slots;
+            if (lane == 0 && !keep) mbar_arrive(&sh.empty[slot]);
             pbuf ^= 1;
         }
-        if (stop) break;
 
-        // ---- epilogue: row sums (lane, quad, warps in order), normalised partial
-        // (stored from registers: measured faster in back-to-back calls than
-        // staging it in shared memory for bulk copies)
+        // ---- epilogue: every MMA warp learns whether to go on ---------------
         float l0 = l_own[0], l1 = l_own[1];
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
         if (tq == 0) {
-            sh.lsum[w][g] = l0;
-            sh.lsum[w][g + 8] = l1;
+            sh.lsum[grp][gw][g] = l0;
+            sh.lsum[grp][gw][g + 8] = l1;
         }
-        named_barrier_sync(kBarMma, kMmaThreads);
+        if (named_barrier_or(kBarMma, kMmaThreads, failed || gstop)) {
+            stop = true;
+            break;
+        }
+        // the group's row sums (its warps in order)
         float L0 = 0.f, L1 = 0.f;
 #pragma unroll
-        for (int v = 0; v < kComputeWarps; ++v) {
-            L0 += sh.lsum[v][g];
-            L1 += sh.lsum[v][g + 8];
+        for (int v = 0; v < kGroupWarps; ++v) {
+            L0 += sh.lsum[grp][v][g];
+            L1 += sh.lsum[grp][v][g + 8];
         }
-        const float inv0 = L0 > 0.f ? rcp_approx(L0) : 0.f;
-        const float inv1 = L1 > 0.f ? rcp_approx(L1) : 0.f;
         const long long row_h0 = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s;
         float* op0 = p.o_part + (row_h0 + static_cast<long long>(g) * p.splits) * kDLatent + f_base + 2 * tq;
         float* op1 = p.o_part + (row_h0 + static_cast<long long>(g + 8) * p.splits) * kDLatent + f_base + 2 * tq;
+        if (it.n_slots == 1) {
+            // one slot: group 0 alone attended rows
+            if (grp == 0) {
+                const float inv0 = L0 > 0.f ? rcp_approx(L0) : 0.f;
+                const float inv1 = L1 > 0.f ? rcp_approx(L1) : 0.f;
 #pragma unroll
-        for (int nt = 0; nt < kPVTiles; ++nt) {
-            *reinterpret_cast<float2*>(op0 + 8 * nt) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-            *reinterpret_cast<float2*>(op1 + 8 * nt) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+                for (int nt = 0; nt < kPVTiles; ++nt) {
+                    *reinterpret_cast<float2*>(op0 + 8 * nt) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
+                    *reinterpret_cast<float2*>(op1 + 8 * nt) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+                }
+                if (gw == 0 && tq == 0) {
+                    p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
+                        L0 > 0.f ? (m_ref[0] + lg2_approx(L0)) * kLn2 : -INFINITY;
+                    p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
+                        L1 > 0.f ? (m_ref[1] + lg2_approx(L1)) * kLn2 : -INFINITY;
+                }
+            }
+        } else {
+            // group 1 stages O (against its own reference), its reference and
+            // row sums in its last slot of the item; group 0 merges the two
+            // online-softmax states and stores the normalised partial
+            const int g1_slot = (stage + 2 * (it.n_slots >> 1) - 1) % kSlots;
+            float* stage_o = reinterpret_cast<float*>(sh.kv[g1_slot]);   // [16][kStagePitch]
+            if (grp == 1) {
+#pragma unroll
+                for (int nt = 0; nt < kPVTiles; ++nt) {
+                    const int f = f_base + 8 * nt + 2 * tq;
+                    *reinterpret_cast<float2*>(stage_o + g * kStagePitch + f) = make_float2(o[nt][0], o[nt][1]);
+                    *reinterpret_cast<float2*>(stage_o + (g + 8) * kStagePitch + f) = make_float2(o[nt][2], o[nt][3]);
+                }
+                fence_proxy_async_smem();   // these bytes are a slot the producer refills later
+                if (gw == 0 && tq == 0) {
+                    sh.merge_m[g] = m_ref[0];
+                    sh.merge_m[g + 8] = m_ref[1];
+                    sh.merge_l[g] = L0;
+                    sh.merge_l[g + 8] = L1;
+                }
+            }
+            named_barrier_sync(kBarMma, kMmaThreads);
+            if (grp == 0) {
+                const float m1a = sh.merge_m[g], m1b = sh.merge_m[g + 8];
+                const float ma = fmaxf(m_ref[0], m1a);
+                const float mb = fmaxf(m_ref[1], m1b);
+                const float s0a = m_ref[0] == -INFINITY ? 0.f : ex2_approx(m_ref[0] - ma);
+                const float s1a = m1a == -INFINITY ? 0.f : ex2_approx(m1a - ma);
+                const float s0b = m_ref[1] == -INFINITY ? 0.f : ex2_approx(m_ref[1] - mb);
+                const float s1b = m1b == -INFINITY ? 0.f : ex2_approx(m1b - mb);
+                const float La = L0 * s0a + sh.merge_l[g] * s1a;
+                const float Lb = L1 * s0b + sh.merge_l[g + 8] * s1b;
+                const float inva = La > 0.f ? rcp_approx(La) : 0.f;
+                const float invb = Lb > 0.f ? rcp_approx(Lb) : 0.f;
+                const float c0a = s0a * inva, c1a = s1a * inva, c0b = s0b * invb, c1b = s1b * invb;
+#pragma unroll
+                for (int nt = 0; nt < kPVTiles; ++nt) {
+                    const int f = f_base + 8 * nt + 2 * tq;
+                    const float2 ua = *reinterpret_cast<const float2*>(stage_o + g * kStagePitch + f);
+                    const float2 ub = *reinterpret_cast<const float2*>(stage_o + (g + 8) * kStagePitch + f);
+                    *reinterpret_cast<float2*>(op0 + 8 * nt) =
+                        make_float2(o[nt][0] * c0a + ua.x * c1a, o[nt][1] * c0a + ua.y * c1a);
+                    *reinterpret_cast<float2*>(op1 + 8 * nt) =
+                        make_float2(o[nt][2] * c0b + ub.x * c1b, o[nt][3] * c0b + ub.y * c1b);
+                }
+                if (gw == 0 && tq == 0) {
+                    p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
+                        La > 0.f ? (ma + lg2_approx(La)) * kLn2 : -INFINITY;
+                    p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
+                        Lb > 0.f ? (mb + lg2_approx(Lb)) * kLn2 : -INFINITY;
+                }
+            }
+            named_barrier_sync(kBarMma, kMmaThreads);   // group 1's staged O has been read
+            if (grp == 1 && lane == 0) mbar_arrive(&sh.empty[g1_slot]);
         }
-        if (w == 1 && tq == 0) {
-            p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
-                L0 > 0.f ? (m_ref[0] + lg2_approx(L0)) * kLn2 : -INFINITY;
-            p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
-                L1 > 0.f ? (m_ref[1] + lg2_approx(L1)) * kLn2 : -INFINITY;
-        }
+        stage += it.n_slots;
     }
     if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
 }
@@ -707,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sh.full[i], 1);
-            mbar_init(&sh.empty[i], kComputeWarps);
+            mbar_init(&sh.empty[i], kGroupWarps);   // the group that consumed the slot
         }
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, kComputeWarps);

@@ -311,9 +311,10 @@ long long derive_splits(long long rows, long long pairs, long long grid_cap, int
 // more rows per SM than the tcgen05 kernel's 16-byte cp.async) and every
 // dense shape with 16 heads (T = 256 .. 131072).  With 32 or more heads it
 // reads each cache row once per 16-head group, so once its slices grow past
-// 512 rows per item the tcgen05 kernel with 32 heads per CTA (one read per
-// 32 heads) is faster; below that the warp-MMA kernel's shorter chain wins.
-constexpr long long kMmaMaxRowsPerItemWide = 512;
+// 1024 rows per item the tcgen05 kernel with 32 heads per CTA (one read per
+// 32 heads) is faster (measured: tie at 864 rows, tcgen05 ahead at 1728);
+// below that the warp-MMA kernel wins.
+constexpr long long kMmaMaxRowsPerItemWide = 1024;
 long long rows_per_item(long long rows, int batch, int heads, long long grid_cap, int variant) {
     const long long pairs = static_cast<long long>(batch) * (heads / variant_head_group(variant));
     const long long S = derive_splits(rows, pairs, grid_cap, variant);

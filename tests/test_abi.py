@@ -126,14 +126,14 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
 
 def _model_auto(sparse, rows, batch, heads, sms):
     """The automatic kernel choice, restated: sparse or 16 heads -> warp-MMA;
-    more heads -> warp-MMA while its slices hold <= 512 rows, else 32 heads
+    more heads -> warp-MMA while its slices hold <= 1024 rows, else 32 heads
     per CTA on tcgen05."""
     def per(v):
         S = _model_split(rows, batch * heads // HEADS[v], sms, v)
         return -(-(-(-rows // S)) // GRANULE[v]) * GRANULE[v]
     if sparse or heads == 16:
         return 1
-    return 1 if per(1) <= 512 else 3
+    return 1 if per(1) <= 1024 else 3
 
 
 @pytest.mark.parametrize("rows", [1, 100, 256, 8192, 20000, 32768, 65536, 131072])

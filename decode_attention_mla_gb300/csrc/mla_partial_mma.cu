@@ -16,7 +16,8 @@
 //                   MMA warps) fills a 4-deep ring of 32-row slots.  Dense slices: one
 //                   TMA box {64, 32 rows, 9 chunks} per slot, landing as
 //                   [chunk][row][128 B], 128-byte swizzled (rows past the end
-//                   of the cache read as zeros).  Sparse lists: one 1152-byte
+//                   of the cache read as zeros).  Sparse lists: all four warps
+//                   of the group, eight rows of a slot each, one 1152-byte
 //                   bulk copy per row into padded 1168-byte rows, rows taken
 //                   from indices[b][e] (a gather, "The Commit That Changed
 //                   Direction"); masked entries are zero-filled.  It also
@@ -63,6 +64,12 @@ constexpr int kGroupWarps = kComputeWarps / kGroups;       // 4: one per SM sub-
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kThreads = (kComputeWarps + 4) * 32;         // + a producer warpgroup (one working warp)
 constexpr int kProducerWarp = kComputeWarps;
+// Sparse rows are copied by all four warps of the producer warpgroup, eight
+// rows of a slot each: one warp issuing 32 row copies caps a CTA at ~27 GB/s
+// (measured), four warps of 8 at ~56 GB/s.  Each producer warp signals its
+// own full barrier per slot, so that it can drain its own copies.
+constexpr int kProdWarps = 4;
+constexpr int kRowsPerProd = 32 / kProdWarps;
 // Register split: the CTA is launched with kLaunchRegs per thread; the
 // producer warpgroup drops to kProducerRegs and the two MMA warpgroups rise to
 // kMmaRegs (the query fragments of a contraction half alone take 72).
@@ -110,7 +117,7 @@ struct __align__(1024) SharedStorage {
     float merge_m[kHeadGroup];                             // group 1's reference and row sum, for the merge
     float merge_l[kHeadGroup];
     int valid[kSlots][kStageRows];                         // sparse: row holds an attended entry
-    uint64_t full[kSlots];
+    uint64_t full[kSlots][kDense ? 1 : kProdWarps];        // per slot, one per producer warp (dense: one)
     uint64_t empty[kSlots];
     uint64_t q_full;
     uint64_t q_empty;
@@ -281,8 +288,10 @@ __device__ void prefetch_first_slots(const TcMaps& maps, const PartialParams& p)
         tma_prefetch_3d(&maps.kv, 0, static_cast<int>(base + e), 0);
 }
 
+// wp: producer warp (0 .. kProdWarps-1); dense slices use warp 0 alone, which
+// also stages the query tiles.
 template <bool kDense>
-__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh, int lane) {
+__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh, int wp, int lane) {
     const uint64_t policy = l2_policy_evict_first();
     int stage = 0;            // slots issued so far (ring position)
     // the first query tile is requested before the item is decoded (its key
@@ -290,18 +299,23 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     // (a new tile whenever a busy item's key differs) and release a tile
     // through q_empty, read or not
     int q_key = first_key(p);
+    int q_loads = 0;          // query tiles staged so far
     // the first item's request fields are read before the query tile is
     // requested, so that the two latencies overlap
-    const RequestRead first = read_request(p, blockIdx.x < p.n_items ? request_of(p, blockIdx.x) : 0);
-    load_q(maps, p, sh, q_key, lane);
-    int q_loads = 1;          // query tiles staged so far
+    RequestRead first{0, 0};
+    if (wp == 0) {
+        first = read_request(p, blockIdx.x < p.n_items ? request_of(p, blockIdx.x) : 0);
+        load_q(maps, p, sh, q_key, lane);
+        q_loads = 1;
+    }
     // test hook: a wait that runs out, so every role takes the abort path
-    bool ok = !(p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
+    bool ok = !(wp == 0 && p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, item, item == static_cast<int>(blockIdx.x) ? &first : nullptr);
+        const Item it =
+            decode_item(p, item, (wp == 0 && item == static_cast<int>(blockIdx.x)) ? &first : nullptr);
         if (it.n_slots == 0) continue;
         const int key = it.b * p.n_groups + it.hg;
-        if (key != q_key) {
+        if (wp == 0 && key != q_key) {
             if (!mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag)) {
                 ok = false;
                 break;
@@ -323,22 +337,24 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                     }
                     long long y = it.base + it.e0 + static_cast<long long>(st) * kStageRows;
                     if (y < -2 * kStageRows) y = -2 * kStageRows;   // a box wholly before row 0 either way
-                    mbar_arrive_expect_tx(&sh.full[slot], kDenseSlotBytes);
-                    tma_load_3d(sh.kv[slot], &maps.kv, 0, static_cast<int>(y), 0, &sh.full[slot], policy);
+                    mbar_arrive_expect_tx(&sh.full[slot][0], kDenseSlotBytes);
+                    tma_load_3d(sh.kv[slot], &maps.kv, 0, static_cast<int>(y), 0, &sh.full[slot][0], policy);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             stage = __shfl_sync(0xffffffffu, stage, 0);
         } else {
-            // one row per lane per slot; indices of the next few slots are
-            // loaded ahead of their use
+            // rows 8*wp .. 8*wp+7 of each slot, one per lane 0..7; indices
+            // of the next few slots are loaded ahead of their use
+            const int r_slot = kRowsPerProd * wp + lane;    // row of the slot this lane copies (lane < 8)
+            const bool mine = lane < kRowsPerProd;
             const int seg_len = p.cache_len[it.b];
             const int* idx = p.indices + static_cast<long long>(it.b) * p.topk;
             int idx_pf[kIdxPrefetch];
 #pragma unroll
             for (int k = 0; k < kIdxPrefetch; ++k) {
-                const uint32_t e = it.e0 + static_cast<uint32_t>(k * kStageRows + lane);
-                idx_pf[k] = (e < it.e1) ? idx[e] : -1;
+                const uint32_t e = it.e0 + static_cast<uint32_t>(k * kStageRows + r_slot);
+                idx_pf[k] = (mine && e < it.e1) ? idx[e] : -1;
             }
             for (int st = 0; st < it.n_slots; ++st, ++stage) {
                 const int slot = stage % kSlots;
@@ -356,12 +372,12 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 }
 #pragma unroll
                 for (int k = 0; k + 1 < kIdxPrefetch; ++k) idx_pf[k] = idx_pf[k + 1];
-                const uint32_t en = it.e0 + static_cast<uint32_t>((st + kIdxPrefetch) * kStageRows + lane);
-                idx_pf[kIdxPrefetch - 1] = (en < it.e1) ? idx[en] : -1;
+                const uint32_t en = it.e0 + static_cast<uint32_t>((st + kIdxPrefetch) * kStageRows + r_slot);
+                idx_pf[kIdxPrefetch - 1] = (mine && en < it.e1) ? idx[en] : -1;
 
-                uint8_t* dst = sh.kv[slot] + lane * kSmemRow;
-                sh.valid[slot][lane] = valid ? 1 : 0;
-                if (!valid) {
+                uint8_t* dst = sh.kv[slot] + r_slot * kSmemRow;
+                if (mine) sh.valid[slot][r_slot] = valid ? 1 : 0;
+                if (mine && !valid) {
                     // masked rows still feed P . V (with p = 0): keep them finite
                     uint4* z = reinterpret_cast<uint4*>(dst);
 #pragma unroll 8
@@ -370,19 +386,21 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                 }
                 const uint32_t n_valid = __popc(__ballot_sync(0xffffffffu, valid));
                 __syncwarp();                   // zero rows and flags before the arrival that publishes them
-                if (lane == 0) mbar_arrive_expect_tx(&sh.full[slot], n_valid * static_cast<uint32_t>(kRowBytes));
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&sh.full[slot][wp], n_valid * static_cast<uint32_t>(kRowBytes));
                 __syncwarp();                   // the byte count is registered before any copy lands
-                if (valid) bulk_copy_g2s(dst, p.kv + row * p.row_stride, kRowBytes, &sh.full[slot], policy);
+                if (valid) bulk_copy_g2s(dst, p.kv + row * p.row_stride, kRowBytes, &sh.full[slot][wp], policy);
             }
         }
     }
     if (!ok && lane == 0) raise_device_error(sh, p.status);
-    // Never retire the CTA with copies into its shared memory in flight.
+    // Never retire the CTA with copies into its shared memory in flight: each
+    // producer warp waits for the last phase it armed on its own barriers.
     if (lane == 0) {
         volatile int never = 0;
         for (int slot = 0; slot < kSlots && slot < stage; ++slot) {
             const int last_use = (stage - 1 - slot) / kSlots;
-            if (!mbar_wait_bounded(&sh.full[slot], last_use & 1, &never)) raise_device_error(sh, p.status);
+            if (!mbar_wait_bounded(&sh.full[slot][wp], last_use & 1, &never)) raise_device_error(sh, p.status);
         }
         if (q_loads > 0 && !mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never))
             raise_device_error(sh, p.status);
@@ -563,7 +581,10 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
             const int j = grp + 2 * k;                      // slot of the item
             const int st = stage + j;                       // its ring position
             const int slot = st % kSlots;
-            if (!failed && !warp_wait(&sh.full[slot], (st / kSlots) & 1, &sh.abort_flag)) failed = true;
+            // dense: one TMA box per slot; sparse: each producer warp's rows
+#pragma unroll
+            for (int q = 0; q < (kDense ? 1 : kProdWarps); ++q)
+                if (!failed && !warp_wait(&sh.full[slot][q], (st / kSlots) & 1, &sh.abort_flag)) failed = true;
             // slot rows [v_lo, v_hi) are attended (dense); sparse rows carry flags
             const uint32_t e_slot = it.e0 + static_cast<uint32_t>(j * kStageRows);
             const int v_hi = static_cast<int>(min(it.e1 - e_slot, static_cast<uint32_t>(kStageRows)));
@@ -786,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&sh.full[i], 1);
+            for (int q = 0; q < (kDense ? 1 : kProdWarps); ++q) mbar_init(&sh.full[i][q], 1);
             mbar_init(&sh.empty[i], kGroupWarps);   // the group that consumed the slot
         }
         mbar_init(&sh.q_full, 1);
@@ -811,10 +832,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
             if (warp == kProducerWarp + 1 && lane == 0) prefetch_first_slots(maps, p);
         }
         if (warp == kProducerWarp + 2 && lane == 0) prefetch_first_inputs(maps, p);
-        if (warp == kProducerWarp) {
+        if (warp == kProducerWarp || !kDense) {
             grid_dependency_wait();
             allow_dependent_launch();
-            producer<kDense>(maps, p, sh, lane);
+            producer<kDense>(maps, p, sh, warp - kProducerWarp, lane);
         }
     } else {
         warpgroup_regs_increase<kMmaRegs>();

@@ -41,13 +41,13 @@ def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, pl
     return out, lse, plan, scratch
 
 
-def run_sparse(x, *, splits=0, pdl=False, scratch=None, plan=None, kv_dev=None, variant=0):
+def run_sparse(x, *, splits=0, pdl=False, scratch=None, plan=None, kv_dev=None, variant=0, num_sms=0):
     d = dev()
     B, H, _ = x.q.shape
     topk = x.indices.shape[1]
     if plan is None:
         plan = mla.plan(batch=B, heads=H, sparse=True, topk=topk, scale=x.scale, splits=splits, pdl=pdl,
-                        variant=variant)
+                        variant=variant, num_sms=num_sms)
     if scratch is None:
         scratch = mla.alloc_scratch(plan)
     out = torch.full((B, H, 512), float("nan"), device=d)

@@ -354,7 +354,7 @@ def test_few_ctas_walk_many_slot_items(variant, splits):
 
 @pytest.mark.parametrize("variant", _gpu.VARIANTS)
 def test_sparse_few_ctas_walk_many_items(variant):
-    x = workloads.sparse(3, 16, [5000, 300, 9000], 700, seed=47)
+    x = workloads.sparse(3, 16, [5000, 800, 9000], 700, seed=47)
     ro, rl = _gpu.oracle_sparse(x)
     for s in (1, 2, 5):
         out, lse, plan, _ = _gpu.run_sparse(x, splits=s, num_sms=4, variant=variant)

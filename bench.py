@@ -530,6 +530,26 @@ def time_graph_bench(gb, reps=10, warm=3):
     return us, None, [r / gb.calls * 1e6 for r in rep_list]
 
 
+def project_timing(H, V, reps=50):
+    """mla_decode_project on one merged latent [1, H, 512] with distinct bf16
+    wv_b copies [H, V, 512] (together > 3x L2), captured as one graph."""
+    import decode_attention_mla_gb300 as mla
+    d = torch.device("cuda")
+    g = torch.Generator().manual_seed(5)
+    wbytes = H * V * 512 * 2
+    copies = copies_for(wbytes)
+    w0 = (torch.randn(H, V, 512, generator=g) / 512 ** 0.5).to(torch.bfloat16).to(d)
+    ws = [w0] + [torch.roll(w0, shifts=c, dims=2) for c in range(1, copies)]
+    lat = torch.randn(1, H, 512, generator=g).to(d)
+    y = torch.empty(1, H, V, device=d)
+    gr = capture(lambda c: mla.project(lat, ws[c], y, pdl=True), copies)
+    el = time_graph(gr, reps, 3)
+    us = el / (reps * copies) * 1e6
+    del ws
+    torch.cuda.empty_cache()
+    return {"us": us, "copies": copies, "bytes": wbytes + H * 512 * 4 + H * V * 4}
+
+
 def write_details(args, P):
     rows = []
 
@@ -576,6 +596,14 @@ def write_details(args, P):
            "frac_roofline": max(gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, tensor_us) / us})
     del gb
     torch.cuda.empty_cache()
+    # wv_b projection of the merged latent (H heads, v_dim = 128), one weight copy per call
+    for H in (16, 128):
+        pr = project_timing(H, 128)
+        r = {"workload": f"project_h{H}_v128", "copies": pr["copies"], "us_per_call": pr["us"],
+             "alg_bytes": pr["bytes"], "gbs": pr["bytes"] / (pr["us"] * 1e-6) / 1e9,
+             "frac_hbm": pr["bytes"] / (P["hbm_gbs"] * 1e9) / (pr["us"] * 1e-6)}
+        rows.append(r)
+        log(json.dumps(r))
     with open(args.details, "w") as f:
         json.dump({"peaks": P, "rows": rows}, f, indent=1)
 

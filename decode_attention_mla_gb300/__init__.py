@@ -74,7 +74,7 @@ _lib = None
 
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
-            "mla_decode_strerror", "mla_decode_forward_static")
+            "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project")
 
 
 def lib():
@@ -100,6 +100,8 @@ def lib():
         L.mla_decode_forward_static.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P]
         L.mla_decode_append.restype = I
         L.mla_decode_append.argtypes = [P, LL, LL, P, P, P, I, P]
+        L.mla_decode_project.restype = I
+        L.mla_decode_project.argtypes = [P, P, I, I, I, P, I, P]
         L.mla_decode_advance.restype = I
         L.mla_decode_advance.argtypes = [P, I, P]
         L.mla_decode_scratch_init.restype = I
@@ -233,6 +235,16 @@ def append(kv, new_rows, d_pos, *, row_offset=None, kv_rows=None, row_stride=Non
     batch = int(d_pos.numel())
     _check(lib().mla_decode_append(_ptr(kv), int(kv_rows), int(row_stride), _ptr(new_rows), _ptr(d_pos),
                                    _ptr(row_offset), batch, _stream(stream)), "mla_decode_append")
+
+
+def project(latent, wv_b, y, *, pdl: bool = False, stream=None) -> None:
+    """``mla_decode_project``: y[B,H,v] = latent[B,H,512] . wv_b[H,v,512]^T per head (fp32 out)."""
+    B, H, r = latent.shape
+    if r != D_LATENT or tuple(wv_b.shape[:1]) != (H,) or wv_b.shape[-1] != D_LATENT:
+        raise ValueError("latent must be [B, H, 512] and wv_b [H, v_dim, 512]")
+    v_dim = int(wv_b.shape[1])
+    _check(lib().mla_decode_project(_ptr(latent), _ptr(wv_b), int(B), int(H), v_dim, _ptr(y), int(bool(pdl)),
+                                    _stream(stream)), "mla_decode_project")
 
 
 def advance(d_pos, stream=None) -> None:

@@ -420,6 +420,21 @@ int mla_decode_append(void* kv, long long kv_rows, long long row_stride, const v
     return launch_status(mla::launch_append(p, false, static_cast<cudaStream_t>(stream)));
 }
 
+int mla_decode_project(const float* latent, const void* wv_b, int batch, int heads, int v_dim, float* y, int pdl,
+                       void* stream) {
+    if (!latent || !wv_b || !y || batch < 1 || batch > 65535 || (pdl != 0 && pdl != 1)) return MLA_EINVAL;
+    if (heads < 1 || heads > 128 || v_dim < 16 || v_dim > 512 || v_dim % 16 != 0) return MLA_EUNSUPPORTED;
+    if (misaligned(latent, 16) || misaligned(wv_b, 16) || misaligned(y, 16)) return MLA_EALIGN;
+    mla::ProjectParams p{};
+    p.latent = latent;
+    p.wv_b = static_cast<const uint16_t*>(wv_b);
+    p.y = y;
+    p.batch = batch;
+    p.heads = heads;
+    p.v_dim = v_dim;
+    return launch_status(mla::launch_project(p, pdl != 0, static_cast<cudaStream_t>(stream)));
+}
+
 int mla_decode_advance(int* d_pos, int batch, void* stream) {
     if (!d_pos || batch < 1) return MLA_EINVAL;
     if (misaligned(d_pos, 4)) return MLA_EALIGN;

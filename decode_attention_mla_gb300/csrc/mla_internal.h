@@ -58,6 +58,13 @@ struct CombineParams {
     long long kv_rows;
 };
 
+struct ProjectParams {
+    const float* latent;        // fp32 [B][H][512] (the merged, normalised latent)
+    const uint16_t* wv_b;       // bf16 [H][v_dim][512]
+    float* y;                   // fp32 [B][H][v_dim]
+    int batch, heads, v_dim;
+};
+
 struct AppendParams {
     uint16_t* kv;
     long long kv_rows;
@@ -96,6 +103,7 @@ cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int he
 int combine_block_threads();
 int combine_grid_rows(int rows, int splits);    // combine grid x for B*H rows
 cudaError_t combine_prepare();
+cudaError_t launch_project(const ProjectParams& p, bool pdl, cudaStream_t stream);
 // spread: one CTA per SM (for grids no larger than the SM count)
 cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pdl, bool spread,
                            cudaStream_t stream);

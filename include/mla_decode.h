@@ -223,6 +223,24 @@ MLA_API int mla_decode_append(void *kv, long long kv_rows, long long row_stride,
  * Errors: MLA_EINVAL, MLA_ECUDA. */
 MLA_API int mla_decode_advance(int *d_pos, int batch, void *stream);
 
+/* Project the merged latent through wv_b, per head:
+ *   y[b][h][v] = sum_{r < 512} latent[b][h][r] * wv_b[h][v][r]
+ * ("Graph-resident decode", Lecture 08, s.6: after the merge writes the
+ * normalised latent, a second kernel with grid (n_head, 16) projects it,
+ * each block owning a slice of v_dim and reading only its own wv_b rows; the
+ * dot strides r by 32 across the warp).  latent: (device) fp32 [B][H][512],
+ * e.g. mla_decode_combine's out; wv_b: (device) bf16 [H][v_dim][512], row v
+ * of head h contiguous over r; y: (device) fp32 [B][H][v_dim].  All three
+ * 16-byte aligned, owned by the caller, not retained.  v_dim a multiple of 16
+ * in [16, 512]; 1 <= heads <= 128; 1 <= batch <= 65535.  fp32 arithmetic in a
+ * fixed order (bit-identical across runs).  pdl = 1 launches with
+ * programmatic dependent launch (the kernel waits on the preceding one before
+ * reading latent).  Async on `stream`, capture-safe.  Errors: MLA_EINVAL (null
+ * pointer, batch, pdl), MLA_EUNSUPPORTED (heads, v_dim), MLA_EALIGN,
+ * MLA_ECUDA. */
+MLA_API int mla_decode_project(const float *latent, const void *wv_b, int batch, int heads, int v_dim, float *y,
+                               int pdl, void *stream);
+
 /* Zero the scratch region (async memset on `stream`), clearing the status
  * word.  Errors: MLA_EINVAL, MLA_ECUDA. */
 MLA_API int mla_decode_scratch_init(void *scratch, size_t scratch_bytes, void *stream);

@@ -70,6 +70,8 @@ def _bind(path: str):
                                                 P, P, P, P, I]
     lib.oracle_hardware_threads.restype = I
     lib.oracle_hardware_threads.argtypes = []
+    lib.oracle_mla_project_f64.restype = I
+    lib.oracle_mla_project_f64.argtypes = [P, P, I, I, I, I, P]
     return lib
 
 
@@ -183,3 +185,22 @@ def decode_split(q, kv, *, scale: float, splits: int, granule: int = 1, d_latent
     if return_partials:
         return out, lse, o_part, lse_part
     return out, lse
+
+
+def project(latent, wv_b, *, lib=None):
+    """fp64 projection of a merged latent through wv_b, per head:
+    ``y[b,h,v] = sum_r latent[b,h,r] * wv_b[h,v,r]``.
+
+    ``latent`` [B, H, d_latent] (any float dtype, taken exactly as double),
+    ``wv_b`` bf16 [H, v_dim, d_latent]; returns y [B, H, v_dim] float64."""
+    lat = _np(latent, np.float64)
+    w16 = _u16(wv_b)
+    if lat.ndim != 3 or w16.ndim != 3 or w16.shape[0] != lat.shape[1] or w16.shape[2] != lat.shape[2]:
+        raise ValueError("latent must be [B, H, d] and wv_b [H, v_dim, d]")
+    B, H, d = lat.shape
+    v_dim = w16.shape[1]
+    y = np.zeros((B, H, v_dim), np.float64)
+    rc = (lib or _load()).oracle_mla_project_f64(_ptr(lat), _ptr(w16), B, H, d, v_dim, _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle_mla_project_f64 failed with status {rc}")
+    return y

@@ -306,6 +306,28 @@ int oracle_mla_decode_split_f64(const uint16_t *q, const uint16_t *kv, long long
     return run_job(&J, n_threads);
 }
 
+/* Projection of a merged latent through wv_b, per head ("Graph-resident
+ * decode", Lecture 08, s.6: the merged latent is projected through wv_b by a
+ * second kernel):
+ *   y[b][h][v] = sum_{r < d_latent} latent[b][h][r] * wv_b[h][v][r]
+ * latent fp64 [B][H][d_latent]; wv_b bf16 [H][v_dim][d_latent], widened
+ * exactly; the sum runs r ascending in double. */
+int oracle_mla_project_f64(const double *latent, const uint16_t *wv_b, int batch, int heads, int d_latent,
+                           int v_dim, double *y) {
+    if (!latent || !wv_b || !y || batch < 0 || heads < 1 || d_latent < 1 || v_dim < 1) return ORACLE_EINVAL;
+    for (int b = 0; b < batch; ++b)
+        for (int h = 0; h < heads; ++h) {
+            const double *lat = latent + ((long long)b * heads + h) * d_latent;
+            for (int v = 0; v < v_dim; ++v) {
+                const uint16_t *w = wv_b + ((long long)h * v_dim + v) * d_latent;
+                double acc = 0.0;
+                for (int r = 0; r < d_latent; ++r) acc += lat[r] * widen_bf16(w[r]);
+                y[((long long)b * heads + h) * v_dim + v] = acc;
+            }
+        }
+    return 0;
+}
+
 int oracle_hardware_threads(void) {
     long n = sysconf(_SC_NPROCESSORS_ONLN);
     return n > 0 ? (int)n : 1;

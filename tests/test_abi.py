@@ -301,3 +301,21 @@ def test_append_advance_argument_checks():
     assert L.mla_decode_advance(ctypes.c_void_p(0x1000), 0, None) == mla.EINVAL
     assert L.mla_decode_advance(ctypes.c_void_p(0x1002), 1, None) == mla.EALIGN
     assert L.mla_decode_scratch_init(None, 16, None) == mla.EINVAL
+
+
+def test_project_argument_checks():
+    """mla_decode_project validates everything before any launch."""
+    L = mla.lib()
+    A, W, Y = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    assert L.mla_decode_project(None, W, 1, 16, 128, Y, 0, None) == mla.EINVAL
+    assert L.mla_decode_project(A, None, 1, 16, 128, Y, 0, None) == mla.EINVAL
+    assert L.mla_decode_project(A, W, 1, 16, 128, None, 0, None) == mla.EINVAL
+    assert L.mla_decode_project(A, W, 0, 16, 128, Y, 0, None) == mla.EINVAL
+    assert L.mla_decode_project(A, W, 1, 16, 128, Y, 2, None) == mla.EINVAL
+    assert L.mla_decode_project(A, W, 1, 0, 128, Y, 0, None) == mla.EUNSUPPORTED
+    assert L.mla_decode_project(A, W, 1, 129, 128, Y, 0, None) == mla.EUNSUPPORTED
+    assert L.mla_decode_project(A, W, 1, 16, 120, Y, 0, None) == mla.EUNSUPPORTED
+    assert L.mla_decode_project(A, W, 1, 16, 528, Y, 0, None) == mla.EUNSUPPORTED
+    assert L.mla_decode_project(ctypes.c_void_p(0x1004), W, 1, 16, 128, Y, 0, None) == mla.EALIGN
+    assert L.mla_decode_project(A, ctypes.c_void_p(0x2008), 1, 16, 128, Y, 0, None) == mla.EALIGN
+    assert L.mla_decode_project(A, W, 1, 16, 128, ctypes.c_void_p(0x3004), 0, None) == mla.EALIGN

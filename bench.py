@@ -58,10 +58,19 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_source_hash():
+# the sources each kernel is compiled from (its traffic counters stay valid while they are unchanged)
+KERNEL_SOURCES = {
+    "mla_partial_mma_kernel": ("mla_partial_mma.cu", "tc_utils.cuh", "device_utils.cuh", "mla_internal.h",
+                               "slicing.cuh"),
+    "mla_partial_tc_kernel": ("mla_partial_tc.cu", "tc_utils.cuh", "device_utils.cuh", "mla_internal.h",
+                              "slicing.cuh"),
+    "mla_combine_kernel": ("mla_combine.cu", "device_utils.cuh", "mla_internal.h"),
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    for fn in ("mla_partial_tc.cu", "mla_partial_mma.cu", "tc_utils.cuh", "device_utils.cuh", "mla_internal.h",
-               "slicing.cuh"):
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "decode_attention_mla_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -76,7 +85,7 @@ def ncu_traffic(kernel, workload):
     with open(path) as f:
         d = json.load(f)
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("source_sha256") != kernel_source_hash():
+    if not e or kernel not in KERNEL_SOURCES or e.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

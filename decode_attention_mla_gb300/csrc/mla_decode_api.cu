@@ -27,13 +27,16 @@ constexpr size_t kScratchAlign = 256;
 constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 64-row steps of 32-row slots
 constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
 constexpr int kVariantTc32 = 3;              // tcgen05 head-group-32 kernel, 64-row tiles (dense)
+constexpr int kVariantTc64 = 4;              // tcgen05 head-group-64 kernel, 64-row tiles (dense)
 
 int variant_tile_rows(int v) {
     // warp-MMA: the model counts 32-row slots (a 64-row step costs about two)
-    return v == kVariantTc ? mla::kTcTileRows : v == kVariantTc32 ? mla::kTcTileRows32 : mla::kStageRows;
+    return v == kVariantTc ? mla::kTcTileRows : (v == kVariantTc32 || v == kVariantTc64) ? mla::kTcTileRows32
+                                                                                          : mla::kStageRows;
 }
 int variant_granule(int v) { return v == kVariantWarpMma ? mla::kStageRows : mla::kTcGranule; }
-int variant_head_group(int v) { return v == kVariantTc32 ? 32 : mla::kHeadGroup; }
+int variant_head_group(int v) { return v == kVariantTc64 ? 64 : v == kVariantTc32 ? 32 : mla::kHeadGroup; }
+bool variant_is_tc(int v) { return v == kVariantTc || v == kVariantTc32 || v == kVariantTc64; }
 
 // cuTensorMapEncodeTiled, reached through the runtime (no link-time libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -138,7 +141,7 @@ int check_shape(const mla_decode_shape* s) {
     if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
     if (s->stall_test != 0 && s->stall_test != 1) return MLA_EINVAL;
-    if (s->variant < 0 || s->variant > 3) return MLA_EINVAL;
+    if (s->variant < 0 || s->variant > 4) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
     if (!s->sparse && s->max_ctx < 1) return MLA_EINVAL;
@@ -147,6 +150,8 @@ int check_shape(const mla_decode_shape* s) {
     if (s->heads != 16 && s->heads != 32 && s->heads != 64 && s->heads != 128) return MLA_EUNSUPPORTED;
     // 32 heads per CTA: dense decode with a multiple of 32 heads
     if (s->variant == kVariantTc32 && (s->sparse || s->heads % 32 != 0)) return MLA_EUNSUPPORTED;
+    // 64 heads per CTA: dense decode with a multiple of 64 heads
+    if (s->variant == kVariantTc64 && (s->sparse || s->heads % 64 != 0)) return MLA_EUNSUPPORTED;
     return MLA_OK;
 }
 
@@ -154,8 +159,8 @@ int check_plan(const mla_decode_plan_t* pl) {
     if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
     if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
-    if (pl->variant != kVariantWarpMma && pl->variant != kVariantTc && pl->variant != kVariantTc32) return MLA_EINVAL;
-    if (pl->variant == kVariantTc32 && pl->shape.sparse) return MLA_EINVAL;
+    if (pl->variant != kVariantWarpMma && !variant_is_tc(pl->variant)) return MLA_EINVAL;
+    if ((pl->variant == kVariantTc32 || pl->variant == kVariantTc64) && pl->shape.sparse) return MLA_EINVAL;
     if (pl->head_group != variant_head_group(pl->variant) || pl->n_head_groups * pl->head_group != pl->shape.heads)
         return MLA_EINVAL;
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
@@ -228,7 +233,7 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
     p.stall_test = pl->shape.stall_test;
     const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
-    if (pl->variant == kVariantTc || pl->variant == kVariantTc32) {
+    if (variant_is_tc(pl->variant)) {
         // TMA coordinates are 32-bit: the cache must be addressable by them
         if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
         const int hg = variant_head_group(pl->variant);
@@ -311,10 +316,12 @@ long long derive_splits(long long rows, long long pairs, long long grid_cap, int
 // more rows per SM than the tcgen05 kernel's 16-byte cp.async) and every
 // dense shape with 16 heads (T = 256 .. 131072).  With 32 or more heads it
 // reads each cache row once per 16-head group, so once its slices grow past
-// 1024 rows per item the tcgen05 kernel with 32 heads per CTA (one read per
-// 32 heads) is faster (measured: tie at 864 rows, tcgen05 ahead at 1728);
-// below that the warp-MMA kernel wins.
-constexpr long long kMmaMaxRowsPerItemWide = 1024;
+// 768 rows per item a tcgen05 kernel with the widest head group that divides
+// H (64 heads per CTA: one read per 64 heads; else 32) is faster (measured,
+// H = 64: tie at 864 rows per warp-MMA item, 64 heads per CTA 16% ahead at
+// 1728; H = 128: 4% ahead at 864, 19% at 1728; H = 32: tie at 864, 32 heads
+// per CTA ahead at 1728); below that the warp-MMA kernel wins.
+constexpr long long kMmaMaxRowsPerItemWide = 768;
 long long rows_per_item(long long rows, int batch, int heads, long long grid_cap, int variant) {
     const long long pairs = static_cast<long long>(batch) * (heads / variant_head_group(variant));
     const long long S = derive_splits(rows, pairs, grid_cap, variant);
@@ -322,8 +329,8 @@ long long rows_per_item(long long rows, int batch, int heads, long long grid_cap
 }
 int auto_variant(bool sparse, int batch, int heads, long long rows, long long grid_cap) {
     if (sparse || heads == mla::kHeadGroup) return kVariantWarpMma;
-    return rows_per_item(rows, batch, heads, grid_cap, kVariantWarpMma) <= kMmaMaxRowsPerItemWide ? kVariantWarpMma
-                                                                                                 : kVariantTc32;
+    if (rows_per_item(rows, batch, heads, grid_cap, kVariantWarpMma) <= kMmaMaxRowsPerItemWide) return kVariantWarpMma;
+    return heads % 64 == 0 ? kVariantTc64 : kVariantTc32;
 }
 
 }  // namespace
@@ -368,7 +375,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.grid_x = static_cast<int>(std::min(items, grid_cap));
     pl.grid_y = 1;
     pl.grid_z = 1;
-    const bool tc = pl.variant == kVariantTc || pl.variant == kVariantTc32;
+    const bool tc = variant_is_tc(pl.variant);
     pl.block = tc ? mla::partial_tc_block_threads(pl.head_group) : mla::partial_mma_block_threads();
     pl.smem_bytes = static_cast<int>(tc ? mla::partial_tc_smem_bytes(pl.head_group)
                                                               : mla::partial_mma_smem_bytes());

@@ -1,5 +1,5 @@
 // mla_partial_tc.cu -- split-KV MLA decode partials on the 5th-generation
-// tensor cores (tcgen05 + tensor memory), head groups of 16 or 32.
+// tensor cores (tcgen05 + tensor memory), head groups of 16, 32 or 64.
 //
 // Same work decomposition as the warp-MMA kernel: work item = (request b,
 // head group hg, context slice s); a persistent grid of at most one CTA per
@@ -9,12 +9,15 @@
 // Lecture 08, s.6).
 //
 // A slice is walked in tiles of TR cache rows (80 for head groups of 16, 64
-// for 32), double-buffered in shared memory as 9 column chunks of
+// for 32 and 64), double-buffered in shared memory as 9 column chunks of
 // [TR rows x 64 bf16] in the 128-byte-swizzled layout the tensor cores read;
 // a tile arrives as three TMA boxes of three chunks, each with its own
 // barrier, so the score MMAs start on the first third while the rest is in
-// flight.  The products are taken "swapped", so the long axis (cache rows,
-// or latent features) is the 128-wide M of the MMA and the HG heads are N:
+// flight.
+//
+// Head groups of 16 and 32: the products are taken "swapped", so the long
+// axis (cache rows, or latent features) is the 128-wide M of the MMA and the
+// HG heads are N:
 //   S^T[rows x HG]   = K_tile[rows x 576] . Q^T         36 MMAs, M=128 (TR valid rows), N=HG
 //   O^T[512 x 2HG]  += V_tile^T[512 x rows] . [P_hi | P_lo]^T
 //                                                        4 x TR/16 MMAs, M=128 features, N=2HG
@@ -24,14 +27,29 @@
 // flat in N up to 64, so 32 heads per CTA halve the instructions per head
 // (and the re-reads of each cache row) of wide-head decode.
 //
+// Head group of 64 ("wide"): O^T with P_hi and P_lo side by side would fill
+// all of tensor memory, so the pair is taken along K instead (two MMAs per
+// k-step into one accumulator), and the scores are taken with the heads on M:
+//   S[64 heads x rows]  = Q[64 x 576] . K_tile^T        36 MMAs, M=64, N=TR
+//   O^T[512 x 64]      += V_tile^T . P_hi^T + V_tile^T . P_lo^T
+//                                                        4 x 2 x TR/16 MMAs, M=128 features, N=64
+// so the scores of one head lie in one tensor-memory lane: two threads own
+// a head (32 rows each) and share nothing but the head's tile max.  P_hi^T of a tile is written
+// over the tile's rope chunk (the scores are its only reader), which makes
+// room in shared memory for the 64-head query tile.  Per cache row and head
+// this issues 1.5x fewer MMAs than head groups of 32 and reads each row half
+// as often.
+//
 // Online softmax in base 2 with a lazily moved reference m (per head, the
-// same in every thread): a tile whose scores all stay below m + 8 is turned
-// into probabilities at once (one barrier that ORs "some score is above");
-// only otherwise (the first tile of a slice, or a max that grew by more than
-// 2^8) the tile max is taken (warp max instructions and a four-warp exchange
-// through shared memory), m moves to it and O is rescaled.  Row sums stay
-// per thread (each thread owns one tile row) and are added across the 128
-// threads of its warpgroup once per slice, in a fixed order.
+// same in every thread that sees the head): a tile whose scores all stay
+// below m + 8 is turned into probabilities at once (one barrier that ORs
+// "some score is above"); only otherwise (the first tile of a slice, or a max
+// that grew by more than 2^8) the tile max becomes the reference and O is
+// rescaled.  Head groups of 16 and 32 take the tile max with warp max
+// instructions and a four-warp exchange through shared memory, and keep row
+// sums per thread (one tile row each), added across the warpgroup once per
+// slice in a fixed order; the wide group keeps one running sum per thread
+// (32 rows of one head), the two of a head added once per slice.
 //
 // Warp roles, head group 16 (320 threads):
 //   warps 0-3  producer.  Dense: one thread issues the TMA boxes (rows past
@@ -48,6 +66,9 @@
 // Head group 32 (384 threads, dense only): warp 0 producer, warp 1 score
 // MMAs and allocation, warp 2 P . V MMAs, warps 4-7 and 8-11 softmax for
 // heads 0-15 and 16-31 of the group (each warpgroup covers the tile's rows).
+// Head group 64 (256 threads, dense only): warps 0-2 as for 32; warps 4-7
+// own 16 heads each, two threads per head, and write the partial (O^T lane
+// = feature).
 // Every wait is bounded (MLA_EDEVICE in the status word on a timeout); the
 // threads of a hardware barrier leave a loop together (the decision to leave
 // is the barrier's own OR-reduction); the CTA drains its copies and its MMAs
@@ -82,30 +103,34 @@ static_assert(kChunks % kTcBoxChunks == 0, "a tile is a whole number of TMA boxe
 static_assert(kGroups % kGatherBatches == 0, "gather batches cover whole boxes");
 static_assert((kTcGranule & (kTcGranule - 1)) == 0, "power-of-two granule");
 
-// Everything that follows from the head group HG (16 or 32).
+// Everything that follows from the head group HG (16, 32 or 64).
 template <int HG>
 struct Cfg {
+    static constexpr bool kWide = HG == 64;                        // heads on M for the scores, P pair along K
     static constexpr int kTileRows = HG == 16 ? kTcTileRows : kTcTileRows32;
     static constexpr int kChunkBytes = kTileRows * 128;
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kGroupBytes = kTcBoxChunks * kChunkBytes;
     static constexpr int kQChunkBytes = HG * 128;
     static constexpr int kQBytes = kChunks * kQChunkBytes;
-    static constexpr int kPVHeads = 2 * HG;                        // [P_hi | P_lo] along N
+    static constexpr int kPVHeads = kWide ? HG : 2 * HG;           // N of P . V: [P_hi | P_lo], or one of them
     static constexpr int kPAtomBytes = kPVHeads * 128;             // one 64-row K atom of P^T
     static constexpr int kPAtoms = (kTileRows + 63) / 64;
     static constexpr int kPBytes = kPAtoms * kPAtomBytes;
-    static constexpr int kWGs = HG / 16;                           // softmax warpgroups
+    static constexpr int kWGs = kWide ? 1 : HG / 16;               // softmax warpgroups
     static constexpr int kSoftmaxWarps = 4 * kWGs;
     static constexpr int kMmaWarp = HG == 16 ? 8 : 1;              // QK issue + TMEM allocation
     static constexpr int kPvWarp = HG == 16 ? 9 : 2;               // P . V issue (its own warp)
-    static constexpr int kThreads = HG == 16 ? 320 : 384;
-    static constexpr uint32_t kTmemS = 0;                          // S^T[buf] at columns HG*buf
-    static constexpr uint32_t kTmemO = 2 * HG;                     // O^T block j at 2HG + 2HG*j
+    static constexpr int kThreads = HG == 16 ? 320 : HG == 32 ? 384 : 256;
+    static constexpr int kSCols = kWide ? kTileRows : HG;          // columns of one score buffer
+    static constexpr uint32_t kTmemS = 0;                          // scores [buf] at columns kSCols*buf
+    static constexpr uint32_t kTmemO = 2 * kSCols;                 // O^T block j at kTmemO + kPVHeads*j
     static constexpr uint32_t kTmemCols = HG == 16 ? 256 : 512;
     static_assert(kTileRows % 16 == 0 && kTileRows <= 128, "tile rows: whole k-steps, at most M=128");
     static_assert(kChunkBytes % 1024 == 0, "chunks stay 1024-byte aligned for the 128-byte swizzle");
-    static_assert(kTmemO + 8 * HG <= kTmemCols, "tensor memory holds S and O");
+    static_assert(kTmemO + 4 * kPVHeads <= kTmemCols, "tensor memory holds S and O");
+    static_assert(!kWide || (kTileRows == 64 && kPBytes == kChunkBytes),
+                  "wide: a tile's P_hi^T (64 head lines of 64 rows) fits its rope chunk exactly");
 };
 
 template <int HG>
@@ -124,6 +149,30 @@ struct __align__(1024) SharedStorage {
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// Wide head group: the rope chunk of each tile buffer takes the tile's P_hi^T
+// once its scores are taken; P_lo^T has one buffer of its own.
+template <>
+struct __align__(1024) SharedStorage<64> {
+    using C = Cfg<64>;
+    uint8_t kv[2][C::kTileBytes];         // chunk c of buffer b at kv[b] + c*kChunkBytes; chunk 8 -> P_hi^T
+    uint8_t q[C::kQBytes];                // Q, K-major: head lines of 128 bytes per 64-column chunk
+    uint8_t p_lo[C::kPBytes];             // P_lo^T
+    alignas(16) float alpha[64];          // per-head factors of a rescale of O
+    alignas(16) float inv_l[64];          // 1 / row sum per head, for the partial
+    uint64_t p_hi_full[2];                // P_hi^T of the tile written (its P . V MMAs may start)
+    uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
+    uint64_t q_full, q_empty, o_free, mma_done[2];
+    uint64_t stall_bar;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// 227 KB of dynamic shared memory per CTA, 1 KB of it kept for aligning the window
+constexpr size_t kMaxDynamicSmem = 227 * 1024;
+static_assert(sizeof(SharedStorage<16>) + 1024 <= kMaxDynamicSmem, "head group 16 fits shared memory");
+static_assert(sizeof(SharedStorage<32>) + 1024 <= kMaxDynamicSmem, "head group 32 fits shared memory");
+static_assert(sizeof(SharedStorage<64>) + 1024 <= kMaxDynamicSmem, "head group 64 fits shared memory");
 
 struct Item {
     int b, hg, s, n_tiles;
@@ -410,11 +459,13 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
 // the other): the scores of each tile, and the P . V products.  QK of tile g
 // waits for each third of its tile and for the softmax of tile g-2 (the
 // owner of its score buffer); P . V of tile g waits for the softmax of tile
-// g, and the first one of an item for the previous item's epilogue.
+// g (wide: its P_hi products for P_hi, its P_lo products for P_lo), and the
+// first one of an item for the previous item's epilogue.
 template <int HG>
 __device__ void mma_issue_qk(const PartialParams& p, SharedStorage<HG>& sh, uint32_t tmem) {
     using C = Cfg<HG>;
-    const uint32_t idesc_qk = make_idesc_bf16(128, HG, 0, 0);
+    // swapped: M = 128 cache rows, N = HG heads; wide: M = 64 heads, N = TR rows
+    const uint32_t idesc_qk = C::kWide ? make_idesc_bf16(64, C::kTileRows, 0, 0) : make_idesc_bf16(128, HG, 0, 0);
     // K-major 128-byte-swizzled operands: 8-row groups 1024 bytes apart
     const uint64_t kv_desc0 = make_sdesc(smem_u32(sh.kv[0]), 16, 1024, kLayoutSw128);
     const uint64_t q_desc0 = make_sdesc(smem_u32(sh.q), 16, 1024, kLayoutSw128);
@@ -468,7 +519,14 @@ __device__ void mma_issue_qk(const PartialParams& p, SharedStorage<HG>& sh, uint
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t off = (c * C::kChunkBytes + kk * 32u) >> 4;
                     const uint32_t qoff = (c * C::kQChunkBytes + kk * 32u) >> 4;
-                    umma_bf16(tmem + C::kTmemS + HG * buf, kb + off, q_desc0 + qoff, idesc_qk, (c | kk) ? 1u : 0u);
+                    if constexpr (C::kWide) {
+                        // S[heads x rows]: A = the 64 query lines, B = the tile's rows
+                        umma_bf16(tmem + C::kTmemS + C::kSCols * buf, q_desc0 + qoff, kb + off, idesc_qk,
+                                  (c | kk) ? 1u : 0u);
+                    } else {
+                        umma_bf16(tmem + C::kTmemS + C::kSCols * buf, kb + off, q_desc0 + qoff, idesc_qk,
+                                  (c | kk) ? 1u : 0u);
+                    }
                 }
             }
         }
@@ -487,7 +545,14 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint
     using C = Cfg<HG>;
     constexpr int TR = C::kTileRows;
     const uint32_t idesc_pv = make_idesc_bf16(128, C::kPVHeads, 1, 0);
-    const uint64_t p_desc0 = make_sdesc(smem_u32(sh.p[0]), 16, 1024, kLayoutSw128);
+    // P^T, K-major: head lines of 128 bytes (64 rows), 8-line groups 1024 apart
+    uint64_t p_desc0, plo_desc = 0;
+    if constexpr (C::kWide) {
+        p_desc0 = make_sdesc(smem_u32(sh.kv[0] + (kChunks - 1) * C::kChunkBytes), 16, 1024, kLayoutSw128);
+        plo_desc = make_sdesc(smem_u32(sh.p_lo), 16, 1024, kLayoutSw128);
+    } else {
+        p_desc0 = make_sdesc(smem_u32(sh.p[0]), 16, 1024, kLayoutSw128);
+    }
     // V^T is MN-major: 64-feature atoms one chunk apart, 8-row groups 1024 apart
     const uint64_t v_desc0 = make_sdesc(smem_u32(sh.kv[0]), C::kChunkBytes, 1024, kLayoutSw128);
     Cursor pc;
@@ -497,7 +562,12 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint
     while (pc.valid && ok) {
         const int buf = pc.g & 1;
         const bool first = pc.k == 0;
-        if (!mbar_wait_bounded(&sh.p_full[buf], (pc.g >> 1) & 1, &sh.abort_flag) ||
+        uint64_t* p_ready;                   // wide: P_hi first (P_lo is waited for below)
+        if constexpr (C::kWide)
+            p_ready = &sh.p_hi_full[buf];
+        else
+            p_ready = &sh.p_full[buf];
+        if (!mbar_wait_bounded(p_ready, (pc.g >> 1) & 1, &sh.abort_flag) ||
             (first && items_done > 0 && !mbar_wait_bounded(&sh.o_free, (items_done - 1) & 1, &sh.abort_flag))) {
             ok = false;
             break;
@@ -505,9 +575,39 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint
         tc_fence_after_sync();
         const int ksteps = (rows_in_tile<HG>(pc.it, pc.k) + 15) >> 4;
         const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(buf) * C::kTileBytes) >> 4);
-        const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * C::kPBytes) >> 4);
+        [[maybe_unused]] const uint64_t pb = p_desc0 + ((static_cast<uint32_t>(buf) * C::kPBytes) >> 4);
         const uint32_t acc0 = first ? 0u : 1u;
-        if (ksteps == TR / 16) {
+        if constexpr (C::kWide) {
+            // P_hi^T (over the tile's rope chunk) into every block, then P_lo^T (its
+            // own buffer, written once the previous tile's products are done)
+            const uint64_t phi = p_desc0 + ((static_cast<uint32_t>(buf) * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < TR / 16; ++kk) {
+                    if (kk < ksteps) {
+                        const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
+                        umma_bf16(tmem + C::kTmemO + C::kPVHeads * j, a, phi + ((kk * 32u) >> 4), idesc_pv,
+                                  kk == 0 ? acc0 : 1u);
+                    }
+                }
+            }
+            if (!mbar_wait_bounded(&sh.p_full[buf], (pc.g >> 1) & 1, &sh.abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < TR / 16; ++kk) {
+                    if (kk < ksteps) {
+                        const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
+                        umma_bf16(tmem + C::kTmemO + C::kPVHeads * j, a, plo_desc + ((kk * 32u) >> 4), idesc_pv, 1u);
+                    }
+                }
+            }
+        } else if (ksteps == TR / 16) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -515,7 +615,7 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint
                     const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
                     const uint64_t bd =
                         pb + ((static_cast<uint32_t>(kk >> 2) * C::kPAtomBytes + (kk & 3) * 32u) >> 4);
-                    umma_bf16(tmem + C::kTmemO + 2 * HG * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                    umma_bf16(tmem + C::kTmemO + C::kPVHeads * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
                 }
             }
         } else {
@@ -527,7 +627,7 @@ __device__ void mma_issue_pv(const PartialParams& p, SharedStorage<HG>& sh, uint
                         const uint64_t a = vb + ((2u * j * C::kChunkBytes + kk * 2048u) >> 4);
                         const uint64_t bd =
                             pb + ((static_cast<uint32_t>(kk >> 2) * C::kPAtomBytes + (kk & 3) * 32u) >> 4);
-                        umma_bf16(tmem + C::kTmemO + 2 * HG * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
+                        umma_bf16(tmem + C::kTmemO + C::kPVHeads * j, a, bd, idesc_pv, kk == 0 ? acc0 : 1u);
                     }
                 }
             }
@@ -621,7 +721,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage<HG>& sh, uin
             tc_fence_after_sync();
             float s[16];
             if (w && has_rows) {
-                tmem_ld16(tmem + lane_addr + C::kTmemS + HG * buf + h_off, s);
+                tmem_ld16(tmem + lane_addr + C::kTmemS + C::kSCols * buf + h_off, s);
             } else {
 #pragma unroll
                 for (int h = 0; h < 16; ++h) s[h] = 0.f;
@@ -689,7 +789,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage<HG>& sh, uin
                     tc_fence_after_sync();
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t a = tmem + lane_addr + C::kTmemO + 2 * HG * j + h_off;
+                        const uint32_t a = tmem + lane_addr + C::kTmemO + C::kPVHeads * j + h_off;
                         float hi[16], lo[16];
                         tmem_ld16(a, hi);
                         tmem_ld16(a + HG, lo);
@@ -786,7 +886,7 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage<HG>& sh, uin
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
             float hi[16], lo[16];                         // features 128 j + t of the 16 heads
-            const uint32_t a = tmem + lane_addr + C::kTmemO + 2 * HG * j + h_off;
+            const uint32_t a = tmem + lane_addr + C::kTmemO + C::kPVHeads * j + h_off;
             if constexpr (HG == 16) {
                 float o[32];
                 tmem_ld32(a, o);
@@ -802,6 +902,219 @@ __device__ void softmax_warps(const PartialParams& p, SharedStorage<HG>& sh, uin
 #pragma unroll
             for (int h = 0; h < 16; ++h)
                 o_row[static_cast<long long>(h) * p.splits * kDLatent + 128 * j] = (hi[h] + lo[h]) * inv[h];
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&sh.o_free);
+    }
+    if (!ok && lane == 0) raise_device_error(&sh.abort_flag, p.status);
+}
+
+// ---- wide head group (64 heads): two softmax threads per head -------------
+// The scores come from an M = 64 product, which places head 16i + j in
+// tensor-memory lane 32i + j (i = 0..3, j = 0..15): warp i of the warpgroup
+// reads heads 16i .. 16i + 15 in its lanes 0-15 and hands the tile's rows
+// 32-63 of each head to lane j + 16 (shuffles), so every thread works on 32
+// rows of one head.  The head's reference m is the same in both threads (the
+// tile max is exchanged); each keeps the sum of its own rows, and the two
+// sums are added once per slice.  For the rescales of O and the partial
+// writes, tensor-memory lane 32i + lane is latent feature 128j + 32i + lane
+// of block j.
+__device__ __forceinline__ uint32_t bf16_rn_bits(float x) {
+    // round-to-nearest-even to bf16 for finite x (the upper 16 bits of the result)
+    const uint32_t b = __float_as_uint(x);
+    return (b + 0x7fffu + ((b >> 16) & 1u)) >> 16;
+}
+
+__device__ void softmax_wide(const PartialParams& p, SharedStorage<64>& sh, uint32_t tmem, int q, int lane) {
+    using C = Cfg<64>;
+    constexpr int TR = C::kTileRows;
+    constexpr int HG = 64;
+    constexpr int RH = TR / 2;                       // rows of a tile per thread
+    const int t = q * 32 + lane;                     // thread of the warpgroup (O^T lane in the epilogue)
+    const int half = lane >> 4;                      // rows 32 * half .. 32 * half + 31 of the tile
+    const int head = 16 * q + (lane & 15);           // head of this thread's scores
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t line = (static_cast<uint32_t>(head) >> 3) * 1024u + (static_cast<uint32_t>(head) & 7u) * 128u;
+    const uint32_t swz = static_cast<uint32_t>(head) & 7u;
+    int g = 0;
+    bool ok = true;
+    bool lo_wait_failed = false;                     // a P_lo wait that ran out, reported at the next barrier
+    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        const Item it = decode_item<HG>(p, item);
+        const long long row0 = (static_cast<long long>(it.b) * p.heads + it.hg * HG) * p.splits + it.s;
+        if (it.n_tiles == 0) {
+            for (int k = 0; k < HG / kHeadGroup; ++k)
+                write_empty_partial(p.o_part, p.lse_part, row0 + static_cast<long long>(k) * kHeadGroup * p.splits,
+                                    p.splits, t, kSoftmaxThreads);
+            continue;
+        }
+        float m_ref = -INFINITY;
+        float l = 0.f;                               // sum over this thread's rows
+        const int first_g = g;
+        for (int k = 0; k < it.n_tiles; ++k, ++g) {
+            const int buf = g & 1;
+            const int rows = rows_in_tile<HG>(it, k);
+            // rows at or past the end of the cache were zero-filled by the TMA unit and are masked
+            const long long row_first = it.base + it.e0 + static_cast<long long>(k) * TR;
+            const long long in_cache = p.kv_rows - row_first;
+            const int valid = in_cache < rows ? static_cast<int>(in_cache > 0 ? in_cache : 0) : rows;
+            bool w = mbar_wait_bounded(&sh.s_full[buf], (g >> 1) & 1, &sh.abort_flag) && !lo_wait_failed;
+            w = __all_sync(0xffffffffu, w);
+            tc_fence_after_sync();
+            // raw scores of rows 32 * half + i (lanes 16-31 take theirs from lane - 16)
+            float s[RH];
+            {
+                float v[RH], u[RH];                  // rows 0-31 / 32-63 of the lane's head (lanes 0-15)
+                const uint32_t sa = tmem + lane_addr + C::kTmemS + C::kSCols * buf;
+                if (w) {                             // warp-uniform (the loads are .sync.aligned)
+                    tmem_ld32(sa, v);
+                    tmem_ld32(sa + RH, u);
+                }
+#pragma unroll
+                for (int i = 0; i < RH; ++i) {
+                    const float x = __shfl_sync(0xffffffffu, u[i], lane & 15);
+                    s[i] = (w && RH * half + i < valid) ? (half ? x : v[i]) : -INFINITY;
+                }
+            }
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < RH; ++i) tmax = fmaxf(tmax, s[i]);
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16)) * p.scale_log2;   // base-2 units (scale > 0)
+            // false while the tile max is -inf (nothing attended yet, or all masked)
+            const bool need = tmax > m_ref + kRescaleLog2;
+            if (softmax_barrier_or(0, need || !w)) {
+                if (softmax_barrier_or(0, sh.abort_flag != 0 || !w)) {
+                    ok = false;
+                    break;
+                }
+                // the reference of the head moves to its tile max; the row sums and O
+                // (if it holds earlier tiles of this slice) are scaled to it
+                float alpha = 1.f;
+                if (need) {
+                    alpha = m_ref > -INFINITY ? ex2_approx(m_ref - tmax) : 1.f;
+                    m_ref = tmax;
+                    l *= alpha;
+                }
+                if (softmax_barrier_or(0, alpha != 1.f && g > first_g)) {
+                    if (half == 0) sh.alpha[head] = alpha;
+                    const int gp = g - 1;
+                    bool w2 = mbar_wait_bounded(&sh.o_done[gp & 1], (gp >> 1) & 1, &sh.abort_flag);
+                    w2 = __all_sync(0xffffffffu, w2);
+                    // (the barrier also publishes the factors)
+                    if (softmax_barrier_or(0, !w2)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll 1
+                        for (int c = 0; c < HG; c += 16) {
+                            const uint32_t a = tmem + lane_addr + C::kTmemO + C::kPVHeads * j + c;
+                            float o[16];
+                            tmem_ld16(a, o);
+#pragma unroll
+                            for (int h = 0; h < 16; ++h) o[h] *= sh.alpha[c + h];
+                            tmem_st16(a, o);
+                        }
+                    }
+                }
+            }
+
+            // ---- probabilities as the bf16 pair: P_hi^T into the tile's rope chunk
+            //      (line = head, 64 rows x 2 bytes; this thread: units 4 half .. +3),
+            //      P_lo^T into its buffer ---------------------------------------------
+            uint32_t lo[RH / 2];
+            {
+                const float neg_m = m_ref > -INFINITY ? -m_ref : 0.f;    // m = -inf: every score is -inf
+                const uint32_t hi_base = smem_u32(sh.kv[buf] + (kChunks - 1) * C::kChunkBytes) + line;
+#pragma unroll
+                for (int u = 0; u < RH / 8; ++u) {
+                    uint32_t hi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 8 * u + 2 * i;
+                        const float p0 = ex2_approx(fmaf(s[r], p.scale_log2, neg_m));   // masked: 2^-inf = 0
+                        const float p1 = ex2_approx(fmaf(s[r + 1], p.scale_log2, neg_m));
+                        l += p0;
+                        l += p1;
+                        hi[i] = pack_bf16x2(p0, p1);
+                        const float r0 = p0 - __uint_as_float(hi[i] << 16);          // exact
+                        const float r1 = p1 - __uint_as_float(hi[i] & 0xffff0000u);
+                        lo[4 * u + i] = bf16_rn_bits(r0) | (bf16_rn_bits(r1) << 16);
+                    }
+                    const uint32_t unit = static_cast<uint32_t>(4 * half + u);
+                    st_shared_v4(hi_base + ((unit ^ swz) << 4), hi[0], hi[1], hi[2], hi[3]);
+                }
+            }
+            // ---- dense: masked rows inside the last k-step must hold zeros in V
+            //      (they meet p = 0, and 0 * NaN would not vanish) --------------------
+            {
+                const int rows_read = (rows + 15) & ~15;
+                const uint32_t base = smem_u32(sh.kv[buf]);
+                for (int i = t; i < (rows_read - rows) * 64; i += kSoftmaxThreads) {
+                    const int r = rows + (i >> 6);
+                    const int c = (i >> 3) & 7;
+                    st_shared_v4_zero(base + c * C::kChunkBytes + r * 128 + (i & 7) * 16);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&sh.p_hi_full[buf]);
+            // P_lo^T has one buffer: the P . V of the previous tile must be done with it
+            if (g > 0) {
+                const int gp = g - 1;
+                lo_wait_failed = !mbar_wait_bounded(&sh.o_done[gp & 1], (gp >> 1) & 1, &sh.abort_flag);
+            }
+            if (!lo_wait_failed) {
+                const uint32_t lo_base = smem_u32(sh.p_lo) + line;
+#pragma unroll
+                for (int u = 0; u < RH / 8; ++u) {
+                    const uint32_t unit = static_cast<uint32_t>(4 * half + u);
+                    st_shared_v4(lo_base + ((unit ^ swz) << 4), lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&sh.p_full[buf]);
+        }
+        if (!ok) break;
+
+        // ---- epilogue: lse = m + log2(l) (to natural log) per head, then every
+        //      thread writes its latent feature of the 64 partials, O / l ------------
+        const float l_head = l + __shfl_xor_sync(0xffffffffu, l, 16);   // the same sum in both threads
+        if (half == 0) {
+            p.lse_part[row0 + static_cast<long long>(head) * p.splits] =
+                l_head > 0.f ? (m_ref + log2f(l_head)) * kLn2 : -INFINITY;
+            sh.inv_l[head] = l_head > 0.f ? __frcp_rn(l_head) : 0.f;
+        }
+        const int gl = g - 1;
+        bool w = mbar_wait_bounded(&sh.o_done[gl & 1], (gl >> 1) & 1, &sh.abort_flag) && !lo_wait_failed;
+        w = __all_sync(0xffffffffu, w);
+        if (softmax_barrier_or(0, !w)) {                 // (also publishes 1 / l)
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        {
+            float* o_row = p.o_part + row0 * kDLatent + t;
+            const long long head_stride = static_cast<long long>(p.splits) * kDLatent;
+            // eight pieces (block j, heads c .. c + 31) of feature 128 j + t; the next
+            // piece's tensor-memory load is in flight while this one is stored
+            uint32_t ob[2][32];
+            tmem_ld32_async(tmem + lane_addr + C::kTmemO, ob[0]);
+            tmem_wait_ld32(ob[0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = i >> 1, c = 32 * (i & 1);
+                if (i + 1 < 8)
+                    tmem_ld32_async(tmem + lane_addr + C::kTmemO + C::kPVHeads * ((i + 1) >> 1) + 32 * ((i + 1) & 1),
+                                    ob[(i + 1) & 1]);
+#pragma unroll
+                for (int h = 0; h < 32; ++h)
+                    o_row[(c + h) * head_stride + 128 * j] = __uint_as_float(ob[i & 1][h]) * sh.inv_l[c + h];
+                if (i + 1 < 8) tmem_wait_ld32(ob[(i + 1) & 1]);
+            }
         }
         tc_fence_before_sync();
         mbar_arrive(&sh.o_free);
@@ -826,6 +1139,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(co
             mbar_init(&sh.empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
             mbar_init(&sh.p_full[i], kSoftmaxThreads * C::kWGs);
+            if constexpr (C::kWide) mbar_init(&sh.p_hi_full[i], kSoftmaxThreads);
             mbar_init(&sh.o_done[i], 1);
         }
         mbar_init(&sh.q_full, 1);
@@ -861,7 +1175,10 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(co
         producer<HG>(maps, p, sh, threadIdx.x);
     } else if (softmax) {
         const int sw = warp - kSoftmaxWarp0;
-        softmax_warps<HG>(p, sh, tmem, sw >> 2, sw & 3, lane);
+        if constexpr (C::kWide)
+            softmax_wide(p, sh, tmem, sw, lane);
+        else
+            softmax_warps<HG>(p, sh, tmem, sw >> 2, sw & 3, lane);
     } else if (warp == C::kMmaWarp) {
         if (lane == 0) mma_issue_qk<HG>(p, sh, tmem);
     } else if (warp == C::kPvWarp && lane == 0) {
@@ -878,16 +1195,25 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(co
 }  // namespace
 
 size_t partial_tc_smem_bytes(int head_group) {
-    return (head_group == 32 ? sizeof(SharedStorage<32>) : sizeof(SharedStorage<16>)) + 1024;
+    const size_t storage = head_group == 64   ? sizeof(SharedStorage<64>)
+                           : head_group == 32 ? sizeof(SharedStorage<32>)
+                                              : sizeof(SharedStorage<16>);
+    return storage + 1024;                               // + the alignment of the dynamic window
 }
-int partial_tc_block_threads(int head_group) { return head_group == 32 ? Cfg<32>::kThreads : Cfg<16>::kThreads; }
+int partial_tc_block_threads(int head_group) {
+    return head_group == 64 ? Cfg<64>::kThreads : head_group == 32 ? Cfg<32>::kThreads : Cfg<16>::kThreads;
+}
 
 cudaError_t partial_tc_prepare(int /*device*/) {
-    const cudaError_t e = cudaFuncSetAttribute(mla_partial_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(partial_tc_smem_bytes(16)));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mla_partial_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(partial_tc_smem_bytes(32)));
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(partial_tc_smem_bytes(16)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mla_partial_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(partial_tc_smem_bytes(32)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mla_partial_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(partial_tc_smem_bytes(64)));
+    return e;
 }
 
 cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int head_group, dim3 grid, bool pdl,
@@ -902,6 +1228,7 @@ cudaError_t launch_partial_tc(const TcMaps& maps, const PartialParams& p, int he
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (head_group == 64) return cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<64>, maps, p);
     return head_group == 32 ? cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<32>, maps, p)
                             : cudaLaunchKernelEx(&cfg, mla_partial_tc_kernel<16>, maps, p);
 }

@@ -90,8 +90,11 @@ typedef struct {
                              2 = tcgen05/TMEM kernel, 80-row TMA tiles, 16 heads per CTA;
                              3 = tcgen05/TMEM kernel, 64-row tiles, 32 heads per CTA (dense,
                                  heads a multiple of 32);
+                             4 = tcgen05/TMEM kernel, 64-row tiles, 64 heads per CTA (dense,
+                                 heads a multiple of 64);
                              0 = auto (measured crossovers): sparse or H = 16 -> 1; dense
-                                 H >= 32 -> 1 while its slices hold <= 1024 rows, else 3 */
+                                 H >= 32 -> 1 while its slices hold <= 768 rows, else 4
+                                 (H a multiple of 64) or 3 */
     int pdl;              /* 1 = launch with programmatic dependent launch */
     int stall_test;       /* test hook, 0 in normal use.  1 = one thread of the partial kernel
                              waits (about 1 ms) on a barrier nothing arrives at, so the timeout

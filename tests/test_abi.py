@@ -47,9 +47,9 @@ def _plan(**kw):
     return mla.plan(**base)
 
 
-TILE = {1: 32, 2: 80, 3: 64}     # rows per modelled step: warp-MMA slot, tcgen05 tiles (16 / 32 heads)
-GRANULE = {1: 32, 2: 16, 3: 16}  # slices are whole multiples of this
-HEADS = {1: 16, 2: 16, 3: 32}    # heads per CTA
+TILE = {1: 32, 2: 80, 3: 64, 4: 64}     # rows per modelled step: warp-MMA slot, tcgen05 tiles (16 / 32 / 64 heads)
+GRANULE = {1: 32, 2: 16, 3: 16, 4: 16}  # slices are whole multiples of this
+HEADS = {1: 16, 2: 16, 3: 32, 4: 64}    # heads per CTA
 
 
 def _model_split(rows, pairs, sms, variant=2, max_splits=256):
@@ -72,7 +72,9 @@ def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     (dict(max_ctx=8192), 1, 128, 64),
     (dict(sparse=True, topk=2048), 1, 64, 32),
     (dict(batch=64, sparse=True, topk=2048), 1, 2, 1024),
-    (dict(heads=128, max_ctx=32768 + 64), 3, 37, 896),
+    (dict(heads=128, max_ctx=32768 + 64), 4, 74, 448),
+    (dict(heads=128, max_ctx=32768 + 64, variant=3), 3, 37, 896),
+    (dict(heads=64, max_ctx=32768), 4, 128, 256),
     (dict(max_ctx=131072), 1, 152, 864),
     (dict(max_ctx=131072, variant=2), 2, 149, 880),
     (dict(heads=32, max_ctx=32768), 1, 74, 448),
@@ -97,6 +99,20 @@ def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     assert p.status_offset == 0 and p.o_part_offset % 256 == 0 and p.lse_part_offset % 256 == 0
     assert p.lse_part_offset >= p.o_part_offset + bh * p.splits * 512 * 4
     assert p.scratch_bytes >= p.lse_part_offset + bh * p.splits * 4 and p.scratch_bytes % 256 == 0
+
+
+@pytest.mark.parametrize("rows", [1, 100, 8192, 32768, 131072])
+@pytest.mark.parametrize("batch,heads", [(1, 64), (2, 64), (1, 128), (3, 128)])
+def test_plan_head_group_64(rows, batch, heads):
+    p = _plan(max_ctx=rows, batch=batch, heads=heads, variant=4)
+    assert p.variant == 4 and p.head_group == 64 and p.n_head_groups == heads // 64
+    assert p.splits == _model_split(rows, batch * heads // 64, 152, 4)
+    assert p.entries_per_split == -(-(-(-rows // p.splits)) // 16) * 16
+    assert p.grid_x == min(batch * (heads // 64) * p.splits, 152)
+    assert p.block == 256 and p.smem_bytes <= 227 * 1024
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.head_group = 32
+    assert _call("mla_decode_run", bad, _args(row_offset=0x60000)) == mla.EINVAL
 
 
 @pytest.mark.parametrize("rows", [1, 100, 8192, 131072])
@@ -126,14 +142,16 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
 
 def _model_auto(sparse, rows, batch, heads, sms):
     """The automatic kernel choice, restated: sparse or 16 heads -> warp-MMA;
-    more heads -> warp-MMA while its slices hold <= 1024 rows, else 32 heads
-    per CTA on tcgen05."""
+    more heads -> warp-MMA while its slices hold <= 768 rows, else tcgen05
+    with 64 heads per CTA (H a multiple of 64) or 32."""
     def per(v):
         S = _model_split(rows, batch * heads // HEADS[v], sms, v)
         return -(-(-(-rows // S)) // GRANULE[v]) * GRANULE[v]
     if sparse or heads == 16:
         return 1
-    return 1 if per(1) <= 1024 else 3
+    if per(1) <= 768:
+        return 1
+    return 4 if heads % 64 == 0 else 3
 
 
 @pytest.mark.parametrize("rows", [1, 100, 256, 8192, 20000, 32768, 65536, 131072])
@@ -205,7 +223,9 @@ def test_plan_override():
     (dict(max_ctx=16, splits=-1), mla.EINVAL),
     (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
     (dict(max_ctx=16, variant=7), mla.EINVAL),
-    (dict(max_ctx=16, variant=4), mla.EINVAL),
+    (dict(max_ctx=16, variant=5), mla.EINVAL),
+    (dict(max_ctx=16, heads=32, variant=4), mla.EUNSUPPORTED),         # 64 heads per CTA: H = 32 is too few
+    (dict(heads=64, sparse=True, topk=64, variant=4), mla.EUNSUPPORTED),  # dense only
     (dict(max_ctx=16, variant=3), mla.EUNSUPPORTED),                 # 32 heads per CTA: H = 16 is too few
     (dict(heads=32, sparse=True, topk=64, variant=3), mla.EUNSUPPORTED),  # dense only
 ])

@@ -126,7 +126,8 @@ def test_graph_frozen_position_fails_from_step_one():
 def test_graph_h128_workload(variant):
     """The 64-step, H=128, 32k-context workload: replays byte identical to eager;
     sampled steps against the oracle; every step finite with lse rising as rows are added.
-    Run with the planner's kernel and with the 32-heads-per-CTA tcgen05 kernel."""
+    Run with the planner's kernel (64 heads per CTA here) and with the
+    32-heads-per-CTA tcgen05 kernel forced."""
     g = workloads.make("graph_h128")
     loop = Loop(g, 128, variant=variant)
     loop.reset()

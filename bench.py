@@ -227,9 +227,10 @@ class GraphBench:
     step appends a row to every layer's cache, runs partial + combine per layer,
     then advances d_pos once.  The layers together exceed 3x L2."""
 
-    def __init__(self, H, T0, steps, layers, splits, pdl, seed=0, variant=0):
+    def __init__(self, H, T0, steps, layers, splits, pdl, seed=0, variant=0, fused=False):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
+        self.fused = fused
         d = torch.device("cuda")
         g = workloads.graph(H, T0, steps, seed=seed)
         self.g, self.H, self.T0, self.steps, self.copies = g, H, T0, steps, layers
@@ -258,9 +259,15 @@ class GraphBench:
         self.d_pos.copy_(self.d_pos0)
         for k in range(self.steps):
             for l in range(self.copies):
-                mla.append(self.kv[l], self.new_rows[l][k], self.d_pos)
-                mla.forward_args(self.plan, self.args[l][k], self.scratch)
-            mla.advance(self.d_pos)
+                if self.fused:
+                    # append, partial + combine and (after the last layer) the advance in two launches
+                    mla.forward_step_args(self.plan, self.args[l][k], self.scratch, self.new_rows[l][k:k + 1],
+                                          advance=l == self.copies - 1)
+                else:
+                    mla.append(self.kv[l], self.new_rows[l][k:k + 1], self.d_pos)
+                    mla.forward_args(self.plan, self.args[l][k], self.scratch)
+            if not self.fused:
+                mla.advance(self.d_pos)
 
 
 def capture(fn, n):
@@ -602,6 +609,15 @@ def write_details(args, P):
     entry("graph_h128", gb, us, None, reps,
           {"per": "decode step per layer", "layers": gb.copies,
            "roofline_us_hbm": gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, "roofline_us_tensor": tensor_us,
+           "frac_roofline": max(gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, tensor_us) / us})
+    del gb
+    torch.cuda.empty_cache()
+    # the same steps with the append and the advance folded into the two kernels
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, bool(args.pdl),
+                    variant=args.variant, fused=True)
+    us, _, reps = time_graph_bench(gb)
+    entry("graph_h128_fused_step", gb, us, None, reps,
+          {"per": "decode step per layer", "layers": gb.copies, "launches_per_layer_step": 2,
            "frac_roofline": max(gb.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6, tensor_us) / us})
     del gb
     torch.cuda.empty_cache()

@@ -74,7 +74,7 @@ _lib = None
 
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
-            "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project")
+            "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project", "mla_decode_forward_step")
 
 
 def lib():
@@ -96,6 +96,8 @@ def lib():
             fn = getattr(L, name)
             fn.restype = I
             fn.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P, SZ, P]
+        L.mla_decode_forward_step.restype = I
+        L.mla_decode_forward_step.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P, SZ, P, I, P]
         L.mla_decode_forward_static.restype = I
         L.mla_decode_forward_static.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), P]
         L.mla_decode_append.restype = I
@@ -207,6 +209,21 @@ def forward_args(p: Plan, args: Args, scratch, stream=None) -> None:
     sp, sb = _scratch_args(scratch)
     _check(lib().mla_decode_forward(ctypes.byref(p), ctypes.byref(args), sp, sb, _stream(stream)),
            "mla_decode_forward")
+
+
+def forward_step_args(p: Plan, args: Args, scratch, new_rows, *, advance: bool = True, stream=None) -> None:
+    """``mla_decode_forward_step``: append ``new_rows`` at d_pos, partial + combine, then (if ``advance``)
+    d_pos += 1, in two launches (dense plans)."""
+    sp, sb = _scratch_args(scratch)
+    _check(lib().mla_decode_forward_step(ctypes.byref(p), ctypes.byref(args), sp, sb, _ptr(new_rows),
+                                         int(bool(advance)), _stream(stream)), "mla_decode_forward_step")
+
+
+def forward_step(p: Plan, q, kv, out, lse, scratch, new_rows, *, d_pos, row_offset=None, advance: bool = True,
+                 kv_rows=None, row_stride=None, stream=None) -> None:
+    """As :func:`forward`, with the cache append before it and the position advance after it folded in."""
+    a = make_args(q, kv, out, lse, d_pos=d_pos, row_offset=row_offset, kv_rows=kv_rows, row_stride=row_stride)
+    forward_step_args(p, a, scratch, new_rows, advance=advance, stream=stream)
 
 
 def forward(p: Plan, q, kv, out, lse, scratch, *, d_pos=None, row_offset=None, cache_len=None, indices=None,

@@ -59,6 +59,25 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     }
     grid_dependency_wait();          // the partials come from the preceding kernel
     allow_dependent_launch();
+    // fused state update (dense): the partial kernel took each request's new row
+    // from new_rows; now that it is done reading the cache, CTA (0, 0) writes the
+    // row to cache row d_pos[b] (for the steps after this one) and advances
+    // d_pos.  Nothing in this grid reads either, and the next kernel on the
+    // stream waits for this grid to finish before it does.
+    if (p.new_rows && blockIdx.x == 0 && blockIdx.y == 0) {
+        constexpr int kUnits = kRowBytes / 16;
+        for (int i = threadIdx.x; i < p.batch * kUnits; i += kThreads) {
+            const int b = i / kUnits;
+            const int u = i - b * kUnits;
+            const long long row = (p.row_offset ? p.row_offset[b] : 0) + p.d_pos[b];
+            if (row >= 0 && row < p.kv_rows)
+                reinterpret_cast<uint4*>(p.kv + row * p.row_stride)[u] =
+                    reinterpret_cast<const uint4*>(p.new_rows + static_cast<long long>(b) * kDRow)[u];
+        }
+        __syncthreads();             // every read of d_pos above precedes the increments
+        if (p.advance)
+            for (int b = threadIdx.x; b < p.batch; b += kThreads) p.d_pos_rw[b] += 1;
+    }
     // Every slice holds a partial (the partial kernels write lse = -inf, o = 0
     // for slices without entries), so nothing here depends on the context length.
     const int tu = wl * 32 + lane;                     // thread within the unit: 32 * W >= S

@@ -201,7 +201,15 @@ int launch_status(cudaError_t e) {
     return MLA_ECUDA;
 }
 
-int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch, size_t bytes, void* stream) {
+// Fused decode-step state update (mla_decode_forward_step): the new rows
+// and whether d_pos advances after the merge.
+struct StepUpdate {
+    const uint16_t* new_rows;
+    int advance;
+};
+
+int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch, size_t bytes, void* stream,
+           const StepUpdate* up = nullptr) {
     int rc = check_plan(pl);
     if (rc == MLA_OK) rc = check_args(pl, a);
     if (rc == MLA_OK) rc = check_scratch(pl, scratch, bytes);
@@ -232,6 +240,7 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
     p.stall_test = pl->shape.stall_test;
+    p.new_rows = up ? up->new_rows : nullptr;
     const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
     if (variant_is_tc(pl->variant)) {
         // TMA coordinates are 32-bit: the cache must be addressable by them
@@ -261,7 +270,7 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
 }
 
 int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void* scratch, size_t bytes,
-               void* stream) {
+               void* stream, const StepUpdate* up = nullptr) {
     int rc = check_plan(pl);
     if (rc == MLA_OK) rc = check_args(pl, a);
     if (rc == MLA_OK) rc = check_scratch(pl, scratch, bytes);
@@ -282,6 +291,14 @@ int do_combine(const mla_decode_plan_t* pl, const mla_decode_args* a, const void
     c.row_offset = a->row_offset;
     c.kv_rows = a->kv_rows;
     c.granule = variant_granule(pl->variant);
+    if (up) {
+        // the step's caller hands over the cache and d_pos for writing
+        c.new_rows = up->new_rows;
+        c.kv = static_cast<uint16_t*>(const_cast<void*>(a->kv));
+        c.row_stride = a->row_stride;
+        c.d_pos_rw = const_cast<int*>(a->d_pos);
+        c.advance = up->advance;
+    }
     const bool spread = static_cast<long long>(pl->combine_grid_x) * pl->combine_grid_y <= pl->num_sms;
     return launch_status(mla::launch_combine(c, dim3(pl->combine_grid_x, pl->combine_grid_y, 1), pl->combine_block,
                                              pl->shape.pdl != 0, spread, static_cast<cudaStream_t>(stream)));
@@ -407,6 +424,19 @@ int mla_decode_forward(const mla_decode_plan_t* plan, const mla_decode_args* arg
     int rc = do_run(plan, args, scratch, scratch_bytes, stream);
     if (rc != MLA_OK) return rc;
     return do_combine(plan, args, scratch, scratch_bytes, stream);
+}
+
+int mla_decode_forward_step(const mla_decode_plan_t* plan, const mla_decode_args* args, void* scratch,
+                            size_t scratch_bytes, const void* new_rows, int advance, void* stream) {
+    int rc = check_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (plan->shape.sparse) return MLA_EUNSUPPORTED;
+    if (!new_rows || (advance != 0 && advance != 1)) return MLA_EINVAL;
+    if (misaligned(new_rows, 16)) return MLA_EALIGN;
+    const StepUpdate up{static_cast<const uint16_t*>(new_rows), advance};
+    rc = do_run(plan, args, scratch, scratch_bytes, stream, &up);
+    if (rc != MLA_OK) return rc;
+    return do_combine(plan, args, scratch, scratch_bytes, stream, &up);
 }
 
 int mla_decode_append(void* kv, long long kv_rows, long long row_stride, const void* new_rows, const int* d_pos,

@@ -42,6 +42,9 @@ struct PartialParams {
     float* lse_part;            // [B][H][S]
     int* status;                // status word
     int stall_test;             // test hook: run the timeout path (see mla_decode_shape)
+    // fused append (dense): bf16 [B][576], row b taking the place of cache row
+    // d_pos[b] of request b in the CTA's staged tile; null = read the cache only
+    const uint16_t* new_rows;
 };
 
 struct CombineParams {
@@ -56,6 +59,14 @@ struct CombineParams {
     const int* d_pos;
     const long long* row_offset;
     long long kv_rows;
+    // fused state update after the merge (dense): new_rows[b] written to cache
+    // row d_pos[b] of request b (rows outside [0, kv_rows) are not written),
+    // then d_pos[b] += 1 when advance is set; new_rows null = neither
+    const uint16_t* new_rows;
+    uint16_t* kv;
+    long long row_stride;
+    int* d_pos_rw;
+    int advance;
 };
 
 struct ProjectParams {

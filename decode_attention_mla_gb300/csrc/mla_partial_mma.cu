@@ -122,6 +122,7 @@ struct __align__(1024) SharedStorage {
     uint64_t q_full;
     uint64_t q_empty;
     uint64_t stall_bar;                                    // test hook: a barrier nothing arrives at
+    uint64_t patch_bar;                                    // fused append: the slot holding the new row landed
     int abort_flag;
 };
 
@@ -300,6 +301,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     // through q_empty, read or not
     int q_key = first_key(p);
     int q_loads = 0;          // query tiles staged so far
+    int patch_uses = 0;       // fused append: slots patched so far (phase of patch_bar)
     // the first item's request fields are read before the query tile is
     // requested, so that the two latencies overlap
     RequestRead first{0, 0};
@@ -325,8 +327,18 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             ++q_loads;
         }
         if constexpr (kDense) {
+            // fused append: entry d_pos[b] of the request is the new row; it lies
+            // in this item when the slice holds it (then it is the item's last
+            // entry, in its last slot)
+            int patch_r = -1;
+            if (p.new_rows) {
+                const long long dp = p.d_pos[it.b];
+                if (dp >= static_cast<long long>(it.e0) && dp < static_cast<long long>(it.e1))
+                    patch_r = static_cast<int>(dp - it.e0) - (it.n_slots - 1) * kStageRows;
+            }
             // one TMA box per slot from lane 0; rows before the cache (a
             // negative first row) and past its end read as zeros
+            bool patch_issued = false;
             if (lane == 0) {
                 for (int st = 0; st < it.n_slots; ++st, ++stage) {
                     const int slot = stage % kSlots;
@@ -337,12 +349,38 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                     }
                     long long y = it.base + it.e0 + static_cast<long long>(st) * kStageRows;
                     if (y < -2 * kStageRows) y = -2 * kStageRows;   // a box wholly before row 0 either way
-                    mbar_arrive_expect_tx(&sh.full[slot][0], kDenseSlotBytes);
-                    tma_load_3d(sh.kv[slot], &maps.kv, 0, static_cast<int>(y), 0, &sh.full[slot][0], policy);
+                    // the slot that takes the new row lands on the patch barrier first
+                    const bool patched = patch_r >= 0 && st == it.n_slots - 1;
+                    uint64_t* bar = patched ? &sh.patch_bar : &sh.full[slot][0];
+                    patch_issued = patched;
+                    mbar_arrive_expect_tx(bar, kDenseSlotBytes);
+                    tma_load_3d(sh.kv[slot], &maps.kv, 0, static_cast<int>(y), 0, bar, policy);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             stage = __shfl_sync(0xffffffffu, stage, 0);
+            if (__shfl_sync(0xffffffffu, patch_issued ? 1 : 0, 0)) {
+                // once the slot's rows are in, row patch_r is overwritten with the new
+                // row (same swizzled layout), then the slot is handed to the MMA warps
+                volatile int never = 0;
+                bool w = mbar_wait_bounded(&sh.patch_bar, patch_uses & 1, &never);
+                w = __all_sync(0xffffffffu, w);
+                ++patch_uses;
+                const int slot = (stage - 1) % kSlots;
+                if (w && ok) {
+                    const uint4* src = reinterpret_cast<const uint4*>(p.new_rows + static_cast<long long>(it.b) * kDRow);
+                    const uint32_t row = smem_u32(sh.kv[slot]) + patch_r * 128;
+                    for (int u = lane; u < kRowBytes / 16; u += 32) {
+                        const uint4 v = src[u];
+                        st_shared_v4(row + (u >> 3) * kDenseChunkBytes + (((u & 7) ^ (patch_r & 7)) << 4), v.x, v.y,
+                                     v.z, v.w);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.full[slot][0]);
+                } else {
+                    ok = false;
+                }
+            }
         } else {
             // rows 8*wp .. 8*wp+7 of each slot, one per lane 0..7; indices
             // of the next few slots are loaded ahead of their use
@@ -813,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, kComputeWarps);
         mbar_init(&sh.stall_bar, 1);
+        mbar_init(&sh.patch_bar, 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }

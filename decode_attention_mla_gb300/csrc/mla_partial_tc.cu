@@ -146,6 +146,7 @@ struct __align__(1024) SharedStorage {
     uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
     uint64_t q_full, q_empty, o_free, mma_done[2];
     uint64_t stall_bar;                   // test hook: a barrier nothing arrives at
+    uint64_t patch_bar;                   // fused append: the tile holding the new row landed
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -164,6 +165,7 @@ struct __align__(1024) SharedStorage<64> {
     uint64_t full[2][kGroups], empty[2], s_full[2], p_full[2], o_done[2];
     uint64_t q_full, q_empty, o_free, mma_done[2];
     uint64_t stall_bar;
+    uint64_t patch_bar;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -317,6 +319,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     int q_key = first_key(p);
     const uint64_t pol_kv = l2_policy_evict_first();
     int q_loads = 1;
+    int patch_uses = 0;                                  // fused append: tiles patched so far
     Cursor cur;
     cursor_init<HG>(p, cur);
     // L2 prefetch runs two tiles ahead of the shared-memory loads (dense); the
@@ -363,11 +366,44 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
             stop = sh.abort_flag != 0;
             if (stop) break;
             const int y = static_cast<int>(it.base) + r0;
+            // fused append: the tile holding entry d_pos[b] of the request lands on
+            // the patch barrier; that row is then overwritten with the new row and
+            // the tile handed on through its three barriers
+            int patch_r = -1;
+            if (p.new_rows) {
+                const long long dp = p.d_pos[it.b];
+                if (dp >= r0 && dp < r0 + rows_in_tile<HG>(it, k)) patch_r = static_cast<int>(dp - r0);
+            }
+            if (patch_r < 0) {
 #pragma unroll
-            for (int grp = 0; grp < kGroups; ++grp) {
-                mbar_arrive_expect_tx(&sh.full[buf][grp], C::kGroupBytes);
-                tma_load_3d(sh.kv[buf] + grp * C::kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.full[buf][grp],
-                            pol_kv);
+                for (int grp = 0; grp < kGroups; ++grp) {
+                    mbar_arrive_expect_tx(&sh.full[buf][grp], C::kGroupBytes);
+                    tma_load_3d(sh.kv[buf] + grp * C::kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks,
+                                &sh.full[buf][grp], pol_kv);
+                }
+            } else {
+                mbar_arrive_expect_tx(&sh.patch_bar, C::kTileBytes);
+#pragma unroll
+                for (int grp = 0; grp < kGroups; ++grp)
+                    tma_load_3d(sh.kv[buf] + grp * C::kGroupBytes, &maps.kv, 0, y, grp * kTcBoxChunks, &sh.patch_bar,
+                                pol_kv);
+                volatile int never = 0;
+                const bool landed = mbar_wait_bounded(&sh.patch_bar, patch_uses & 1, &never);
+                ++patch_uses;
+                if (!landed) {
+                    raise_device_error(&sh.abort_flag, p.status);
+                    break;
+                }
+                const uint4* src = reinterpret_cast<const uint4*>(p.new_rows + static_cast<long long>(it.b) * kDRow);
+                const uint32_t row = smem_u32(sh.kv[buf]) + patch_r * 128;
+                for (int u = 0; u < kRowBytes / 16; ++u) {
+                    const uint4 v = src[u];
+                    st_shared_v4(row + (u >> 3) * C::kChunkBytes + (((u & 7) ^ (patch_r & 7)) << 4), v.x, v.y, v.z,
+                                 v.w);
+                }
+                fence_proxy_async_smem();            // the tensor cores read it next
+#pragma unroll
+                for (int grp = 0; grp < kGroups; ++grp) mbar_arrive(&sh.full[buf][grp]);
             }
             if (pf.valid) {
                 const int yp = cursor_row<HG>(pf);
@@ -1148,6 +1184,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) mla_partial_tc_kernel(co
         mbar_init(&sh.mma_done[0], 1);
         mbar_init(&sh.mma_done[1], 1);
         mbar_init(&sh.stall_bar, 1);
+        mbar_init(&sh.patch_bar, 1);
         sh.abort_flag = 0;
         mbar_init_fence();
     }

@@ -182,6 +182,28 @@ MLA_API int mla_decode_combine(const mla_decode_plan_t *plan, const mla_decode_a
 MLA_API int mla_decode_forward(const mla_decode_plan_t *plan, const mla_decode_args *args, void *scratch,
                        size_t scratch_bytes, void *stream);
 
+/* One dense decode step with the cache append and the position advance folded
+ * into the two kernels ("Graph-resident decode", Lecture 08, s.2: append,
+ * attention and the increment inside the captured region; fewer graph nodes
+ * per step).  Same results, bit for bit, as
+ *   mla_decode_append(kv, .., new_rows, d_pos, ..); mla_decode_forward(..);
+ *   if (advance) mla_decode_advance(d_pos, ..);
+ * in two launches instead of three or four: the partial kernel's CTA whose
+ * slice holds row d_pos[b] of request b takes that row from new_rows[b]
+ * (after its tile lands, in shared memory), and after the merge the combine
+ * kernel writes new_rows[b] to cache row row_offset[b] + d_pos[b] (rows
+ * outside [0, kv_rows) are neither written nor attended, as with the append)
+ * and, if advance = 1, increments d_pos[b].  new_rows: (device) bf16 [B][576],
+ * 16-byte aligned, read during the call.  Unlike mla_decode_run, this call
+ * writes args->kv (one row per request) and args->d_pos (when advancing): both
+ * must be writable device memory that no other work on other streams touches
+ * meanwhile.  Dense plans only (MLA_EUNSUPPORTED for sparse).  advance: 0 or 1
+ * (with several caches sharing one position, e.g. the layers of a model, pass
+ * 1 only for the last).  Errors: as mla_decode_forward, and MLA_EINVAL (null
+ * new_rows, advance not 0/1), MLA_EALIGN (new_rows), MLA_EUNSUPPORTED. */
+MLA_API int mla_decode_forward_step(const mla_decode_plan_t *plan, const mla_decode_args *args, void *scratch,
+                                    size_t scratch_bytes, const void *new_rows, int advance, void *stream);
+
 /* Size of the library's own scratch array used by mla_decode_forward_static. */
 #define MLA_STATIC_SCRATCH_BYTES (8u << 20)
 

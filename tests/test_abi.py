@@ -339,3 +339,33 @@ def test_project_argument_checks():
     assert L.mla_decode_project(ctypes.c_void_p(0x1004), W, 1, 16, 128, Y, 0, None) == mla.EALIGN
     assert L.mla_decode_project(A, ctypes.c_void_p(0x2008), 1, 16, 128, Y, 0, None) == mla.EALIGN
     assert L.mla_decode_project(A, W, 1, 16, 128, ctypes.c_void_p(0x3004), 0, None) == mla.EALIGN
+
+
+def test_forward_step_argument_checks():
+    """mla_decode_forward_step rejects what it cannot run before any launch:
+    sparse plans, a missing or misaligned new-row buffer, advance not 0/1, and
+    everything mla_decode_forward rejects."""
+    L = mla.lib()
+    p = _plan(max_ctx=64)
+    a = _args(row_offset=None)
+    rows = ctypes.c_void_p(0x70000)
+
+    def call(plan, args, new_rows, adv, scratch=0x100000, nbytes=None):
+        nb = plan.scratch_bytes if (plan is not None and nbytes is None) else (nbytes or 0)
+        return L.mla_decode_forward_step(ctypes.byref(plan) if plan is not None else None,
+                                         ctypes.byref(args) if args is not None else None,
+                                         ctypes.c_void_p(scratch) if scratch else None, nb, new_rows, adv, None)
+
+    assert call(None, a, rows, 1) == mla.EINVAL
+    assert call(p, a, None, 1) == mla.EINVAL
+    assert call(p, a, rows, 2) == mla.EINVAL
+    assert call(p, a, rows, -1) == mla.EINVAL
+    assert call(p, a, ctypes.c_void_p(0x70008), 1) == mla.EALIGN
+    assert call(p, None, rows, 0) == mla.EINVAL
+    assert call(p, a, rows, 1, scratch=0) == mla.ESCRATCH
+    assert call(p, a, rows, 1, nbytes=16) == mla.ESCRATCH
+    ps = _plan(sparse=True, topk=64)
+    assert call(ps, _args(row_offset=0x60000, indices=0x61000, cache_len=0x62000), rows, 1) == mla.EUNSUPPORTED
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.magic = 0
+    assert call(bad, a, rows, 1) == mla.EINVAL

@@ -18,7 +18,9 @@ split-KV partials and their log-sum-exp merge in float64.  Passages followed:
 cache + pos * key_length) and s.6 (normalised merge of per-slice partials, slice
 sum in ascending order); "Launch Geometry" (Lecture 04) s.8 (a split count only
 re-associates the combine); "The Commit That Changed Direction" (sparse gather
-of indexed latent rows).
+of indexed latent rows).  ``decode_e4m3`` takes an FP8 (OCP E4M3) cache with
+one scale and dequantises it (``e4m3(byte) * kv_scale``, exact in float64)
+before the same definition.
 """
 from __future__ import annotations
 
@@ -72,6 +74,11 @@ def _bind(path: str):
     lib.oracle_hardware_threads.argtypes = []
     lib.oracle_mla_project_f64.restype = I
     lib.oracle_mla_project_f64.argtypes = [P, P, I, I, I, I, P]
+    lib.oracle_mla_decode_e4m3_f64.restype = I
+    lib.oracle_mla_decode_e4m3_f64.argtypes = [P, P, D, LL, LL, I, I, I, I, D, I, P, P, P, P, I, I, I,
+                                               P, P, P, P, I]
+    lib.oracle_e4m3_to_f64.restype = I
+    lib.oracle_e4m3_to_f64.argtypes = [P, LL, P]
     return lib
 
 
@@ -182,6 +189,64 @@ def decode_split(q, kv, *, scale: float, splits: int, granule: int = 1, d_latent
         _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), int(n_threads))
     if rc != 0:
         raise ValueError(f"oracle_mla_decode_split_f64 failed with status {rc}")
+    if return_partials:
+        return out, lse, o_part, lse_part
+    return out, lse
+
+
+def _u8(a) -> np.ndarray:
+    """E4M3 bytes as a contiguous uint8 numpy array (accepts torch uint8 / float8_e4m3fn tensors)."""
+    if hasattr(a, "dtype") and str(a.dtype) in ("torch.float8_e4m3fn", "torch.uint8"):
+        import torch
+        a = a.contiguous().view(torch.uint8).numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("E4M3 inputs must be torch.float8_e4m3fn / uint8 tensors or uint8 arrays")
+    return a
+
+
+def e4m3_values(data, *, lib=None) -> np.ndarray:
+    """The value of every E4M3 byte of ``data`` (float64, same shape): the
+    dequantisation step with scale 1."""
+    b = _u8(data)
+    out = np.zeros(b.shape, np.float64)
+    rc = (lib or _load()).oracle_e4m3_to_f64(_ptr(b), int(b.size), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_e4m3_to_f64 failed with status {rc}")
+    return out
+
+
+def decode_e4m3(q, kv, *, kv_scale: float, scale: float, d_latent: int = 512, d_rope: int = 64, d_pos=None,
+                indices=None, cache_len=None, row_offset=None, row_stride=None, splits: int = 0, granule: int = 1,
+                n_threads: int = 0, return_partials: bool = False, lib=None):
+    """As :func:`decode` (``splits`` >= 1: as :func:`decode_split`) over an
+    E4M3 cache: ``kv`` holds the bytes of rows of ``d_latent + d_rope``
+    values, each value ``e4m3(byte) * kv_scale``; q stays bf16."""
+    q16 = _u16(q)
+    kv8 = _u8(kv)
+    D = d_latent + d_rope
+    if q16.ndim != 3 or q16.shape[-1] != D:
+        raise ValueError("q must be [B, H, d_latent + d_rope]")
+    if row_stride is None:
+        row_stride = kv8.shape[-1]
+    kv_rows = kv8.size // row_stride if kv8.size else 0
+    B, H, _ = q16.shape
+    sparse = indices is not None
+    d_pos_a = _np(d_pos, np.int32)
+    idx_a = _np(indices, np.int32)
+    len_a = _np(cache_len, np.int32)
+    off_a = _np(row_offset, np.int64)
+    topk = int(idx_a.shape[-1]) if sparse else 0
+    out = np.zeros((B, H, d_latent), np.float64)
+    lse = np.zeros((B, H), np.float64)
+    o_part = np.zeros((B, H, splits, d_latent), np.float64) if return_partials else None
+    lse_part = np.zeros((B, H, splits), np.float64) if return_partials else None
+    rc = (lib or _load()).oracle_mla_decode_e4m3_f64(
+        _ptr(q16), _ptr(kv8), float(kv_scale), int(kv_rows), int(row_stride), B, H, d_latent, d_rope, float(scale),
+        int(sparse), _ptr(d_pos_a), _ptr(off_a), _ptr(len_a), _ptr(idx_a), topk, int(splits), int(granule),
+        _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_mla_decode_e4m3_f64 failed with status {rc}")
     if return_partials:
         return out, lse, o_part, lse_part
     return out, lse

@@ -37,7 +37,14 @@
  *
  * Arithmetic: every stored bf16 value is widened exactly to double; every
  * score, exponential and sum is formed in double with plain sequential
- * loops; the two-pass form (max, then sum) is used.  The split emulation
+ * loops; the two-pass form (max, then sum) is used.
+ *
+ * FP8 cache ("Graph-resident decode" s.9 narrows the latent cache from F32
+ * to F16 for bandwidth; this takes that one step further and is not on the
+ * pages): the rows hold OCP FP8 E4M3 bytes and one scale for the whole
+ * cache; the dequantisation step value = e4m3(byte) * kv_scale is done in
+ * double before the definition above, which is otherwise unchanged (q
+ * stays bf16).  The split emulation
  * computes per-slice partials and merges them exactly as a split-KV decode
  * does, still in double, to pin the combine algebra.
  */
@@ -60,9 +67,24 @@ static double widen_bf16(uint16_t bits) {
     return (double)f;
 }
 
+/* Value of an OCP FP8 E4M3 byte: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; exponent field 0 holds the subnormals m/8 * 2^-6; there are
+ * no infinities, and S.1111.111 is NaN (so the largest finite value is
+ * 1.75 * 2^8 = 448). */
+static double widen_e4m3(uint8_t bits) {
+    const int e = (bits >> 3) & 15, m = bits & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (bits & 0x80) ? -v : v;
+}
+
 typedef struct {
     const uint16_t *q;          /* [B][H][d_latent + d_rope] */
-    const uint16_t *kv;         /* rows of [d_latent + d_rope], row_stride apart */
+    const void *kv;             /* rows of [d_latent + d_rope], row_stride apart: bf16, or E4M3 bytes */
+    int kv_fp8;                 /* 1: the rows are E4M3 bytes, dequantised with kv_scale */
+    double kv_scale;
     long long kv_rows;
     long long row_stride;       /* elements */
     int batch, heads, d_latent, d_rope;
@@ -84,6 +106,12 @@ typedef struct {
     pthread_mutex_t lock;
     int status;
 } job_t;
+
+/* Element i of cache row r, in double. */
+static double kv_at(const job_t *J, long long r, int i) {
+    if (J->kv_fp8) return widen_e4m3(((const uint8_t *)J->kv)[r * J->row_stride + i]) * J->kv_scale;
+    return widen_bf16(((const uint16_t *)J->kv)[r * J->row_stride + i]);
+}
 
 /* Collect the attended absolute row ids of request b into rows[]; returns count. */
 static long long attended_rows(const job_t *J, int b, long long *rows) {
@@ -113,11 +141,10 @@ static void scores(const job_t *J, int b, int h, const long long *rows, long lon
     const int D = J->d_latent + J->d_rope;
     const uint16_t *qh = J->q + ((long long)b * J->heads + h) * D;
     for (long long t = 0; t < n; ++t) {
-        const uint16_t *row = J->kv + rows[t] * J->row_stride;
         double lat = 0.0, rope = 0.0;
-        for (int i = 0; i < J->d_latent; ++i) lat += widen_bf16(qh[i]) * widen_bf16(row[i]);
+        for (int i = 0; i < J->d_latent; ++i) lat += widen_bf16(qh[i]) * kv_at(J, rows[t], i);
         for (int i = 0; i < J->d_rope; ++i)
-            rope += widen_bf16(qh[J->d_latent + i]) * widen_bf16(row[J->d_latent + i]);
+            rope += widen_bf16(qh[J->d_latent + i]) * kv_at(J, rows[t], J->d_latent + i);
         s[t] = (lat + rope) * J->scale;
     }
 }
@@ -135,8 +162,7 @@ static void attend(const job_t *J, const long long *rows, const double *s, long 
     double lse = m + log(l);
     for (long long t = lo; t < hi; ++t) {
         double w = exp(s[t] - lse);
-        const uint16_t *row = J->kv + rows[t] * J->row_stride;
-        for (int f = 0; f < F; ++f) o[f] += w * widen_bf16(row[f]);
+        for (int f = 0; f < F; ++f) o[f] += w * kv_at(J, rows[t], f);
     }
     *lse_out = lse;
 }
@@ -304,6 +330,32 @@ int oracle_mla_decode_split_f64(const uint16_t *q, const uint16_t *kv, long long
     J.splits = splits; J.granule = granule < 1 ? 1 : granule;
     J.out = out; J.lse = lse; J.o_part = o_part; J.lse_part = lse_part;
     return run_job(&J, n_threads);
+}
+
+/* The two-pass reference (or, with splits >= 1, the split emulation) over an
+ * E4M3 cache with one scale: kv holds bytes, row_stride in bytes (elements). */
+int oracle_mla_decode_e4m3_f64(const uint16_t *q, const uint8_t *kv, double kv_scale, long long kv_rows,
+                               long long row_stride, int batch, int heads, int d_latent, int d_rope, double scale,
+                               int sparse, const int *d_pos, const long long *row_offset, const int *cache_len,
+                               const int *indices, int topk, int splits, int granule, double *out, double *lse,
+                               double *o_part, double *lse_part, int n_threads) {
+    if (splits < 0 || !(kv_scale > 0.0) || !isfinite(kv_scale)) return ORACLE_EINVAL;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.kv = kv; J.kv_fp8 = 1; J.kv_scale = kv_scale; J.kv_rows = kv_rows; J.row_stride = row_stride;
+    J.batch = batch; J.heads = heads; J.d_latent = d_latent; J.d_rope = d_rope;
+    J.scale = scale; J.sparse = sparse; J.d_pos = d_pos; J.row_offset = row_offset;
+    J.cache_len = cache_len; J.indices = indices; J.topk = topk;
+    J.splits = splits; J.granule = granule < 1 ? 1 : granule;
+    J.out = out; J.lse = lse; J.o_part = o_part; J.lse_part = lse_part;
+    return run_job(&J, n_threads);
+}
+
+/* Values of n E4M3 bytes (the dequantisation step with scale 1). */
+int oracle_e4m3_to_f64(const uint8_t *in, long long n, double *out) {
+    if ((!in || !out) && n > 0) return ORACLE_EINVAL;
+    for (long long i = 0; i < n; ++i) out[i] = widen_e4m3(in[i]);
+    return 0;
 }
 
 /* Projection of a merged latent through wv_b, per head ("Graph-resident

@@ -20,6 +20,10 @@ scale = 1/sqrt(576)):
 
 Draw order per workload (stream ids): lengths (sparse_b64 only), q, kv, indices;
 graph_h128 adds the 64 new rows and the 64 per-step queries.
+
+FP8 caches (``to_e4m3``): the same bf16 draws, stored as OCP E4M3 bytes with
+one scale per cache, amax / 448 (PyTorch's float8_e4m3fn rounding,
+nearest-even); the oracle and the GPU both read those bytes.
 """
 from __future__ import annotations
 
@@ -191,3 +195,17 @@ def make(name: str, *, seed: int = 0):
     if w["kind"] == "graph":
         return graph(w["H"], w["T0"], w["steps"], B=w["B"], seed=seed)
     raise KeyError(name)
+
+
+E4M3_MAX = 448.0
+
+
+def to_e4m3(kv: torch.Tensor):
+    """Quantise a bf16 cache to E4M3 bytes with one scale (amax / 448, so the
+    largest magnitude maps to the largest finite E4M3 value).  Returns the
+    uint8 bytes (same shape) and the float scale; the value of a byte b is
+    e4m3(b) * scale."""
+    amax = float(kv.float().abs().max()) if kv.numel() else 0.0
+    scale = amax / E4M3_MAX if amax > 0 else 1.0
+    q8 = (kv.float() / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8), scale

@@ -16,6 +16,9 @@ What pins what:
   pin_sparse_is_dense    sparse with ids = a permutation of 0..T-1 equals dense
   pin_permutation        reordering the id list does not change the result
   pin_argmax_limit       q scaled up: out tends to the arg-max row
+  pin_e4m3_decoding      FP8 (E4M3) bytes: PyTorch's float8_e4m3fn widening of all 256
+  pin_e4m3_decode        FP8-cache decode: numpy float64 softmax over the cache
+                         dequantised by PyTorch's widening times the scale
 """
 from __future__ import annotations
 
@@ -305,6 +308,43 @@ def pin_argmax_limit(lib=None):
         assert np.abs(out[0, h] - _f64(kv)[top, :512]).max() <= 1e-9, "large q: out must be the arg-max row"
 
 
+def _torch_e4m3(b: np.ndarray) -> np.ndarray:
+    """PyTorch's float8_e4m3fn widening of E4M3 bytes (independent of the oracle)."""
+    return torch.from_numpy(np.ascontiguousarray(b)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_decoding(lib=None):
+    every = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3_values(every, lib=lib)
+    ref = _torch_e4m3(every)
+    assert np.array_equal(np.isnan(v), np.isnan(ref)), "E4M3: NaN patterns"
+    fin = ~np.isnan(ref)
+    assert np.array_equal(v[fin], ref[fin]), "E4M3: byte values differ from float8_e4m3fn"
+    assert v[0x01] == 2.0 ** -9 and v[0x38] == 1.0 and v[0x7E] == 448.0, "E4M3: special values"
+
+
+def pin_e4m3_decode(lib=None):
+    """The FP8-cache decode at the real dims against numpy float64 softmax over
+    the cache dequantised by PyTorch's float8 widening times the scale."""
+    rng = np.random.default_rng(31)
+    T = 90
+    kv8 = rng.integers(0, 256, size=(T, 576), dtype=np.uint8)
+    kv8[(kv8 & 0x7F) == 0x7F] = 0x30
+    q = workloads.randn_bf16(3, 576, seed=31, stream=1).view(1, 3, 576)
+    vals = _torch_e4m3(kv8)
+    for kv_scale in (1.0, 0.37):
+        out, lse = oracle.decode_e4m3(q, kv8, kv_scale=kv_scale, scale=workloads.SCALE,
+                                      d_pos=np.array([T - 1], np.int32), lib=lib)
+        v = vals * kv_scale
+        s = (_f64(q)[0] @ v.T) * workloads.SCALE
+        m = s.max(axis=1, keepdims=True)
+        w = np.exp(s - m)
+        ref_lse = (m + np.log(w.sum(axis=1, keepdims=True)))[:, 0]
+        ref = (w / w.sum(axis=1, keepdims=True)) @ v[:, :512]
+        _close(out[0], ref, 1e-9 * max(1.0, np.abs(ref).max()), f"E4M3 decode out (scale {kv_scale})")
+        _close(lse[0], ref_lse, 1e-11, f"E4M3 decode lse (scale {kv_scale})")
+
+
 ALL_PINS = [pin_bruteforce_dense, pin_bruteforce_sparse, pin_numpy_reference, pin_uniform_scores,
             pin_single_row, pin_identical_rows, pin_split_invariance, pin_sparse_is_dense,
-            pin_permutation, pin_argmax_limit]
+            pin_permutation, pin_argmax_limit, pin_e4m3_decoding, pin_e4m3_decode]

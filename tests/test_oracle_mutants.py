@@ -14,7 +14,11 @@ MUTANTS = [
     ("no_scale", "s[t] = (lat + rope) * J->scale;", "s[t] = (lat + rope);"),
     ("exp_sign", "l += exp(s[t] - m);", "l += exp(m - s[t]);"),
     ("ctx_off_by_one", "long long ctx = (long long)J->d_pos[b] + 1;", "long long ctx = (long long)J->d_pos[b];"),
-    ("value_shifted", "o[f] += w * widen_bf16(row[f]);", "o[f] += w * widen_bf16(row[J->d_rope + f]);"),
+    ("value_shifted", "o[f] += w * kv_at(J, rows[t], f);", "o[f] += w * kv_at(J, rows[t], J->d_rope + f);"),
+    ("e4m3_exponent_bias", "else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_subnormal_scale", "if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
+    ("e4m3_scale_dropped", "[r * J->row_stride + i]) * J->kv_scale;", "[r * J->row_stride + i]);"),
     ("q_batch_head_transposed", "J->q + ((long long)b * J->heads + h) * D;",
      "J->q + ((long long)h * J->batch + b) * D;"),
     ("mask_inclusive_end", "if (i < 0 || i >= J->cache_len[b]) continue;\n            long long r = base + i;",

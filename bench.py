@@ -149,26 +149,33 @@ class ClockSampler:
 class DenseBench:
     """Dense decode over `copies` distinct caches of T rows (B=1)."""
 
-    def __init__(self, T, H, copies, splits, pdl, seed=0, variant=0):
+    def __init__(self, T, H, copies, splits, pdl, seed=0, variant=0, fp8=False):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
         d = torch.device("cuda")
         self.T, self.H, self.copies = T, H, copies
         x = workloads.dense(1, H, T, seed=seed)
         self.host = x
+        self.kv_scale = 1.0
+        kv0 = x.kv
+        if fp8:
+            # the same draws as an E4M3 cache with one scale (576-byte rows)
+            kv0, self.kv_scale = workloads.to_e4m3(x.kv)
         # copy 0 is the seeded workload; the others are shifted versions (distinct bytes, same distribution)
-        self.kv = [x.kv.to(d)]
+        self.kv = [kv0.to(d)]
         for c in range(1, copies):
             self.kv.append(torch.roll(self.kv[0], shifts=c * 37, dims=0))
         self.q = [x.q.to(d) for _ in range(copies)]
         self.d_pos = x.d_pos.to(d)
         self.out = [torch.empty(1, H, 512, device=d) for _ in range(copies)]
         self.lse = [torch.empty(1, H, device=d) for _ in range(copies)]
-        self.plan = mla.plan(batch=1, heads=H, max_ctx=T, scale=x.scale, splits=splits, pdl=pdl, variant=variant)
+        self.plan = mla.plan(batch=1, heads=H, max_ctx=T, scale=x.scale, splits=splits, pdl=pdl, variant=variant,
+                             kv_fp8=fp8)
         self.scratch = mla.alloc_scratch(self.plan)
-        self.args = [mla.make_args(self.q[c], self.kv[c], self.out[c], self.lse[c], d_pos=self.d_pos)
-                     for c in range(copies)]
-        self.alg_bytes = T * ROW_BYTES + H * 576 * 2 + 4 + H * 512 * 4 + H * 4
+        self.args = [mla.make_args(self.q[c], self.kv[c], self.out[c], self.lse[c], d_pos=self.d_pos,
+                                   kv_scale=self.kv_scale) for c in range(copies)]
+        row_bytes = ROW_BYTES // 2 if fp8 else ROW_BYTES
+        self.alg_bytes = T * row_bytes + H * 576 * 2 + 4 + H * 512 * 4 + H * 4
         self.flops = T * H * FLOP_PER_ROW_HEAD
 
     def call(self, c, stream=None):
@@ -585,6 +592,13 @@ def write_details(args, P):
         us, usp, reps = time_bench(b)
         entry(f"dense_h16_t{T}", b, us, usp, reps)
         del b
+    # the same workloads over an E4M3 cache (576-byte rows, one scale)
+    for T in (8192, 32768, 131072):
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES // 2), args.splits, bool(args.pdl), fp8=True)
+        us, usp, reps = time_bench(b)
+        entry(f"dense_fp8_h16_t{T}", b, us, usp, reps)
+        del b
+    torch.cuda.empty_cache()
     for s in (1, 2, 4, 8, 16, 32, 64, 128):
         b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), s, bool(args.pdl), variant=args.variant)
         us, usp, reps = time_bench(b)
@@ -638,7 +652,11 @@ def ncu_case(args):
     from decode_attention_mla_gb300 import build as mla_build
     mla_build.build()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    if args.ncu_case.startswith("dense_"):
+    if args.ncu_case.startswith("dense_fp8_"):
+        # dense_fp8_t<T>: the E4M3 cache, H = 16
+        T = int(args.ncu_case[len("dense_fp8_t"):])
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES // 2), args.splits, bool(args.pdl), fp8=True)
+    elif args.ncu_case.startswith("dense_"):
         # dense_t<T> (16 heads) or dense_h<H>_t<T>
         fields = dict((f[0], int(f[1:])) for f in args.ncu_case[len("dense_"):].split("_"))
         T, H = fields["t"], fields.get("h", 16)

@@ -37,7 +37,7 @@ class Shape(ctypes.Structure):
                 ("d_rope", ctypes.c_int), ("sparse", ctypes.c_int), ("max_ctx", ctypes.c_int),
                 ("topk", ctypes.c_int), ("scale", ctypes.c_float), ("num_sms", ctypes.c_int),
                 ("splits_override", ctypes.c_int), ("variant", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("stall_test", ctypes.c_int)]
+                ("stall_test", ctypes.c_int), ("kv_fp8", ctypes.c_int)]
 
 
 class Plan(ctypes.Structure):
@@ -60,7 +60,7 @@ class Args(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("kv", ctypes.c_void_p), ("kv_rows", ctypes.c_longlong),
                 ("row_stride", ctypes.c_longlong), ("d_pos", ctypes.c_void_p), ("row_offset", ctypes.c_void_p),
                 ("cache_len", ctypes.c_void_p), ("indices", ctypes.c_void_p), ("out", ctypes.c_void_p),
-                ("lse", ctypes.c_void_p)]
+                ("lse", ctypes.c_void_p), ("kv_scale", ctypes.c_float)]
 
 
 class MLADecodeError(RuntimeError):
@@ -142,14 +142,16 @@ def _stream(stream):
 
 
 def plan(*, batch: int, heads: int, scale: float, max_ctx: int = 0, topk: int = 0, sparse: bool = False,
-         num_sms: int = 0, splits: int = 0, variant: int = 0, pdl: bool = False, stall_test: bool = False) -> Plan:
+         num_sms: int = 0, splits: int = 0, variant: int = 0, pdl: bool = False, stall_test: bool = False,
+         kv_fp8: bool = False) -> Plan:
     """``mla_decode_plan``: derive the split count, grid and scratch layout.
 
     ``num_sms=0`` queries the current CUDA device and prepares the kernels on it
-    (do this before capturing a graph)."""
+    (do this before capturing a graph).  ``kv_fp8``: the cache holds E4M3 bytes
+    (pass the cache's scale as ``kv_scale`` to :func:`make_args` / :func:`forward`)."""
     s = Shape(batch=batch, heads=heads, d_latent=D_LATENT, d_rope=D_ROPE, sparse=int(bool(sparse)),
               max_ctx=max_ctx, topk=topk, scale=scale, num_sms=num_sms, splits_override=splits,
-              variant=variant, pdl=int(bool(pdl)), stall_test=int(bool(stall_test)))
+              variant=variant, pdl=int(bool(pdl)), stall_test=int(bool(stall_test)), kv_fp8=int(bool(kv_fp8)))
     p = Plan()
     _check(lib().mla_decode_plan(ctypes.byref(s), ctypes.byref(p)), "mla_decode_plan")
     return p
@@ -177,14 +179,16 @@ def status_word(p: Plan, scratch) -> int:
 
 
 def make_args(q, kv, out, lse, *, d_pos=None, row_offset=None, cache_len=None, indices=None,
-              kv_rows: int | None = None, row_stride: int | None = None) -> Args:
+              kv_rows: int | None = None, row_stride: int | None = None, kv_scale: float = 1.0) -> Args:
+    """Per-call arguments.  ``kv``: bf16 rows, or E4M3 bytes (uint8 / float8_e4m3fn) for plans made
+    with ``kv_fp8`` (then ``row_stride`` counts bytes and ``kv_scale`` is the cache's scale)."""
     if row_stride is None:
         row_stride = kv.stride(0) if kv.dim() == 2 else D_ROW
     if kv_rows is None:
         kv_rows = kv.shape[0] if kv.dim() == 2 else kv.numel() // row_stride
     return Args(q=_ptr(q), kv=_ptr(kv), kv_rows=int(kv_rows), row_stride=int(row_stride), d_pos=_ptr(d_pos),
                 row_offset=_ptr(row_offset), cache_len=_ptr(cache_len), indices=_ptr(indices), out=_ptr(out),
-                lse=_ptr(lse))
+                lse=_ptr(lse), kv_scale=float(kv_scale))
 
 
 def _scratch_args(scratch):
@@ -227,10 +231,11 @@ def forward_step(p: Plan, q, kv, out, lse, scratch, new_rows, *, d_pos, row_offs
 
 
 def forward(p: Plan, q, kv, out, lse, scratch, *, d_pos=None, row_offset=None, cache_len=None, indices=None,
-            kv_rows=None, row_stride=None, stream=None) -> None:
-    """Partial + combine: ``out[B,H,512]`` and ``lse[B,H]`` (fp32) from bf16 ``q`` and ``kv``."""
+            kv_rows=None, row_stride=None, kv_scale: float = 1.0, stream=None) -> None:
+    """Partial + combine: ``out[B,H,512]`` and ``lse[B,H]`` (fp32) from bf16 ``q`` and ``kv``
+    (bf16 rows, or E4M3 bytes with ``kv_scale`` for ``kv_fp8`` plans)."""
     a = make_args(q, kv, out, lse, d_pos=d_pos, row_offset=row_offset, cache_len=cache_len, indices=indices,
-                  kv_rows=kv_rows, row_stride=row_stride)
+                  kv_rows=kv_rows, row_stride=row_stride, kv_scale=kv_scale)
     forward_args(p, a, scratch, stream)
 
 

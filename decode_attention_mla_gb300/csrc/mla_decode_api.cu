@@ -73,6 +73,22 @@ int encode_bf16_row_chunks(CUtensorMap* map, const void* base, long long rows, l
     return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
 }
 
+// Rank-3 view of E4M3 rows of 576 bytes: {64 bytes, rows, 9 chunks of 64}
+// with strides {row stride, 64 bytes}; a box {64, 32, 9} lands in shared
+// memory unswizzled as [chunk][row][64 bytes].
+int encode_e4m3_row_chunks(CUtensorMap* map, const void* base, long long rows, long long row_stride_bytes) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return MLA_ECUDA;
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(MLA_D_ROW / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride_bytes), 64u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(mla::kStageRows), static_cast<cuuint32_t>(MLA_D_ROW / 64)};
+    const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                           elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
+}
+
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_prepared[kMaxDevices];
 std::mutex g_prepare_mutex;
@@ -141,6 +157,7 @@ int check_shape(const mla_decode_shape* s) {
     if (s->sparse != 0 && s->sparse != 1) return MLA_EINVAL;
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
     if (s->stall_test != 0 && s->stall_test != 1) return MLA_EINVAL;
+    if (s->kv_fp8 != 0 && s->kv_fp8 != 1) return MLA_EINVAL;
     if (s->variant < 0 || s->variant > 4) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
@@ -152,6 +169,8 @@ int check_shape(const mla_decode_shape* s) {
     if (s->variant == kVariantTc32 && (s->sparse || s->heads % 32 != 0)) return MLA_EUNSUPPORTED;
     // 64 heads per CTA: dense decode with a multiple of 64 heads
     if (s->variant == kVariantTc64 && (s->sparse || s->heads % 64 != 0)) return MLA_EUNSUPPORTED;
+    // E4M3 cache: dense decode on the warp-MMA kernel
+    if (s->kv_fp8 && (s->sparse || (s->variant != 0 && s->variant != kVariantWarpMma))) return MLA_EUNSUPPORTED;
     return MLA_OK;
 }
 
@@ -175,7 +194,13 @@ int check_plan(const mla_decode_plan_t* pl) {
 int check_args(const mla_decode_plan_t* pl, const mla_decode_args* a) {
     if (!a || !a->q || !a->kv || !a->out || !a->lse) return MLA_EINVAL;
     if (a->kv_rows < 1 || a->row_stride < MLA_D_ROW) return MLA_EINVAL;
-    if (a->row_stride % 8 != 0) return MLA_EALIGN;
+    if (pl->shape.kv_fp8) {
+        // row stride in bytes, 16-byte aligned rows; a finite positive scale
+        if (a->row_stride % 16 != 0) return MLA_EALIGN;
+        if (!(a->kv_scale > 0.f) || !std::isfinite(a->kv_scale)) return MLA_EINVAL;
+    } else if (a->row_stride % 8 != 0) {
+        return MLA_EALIGN;
+    }
     if (misaligned(a->q, 16) || misaligned(a->kv, 16) || misaligned(a->out, 16) || misaligned(a->lse, 4))
         return MLA_EALIGN;
     if (a->row_offset && misaligned(a->row_offset, 8)) return MLA_EALIGN;
@@ -236,6 +261,14 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.n_items = pl->shape.batch * pl->n_head_groups * pl->splits;
     p.granule = variant_granule(pl->variant);
     p.scale_log2 = pl->shape.scale * 1.4426950408889634f;
+    p.kv_fp8 = pl->shape.kv_fp8;
+    p.v_scale = 1.f;
+    if (pl->shape.kv_fp8) {
+        // every value is e4m3(byte) * kv_scale: the scores carry it through the
+        // score scale, the partial multiplies O by it
+        p.scale_log2 *= a->kv_scale;
+        p.v_scale = a->kv_scale;
+    }
     p.o_part = reinterpret_cast<float*>(base + pl->o_part_offset);
     p.lse_part = reinterpret_cast<float*>(base + pl->lse_part_offset);
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
@@ -256,11 +289,14 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
         return launch_status(mla::launch_partial_tc(maps, p, hg, grid, pl->shape.pdl != 0, st));
     }
     // warp-MMA kernel: the query tile by TMA; dense cache rows by one TMA box
-    // per 32-row slot, sparse rows by per-row bulk copies
+    // per 32-row slot (E4M3 rows: one box of bytes, widened in shared memory),
+    // sparse rows by per-row bulk copies
     mla::TcMaps maps{};
     if (!pl->shape.sparse) {
         if (a->kv_rows > 0x7fffff00LL) return MLA_EUNSUPPORTED;
-        rc = encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kStageRows, MLA_D_ROW / 64);
+        rc = pl->shape.kv_fp8
+                 ? encode_e4m3_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride)
+                 : encode_bf16_row_chunks(&maps.kv, a->kv, a->kv_rows, a->row_stride, mla::kStageRows, MLA_D_ROW / 64);
         if (rc != MLA_OK) return rc;
     }
     rc = encode_bf16_row_chunks(&maps.q, a->q, static_cast<long long>(pl->shape.batch) * pl->shape.heads, MLA_D_ROW,
@@ -344,8 +380,8 @@ long long rows_per_item(long long rows, int batch, int heads, long long grid_cap
     const long long S = derive_splits(rows, pairs, grid_cap, variant);
     return mla::slice_entries(rows, static_cast<int>(S), variant_granule(variant));
 }
-int auto_variant(bool sparse, int batch, int heads, long long rows, long long grid_cap) {
-    if (sparse || heads == mla::kHeadGroup) return kVariantWarpMma;
+int auto_variant(bool sparse, bool fp8, int batch, int heads, long long rows, long long grid_cap) {
+    if (sparse || fp8 || heads == mla::kHeadGroup) return kVariantWarpMma;
     if (rows_per_item(rows, batch, heads, grid_cap, kVariantWarpMma) <= kMmaMaxRowsPerItemWide) return kVariantWarpMma;
     return heads % 64 == 0 ? kVariantTc64 : kVariantTc32;
 }
@@ -379,7 +415,8 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
 
     const long long rows = s.sparse ? s.topk : s.max_ctx;
     const long long grid_cap = static_cast<long long>(kCtasPerSm) * sms;
-    pl.variant = s.variant != 0 ? s.variant : auto_variant(s.sparse != 0, s.batch, s.heads, rows, grid_cap);
+    pl.variant =
+        s.variant != 0 ? s.variant : auto_variant(s.sparse != 0, s.kv_fp8 != 0, s.batch, s.heads, rows, grid_cap);
     pl.head_group = variant_head_group(pl.variant);
     pl.n_head_groups = s.heads / pl.head_group;
     const long long best_s =
@@ -395,7 +432,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     const bool tc = variant_is_tc(pl.variant);
     pl.block = tc ? mla::partial_tc_block_threads(pl.head_group) : mla::partial_mma_block_threads();
     pl.smem_bytes = static_cast<int>(tc ? mla::partial_tc_smem_bytes(pl.head_group)
-                                                              : mla::partial_mma_smem_bytes());
+                                        : mla::partial_mma_smem_bytes(s.kv_fp8 != 0));
     pl.combine_grid_x = mla::combine_grid_rows(s.batch * s.heads, pl.splits);
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
     pl.combine_block = mla::combine_block_threads();
@@ -430,7 +467,7 @@ int mla_decode_forward_step(const mla_decode_plan_t* plan, const mla_decode_args
                             size_t scratch_bytes, const void* new_rows, int advance, void* stream) {
     int rc = check_plan(plan);
     if (rc != MLA_OK) return rc;
-    if (plan->shape.sparse) return MLA_EUNSUPPORTED;
+    if (plan->shape.sparse || plan->shape.kv_fp8) return MLA_EUNSUPPORTED;
     if (!new_rows || (advance != 0 && advance != 1)) return MLA_EINVAL;
     if (misaligned(new_rows, 16)) return MLA_EALIGN;
     const StepUpdate up{static_cast<const uint16_t*>(new_rows), advance};

@@ -45,6 +45,11 @@ struct PartialParams {
     // fused append (dense): bf16 [B][576], row b taking the place of cache row
     // d_pos[b] of request b in the CTA's staged tile; null = read the cache only
     const uint16_t* new_rows;
+    // E4M3 cache (dense, warp-MMA kernel): kv holds bytes and every value is
+    // e4m3(byte) * v_scale; scale_log2 already carries v_scale, and the partial
+    // multiplies O by it.  v_scale = 1 for bf16 caches.
+    int kv_fp8;
+    float v_scale;
 };
 
 struct CombineParams {
@@ -102,7 +107,7 @@ struct TcMaps {
 
 // Launch helpers (each returns the cudaError_t of the launch).
 cudaError_t partial_mma_prepare(int device);
-size_t partial_mma_smem_bytes();
+size_t partial_mma_smem_bytes(bool fp8 = false);
 int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
 cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);

@@ -47,6 +47,7 @@
 // its copies before it exits.
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "device_utils.cuh"
 #include "mla_decode.h"
@@ -98,14 +99,30 @@ constexpr int kStagePitch = kDLatent + 4;                  // floats per staged 
 constexpr int kBarPair0 = 1;
 constexpr int kBarGroup0 = 5;
 constexpr int kBarMma = 7;
+constexpr int kBarConvert = 8;                             // E4M3 cache: the converting producer warps
 constexpr int kMmaThreads = kComputeWarps * 32;
+// E4M3 cache: a slot's bytes, [9 chunks][32 rows][64 bytes] (one TMA box,
+// unswizzled), land in the upper part of the slot and are widened to f16 in
+// place
+constexpr int kFp8ChunkBytes = kStageRows * 64;            // 2048
+constexpr int kFp8SlotBytes = kChunks * kFp8ChunkBytes;    // 18,432
+constexpr int kFp8StageOffset = kDenseSlotBytes - kFp8SlotBytes;   // 18,432: the slot's upper half
+constexpr int kFp8DirectChunks = 4;                        // chunks 0-3 widen straight into [0, 16 KB)
+constexpr int kConvertThreads = 128;                       // the producer warpgroup
+constexpr int kConvertUnits = kFp8SlotBytes / 8;           // 8 E4M3 bytes -> 16 f16 bytes each
+constexpr float kFp8PScale = 128.f;                        // P enters the f16 products as P * 2^7
 
 static_assert(kDenseSlotBytes % 1024 == 0, "swizzled slots stay 1024-byte aligned");
 static_assert(kKHalf == 2 * kChunks && kGroupWarps == 2 * (kStageRows / 16),
               "a group's warp pairs cover a slot 16 rows each, a contraction half per warp");
 static_assert(kHeadGroup * kStagePitch * 4 <= kDenseSlotBytes, "group 1's O fits in one slot");
 
-template <bool kDense>
+struct Fp8Stage {
+    uint64_t full[kSlots];                                 // a slot's E4M3 bytes landed (upper part of the slot)
+};
+struct NoFp8Stage {};
+
+template <bool kDense, bool kFp8 = false>
 struct __align__(1024) SharedStorage {
     static constexpr int kSlotBytes = kDense ? kDenseSlotBytes : kSparseSlotBytes;
     uint8_t q[kChunks * kQChunkBytes];                     // the item's 16 query rows (1024-byte aligned)
@@ -124,6 +141,7 @@ struct __align__(1024) SharedStorage {
     uint64_t stall_bar;                                    // test hook: a barrier nothing arrives at
     uint64_t patch_bar;                                    // fused append: the slot holding the new row landed
     int abort_flag;
+    std::conditional_t<kFp8, Fp8Stage, NoFp8Stage> fp8;    // dense E4M3 cache only
 };
 
 // Byte offset of byte b of row r in a 128-byte-swizzled chunk-major tile whose
@@ -159,8 +177,8 @@ __host__ __device__ constexpr uint32_t row_pitch() {
     return kDense ? 128 : kSmemRow;
 }
 
-template <bool kDense>
-__device__ __forceinline__ void raise_device_error(SharedStorage<kDense>& sh, int* status) {
+template <class S>
+__device__ __forceinline__ void raise_device_error(S& sh, int* status) {
     sh.abort_flag = 1;
     if (status) atomicCAS(status, 0, static_cast<int>(MLA_EDEVICE));
 }
@@ -231,9 +249,8 @@ __device__ __forceinline__ int first_key(const PartialParams& p) {
     return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
 }
 
-template <bool kDense>
-__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh,
-                                       int key, int lane) {
+template <class S>
+__device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& p, S& sh, int key, int lane) {
     if (lane == 0) {
         const int b = key / p.n_groups;
         const int hg = key - b * p.n_groups;
@@ -445,6 +462,196 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     }
 }
 
+// ---- dense E4M3 cache ------------------------------------------------------
+// A slot's E4M3 bytes (one TMA box {64 bytes, 32 rows, 9 chunks}, no
+// swizzle, 18,432 bytes) land in the upper half of the slot they become, so
+// the ring is as deep as for bf16 rows (four slots in flight), and the four
+// producer warps widen them in place to f16 (one cvt per pair, exact: an
+// E4M3 value has 4 significant bits and an exponent inside f16's normal
+// range; NaN stays NaN), in the 128-byte-swizzled chunk-major layout a bf16
+// cache lands in.  The MMA warps take the f16 forms of their products (query
+// fragments rounded to f16 once per tile, P as f16 pairs).  In place: the f16
+// chunks 0-3 fill [0, 16 KB), below the staged bytes, and are written at
+// once; chunks 4-8 overwrite staged bytes, so every thread first reads its
+// share of them into registers, and writes only after a barrier.  One thread
+// also issues the loads (a slot's load as soon as the MMA warps free it,
+// checked without waiting between slots, waited for only when the slot about
+// to be widened has not been issued yet) and prefetches six slots ahead into
+// L2.  Rows before the cache or past its end read as zero bytes (the TMA
+// fill), i.e. 0.0.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+    return h2;
+}
+
+// The (item, slot) sequence of this CTA, walked ahead of the conversions by
+// the thread that issues the loads and L2 prefetches.
+struct SlotCursor {
+    int item, st, n_slots;
+    long long row0;                               // first cache row of the item's slice
+    bool valid;
+};
+__device__ __forceinline__ void slot_cursor_next_item(const PartialParams& p, SlotCursor& c, int from) {
+    for (int i = from; i < p.n_items; i += gridDim.x) {
+        const Item it = decode_item(p, i);
+        if (it.n_slots > 0) {
+            c.item = i;
+            c.st = 0;
+            c.n_slots = it.n_slots;
+            c.row0 = it.base + it.e0;
+            c.valid = true;
+            return;
+        }
+    }
+    c.valid = false;
+}
+__device__ __forceinline__ void slot_cursor_step(const PartialParams& p, SlotCursor& c) {
+    if (++c.st == c.n_slots) slot_cursor_next_item(p, c, c.item + static_cast<int>(gridDim.x));
+}
+__device__ __forceinline__ int slot_cursor_row(const SlotCursor& c) {
+    long long y = c.row0 + static_cast<long long>(c.st) * kStageRows;
+    if (y < -2 * kStageRows) y = -2 * kStageRows;   // a box wholly before row 0 either way
+    return static_cast<int>(y);
+}
+
+// Unit i of a slot (8 E4M3 bytes -> 16 f16 bytes): chunk c, row r, 8-byte group u.
+__device__ __forceinline__ uint32_t fp8_src(uint32_t slot, int i) {
+    return slot + kFp8StageOffset + (i >> 8) * kFp8ChunkBytes + ((i >> 3) & (kStageRows - 1)) * 64 + (i & 7) * 8;
+}
+__device__ __forceinline__ uint32_t fp8_dst(uint32_t slot, int i) {
+    const int r = (i >> 3) & (kStageRows - 1);
+    return slot + (i >> 8) * kDenseChunkBytes + r * 128 + (((i & 7) ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ void fp8_store(uint32_t dst, uint32_t w0, uint32_t w1) {
+    st_shared_v4(dst, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1),
+                 e4m3x2_to_f16x2(w1 >> 16));
+}
+
+__device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, SharedStorage<true, true>& sh, int wp,
+                             int lane) {
+    constexpr int kDirectUnits = kFp8DirectChunks * 256;             // units of chunks 0-3
+    constexpr int kHeldPerThread = (kConvertUnits - kDirectUnits) / kConvertThreads;   // 10
+    static_assert(kConvertUnits % 256 == 0 && kStageRows == 32, "unit decomposition: 256 units per chunk");
+    static_assert((kConvertUnits - kDirectUnits) % kConvertThreads == 0 && kDirectUnits % kConvertThreads == 0,
+                  "whole units per thread");
+    static_assert(kFp8DirectChunks * kDenseChunkBytes <= kFp8StageOffset, "chunks 0-3 lie below the staged bytes");
+    const uint64_t policy = l2_policy_evict_first();
+    const int ct = wp * 32 + lane;                // converting thread (all four producer warps)
+    const bool issuer = ct == 0;                  // issues the loads, prefetches ahead, loads the query tiles
+    constexpr int kPrefetchAhead = 6;             // slots of L2 prefetch ahead of the loads
+    volatile int never = 0;
+    int q_key = first_key(p);
+    int q_loads = 0;
+    int issued = 0;                               // slot loads issued (issuer)
+    SlotCursor ic{}, pc{};                        // issue and prefetch cursors (issuer)
+    if (wp == 0) {
+        load_q(maps, p, sh, q_key, lane);
+        q_loads = 1;
+    }
+    bool ok = !(wp == 0 && p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
+    ok = !named_barrier_or(kBarConvert, kConvertThreads, !ok);
+    if (issuer && ok) {
+        slot_cursor_next_item(p, ic, blockIdx.x);
+        pc = ic;
+        for (int k = 0; k < kPrefetchAhead && pc.valid; ++k) {
+            tma_prefetch_3d(&maps.kv, 0, slot_cursor_row(pc), 0);
+            slot_cursor_step(p, pc);
+        }
+    }
+    int stage = 0;
+    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        const Item it = decode_item(p, item);
+        if (it.n_slots == 0) continue;
+        bool qw = true;                            // the query tile's buffer was free (warp 0)
+        if (wp == 0) {
+            const int key = it.b * p.n_groups + it.hg;
+            if (key != q_key) {
+                qw = mbar_wait_bounded(&sh.q_empty, (q_loads - 1) & 1, &sh.abort_flag);
+                if (qw) load_q(maps, p, sh, key, lane);
+                q_key = key;
+                ++q_loads;
+            }
+        }
+        for (int st = 0; st < it.n_slots; ++st, ++stage) {
+            const int slot = stage % kSlots;
+            // loads: this slot's for certain (waiting for its previous use to be
+            // released), later ones while their slots are already free
+            bool w = st > 0 || qw;
+            if (issuer) {
+                while (w && ic.valid && issued < stage + kSlots) {
+                    const int js = issued % kSlots;
+                    if (issued >= kSlots) {
+                        const uint32_t par = ((issued / kSlots) - 1) & 1;
+                        if (issued > stage) {
+                            if (!mbar_test(&sh.empty[js], par)) break;
+                        } else if (!mbar_wait_bounded(&sh.empty[js], par, &sh.abort_flag)) {
+                            w = false;
+                            break;
+                        }
+                    }
+                    mbar_arrive_expect_tx(&sh.fp8.full[js], kFp8SlotBytes);
+                    tma_load_3d(sh.kv[js] + kFp8StageOffset, &maps.kv, 0, slot_cursor_row(ic), 0, &sh.fp8.full[js],
+                                policy);
+                    slot_cursor_step(p, ic);
+                    ++issued;
+                    if (pc.valid) {
+                        tma_prefetch_3d(&maps.kv, 0, slot_cursor_row(pc), 0);
+                        slot_cursor_step(p, pc);
+                    }
+                }
+            }
+            w = w && mbar_wait_bounded(&sh.fp8.full[slot], (stage / kSlots) & 1, &sh.abort_flag);
+            if (named_barrier_or(kBarConvert, kConvertThreads, !w)) {   // (the threads decide together)
+                ok = false;
+                break;
+            }
+            const uint32_t sb = smem_u32(sh.kv[slot]);
+            // chunks 0-3: straight into the lower part, which holds no staged
+            // bytes (all loads first: the widening is bound by shared-memory
+            // latency, not by its arithmetic)
+            {
+                constexpr int kDirectPerThread = kDirectUnits / kConvertThreads;   // 8
+                uint32_t d[kDirectPerThread][2];
+#pragma unroll
+                for (int k = 0; k < kDirectPerThread; ++k)
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                 : "=r"(d[k][0]), "=r"(d[k][1])
+                                 : "r"(fp8_src(sb, ct + k * kConvertThreads)));
+#pragma unroll
+                for (int k = 0; k < kDirectPerThread; ++k)
+                    fp8_store(fp8_dst(sb, ct + k * kConvertThreads), d[k][0], d[k][1]);
+            }
+            // chunks 4-8: read this thread's units before anything overwrites them
+            uint32_t held[kHeldPerThread][2];
+#pragma unroll
+            for (int k = 0; k < kHeldPerThread; ++k) {
+                const int i = kDirectUnits + ct + k * kConvertThreads;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(held[k][0]), "=r"(held[k][1]) : "r"(fp8_src(sb, i)));
+            }
+            named_barrier_sync(kBarConvert, kConvertThreads);   // every staged byte has been read
+#pragma unroll
+            for (int k = 0; k < kHeldPerThread; ++k) {
+                const int i = kDirectUnits + ct + k * kConvertThreads;
+                fp8_store(fp8_dst(sb, i), held[k][0], held[k][1]);
+            }
+            named_barrier_sync(kBarConvert, kConvertThreads);   // the slot is complete
+            if (issuer) mbar_arrive(&sh.full[slot][0]);
+        }
+    }
+    if (!ok && lane == 0) raise_device_error(sh, p.status);
+    // never retire with copies in flight: the issuer waits for the last phase
+    // armed on each slot, and for the query tile
+    if (issuer) {
+        for (int s = 0; s < kSlots && s < issued; ++s) {
+            const int last_use = (issued - 1 - s) / kSlots;
+            if (!mbar_wait_bounded(&sh.fp8.full[s], last_use & 1, &never)) raise_device_error(sh, p.status);
+        }
+        if (q_loads > 0 && !mbar_wait_bounded(&sh.q_full, (q_loads - 1) & 1, &never))
+            raise_device_error(sh, p.status);
+    }
+}
+
 // ============================== MMA warps =================================
 // Two groups of four warps (one warp of each on every SM sub-partition) take
 // alternate 32-row slots of an item: group 0 slots 0, 2, 4, ..., group 1
@@ -462,7 +669,7 @@ __device__ __forceinline__ float4 as_float4(const float (&v)[4]) { return make_f
 // This warp's half of the score contraction for its pair's 16 rows of a slot
 // (two 8-row tiles), in two accumulation chains per tile (even / odd k-steps)
 // added once; zeros when `run` is false.
-template <bool kDense>
+template <bool kDense, bool kF16 = false>
 __device__ __forceinline__ void qk_scores(float (&acc)[2][4], const uint32_t (&qa)[kKHalf][4], uint32_t sbase,
                                           const uint32_t (&qk_off)[2], bool run) {
 #pragma unroll
@@ -478,11 +685,11 @@ __device__ __forceinline__ void qk_scores(float (&acc)[2][4], const uint32_t (&q
         uint32_t bf[4];
         ldmatrix_x4(bf, ((kk & 1) ? a1 : a0) + (kk >> 1) * qk_chunk_stride<kDense>());
         if (kk & 1) {
-            mma_bf16_16816(acc2[0], qa[kk], bf[0], bf[1]);
-            mma_bf16_16816(acc2[1], qa[kk], bf[2], bf[3]);
+            mma_16816<kF16>(acc2[0], qa[kk], bf[0], bf[1]);
+            mma_16816<kF16>(acc2[1], qa[kk], bf[2], bf[3]);
         } else {
-            mma_bf16_16816(acc[0], qa[kk], bf[0], bf[1]);
-            mma_bf16_16816(acc[1], qa[kk], bf[2], bf[3]);
+            mma_16816<kF16>(acc[0], qa[kk], bf[0], bf[1]);
+            mma_16816<kF16>(acc[1], qa[kk], bf[2], bf[3]);
         }
     }
 #pragma unroll
@@ -495,7 +702,7 @@ __device__ __forceinline__ void qk_scores(float (&acc)[2][4], const uint32_t (&q
 // P as the A fragments of the group's published hi / lo pairs, V by
 // transposing ldmatrix, in two halves of eight n-tiles (low-part MMAs first,
 // then the high parts: each accumulator's two MMAs eight instructions apart).
-template <bool kDense>
+template <bool kDense, bool kF16 = false>
 __device__ __forceinline__ void pv_kstep(float (&o)[kPVTiles][4], const uint4* pt, int kp, uint32_t vbase,
                                          const uint32_t (&pv_off)[kPVTiles / 2], int v_hi, int tq, int lane) {
     const uint4 t0 = pt[(2 * kp) * 32 + lane];
@@ -523,20 +730,20 @@ __device__ __forceinline__ void pv_kstep(float (&o)[kPVTiles][4], const uint4* p
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            mma_bf16_16816(o[8 * hh + 2 * i], a_lo, v[i][0], v[i][1]);
-            mma_bf16_16816(o[8 * hh + 2 * i + 1], a_lo, v[i][2], v[i][3]);
+            mma_16816<kF16>(o[8 * hh + 2 * i], a_lo, v[i][0], v[i][1]);
+            mma_16816<kF16>(o[8 * hh + 2 * i + 1], a_lo, v[i][2], v[i][3]);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            mma_bf16_16816(o[8 * hh + 2 * i], a_hi, v[i][0], v[i][1]);
-            mma_bf16_16816(o[8 * hh + 2 * i + 1], a_hi, v[i][2], v[i][3]);
+            mma_16816<kF16>(o[8 * hh + 2 * i], a_hi, v[i][0], v[i][1]);
+            mma_16816<kF16>(o[8 * hh + 2 * i + 1], a_hi, v[i][2], v[i][3]);
         }
     }
 }
 
-template <bool kDense>
-__device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int w, int lane) {
-    constexpr uint32_t kSlotBytes = SharedStorage<kDense>::kSlotBytes;
+template <bool kDense, bool kFp8 = false>
+__device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh, int w, int lane) {
+    constexpr uint32_t kSlotBytes = SharedStorage<kDense, kFp8>::kSlotBytes;
     const int g = lane >> 2;
     const int tq = lane & 3;
     const int grp = w / kGroupWarps;        // group: the item's slots grp, grp + 2, ...
@@ -600,6 +807,13 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                     ldmatrix_x4(qa[kk], q_base + sw_off(lrow + ((lmat & 1) << 3),
                                                          (4 * (kk >> 1) + 2 * kh + (kk & 1)) * 32 + ((lmat >> 1) << 4),
                                                          kQChunkBytes));
+                if constexpr (kFp8) {
+                    // the E4M3 path multiplies in f16: the query fragments once per tile
+#pragma unroll
+                    for (int kk = 0; kk < kKHalf; ++kk)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) qa[kk][r] = bf16x2_to_f16x2(qa[kk][r]);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.q_empty);
                 q_in_regs = true;
@@ -633,7 +847,7 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
 
             // ---- scores of this warp's 8-row tile: two contraction halves ------
             float acc[2][4];
-            qk_scores<kDense>(acc, qa, sbase, qk_off, !failed);
+            qk_scores<kDense, kFp8>(acc, qa, sbase, qk_off, !failed);
             sh.red[grp][pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
             named_barrier_sync(bar_pair, 64);
             const float4 other = sh.red[grp][pr][kh][lane];
@@ -667,8 +881,15 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 pv[2] = ex2_approx(sc[2] - ref1);
                 pv[3] = ex2_approx(sc[3] - ref1);
                 uint4 pk;
-                split_bf16x2(pv[0], pv[1], pk.x, pk.z);
-                split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                if constexpr (kFp8) {
+                    // f16 pairs of P * 2^7 (small probabilities stay clear of f16
+                    // subnormals; the epilogue takes the 2^-7 back)
+                    split_f16x2(pv[0] * kFp8PScale, pv[1] * kFp8PScale, pk.x, pk.z);
+                    split_f16x2(pv[2] * kFp8PScale, pv[3] * kFp8PScale, pk.y, pk.w);
+                } else {
+                    split_bf16x2(pv[0], pv[1], pk.x, pk.z);
+                    split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                }
                 sh.p[grp][pbuf][my_tile][lane] = pk;
                 const bool over = mx0 > m_ref[0] + kRescaleThreshold || mx1 > m_ref[1] + kRescaleThreshold;
                 need = named_barrier_or(bar_group, kGroupThreads, over || failed);
@@ -715,8 +936,15 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 pv[2] = ex2_approx(sc[2] - ref1);
                 pv[3] = ex2_approx(sc[3] - ref1);
                 uint4 pk;
-                split_bf16x2(pv[0], pv[1], pk.x, pk.z);
-                split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                if constexpr (kFp8) {
+                    // f16 pairs of P * 2^7 (small probabilities stay clear of f16
+                    // subnormals; the epilogue takes the 2^-7 back)
+                    split_f16x2(pv[0] * kFp8PScale, pv[1] * kFp8PScale, pk.x, pk.z);
+                    split_f16x2(pv[2] * kFp8PScale, pv[3] * kFp8PScale, pk.y, pk.w);
+                } else {
+                    split_bf16x2(pv[0], pv[1], pk.x, pk.z);
+                    split_bf16x2(pv[2], pv[3], pk.y, pk.w);
+                }
                 sh.p[grp][pbuf][my_tile][lane] = pk;
                 named_barrier_sync(bar_group, kGroupThreads);
             }
@@ -725,8 +953,8 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
 
             // ---- O[:, own 128 features] += P . V over the slot's 32 rows --------
             const uint4* pt = &sh.p[grp][pbuf][0][0];
-            pv_kstep<kDense>(o, pt, 0, sbase, pv_off, v_hi, tq, lane);
-            pv_kstep<kDense>(o, pt, 1, sbase + 16 * row_pitch<kDense>(), pv_off, v_hi, tq, lane);
+            pv_kstep<kDense, kFp8>(o, pt, 0, sbase, pv_off, v_hi, tq, lane);
+            pv_kstep<kDense, kFp8>(o, pt, 1, sbase + 16 * row_pitch<kDense>(), pv_off, v_hi, tq, lane);
             __syncwarp();
             // group 1 keeps its last slot of the item: its O is staged there
             const bool keep = grp == 1 && k + 1 == my_slots;
@@ -761,8 +989,10 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
         if (it.n_slots == 1) {
             // one slot: group 0 alone attended rows
             if (grp == 0) {
-                const float inv0 = L0 > 0.f ? rcp_approx(L0) : 0.f;
-                const float inv1 = L1 > 0.f ? rcp_approx(L1) : 0.f;
+                // (v_scale: the E4M3 cache's scale, 1 for bf16; oscale adds the 2^-7 of P)
+                const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
+                const float inv0 = L0 > 0.f ? rcp_approx(L0) * oscale : 0.f;
+                const float inv1 = L1 > 0.f ? rcp_approx(L1) * oscale : 0.f;
 #pragma unroll
                 for (int nt = 0; nt < kPVTiles; ++nt) {
                     *reinterpret_cast<float2*>(op0 + 8 * nt) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
@@ -807,8 +1037,9 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
                 const float s1b = m1b == -INFINITY ? 0.f : ex2_approx(m1b - mb);
                 const float La = L0 * s0a + sh.merge_l[g] * s1a;
                 const float Lb = L1 * s0b + sh.merge_l[g + 8] * s1b;
-                const float inva = La > 0.f ? rcp_approx(La) : 0.f;
-                const float invb = Lb > 0.f ? rcp_approx(Lb) : 0.f;
+                const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
+                const float inva = La > 0.f ? rcp_approx(La) * oscale : 0.f;
+                const float invb = Lb > 0.f ? rcp_approx(Lb) * oscale : 0.f;
                 const float c0a = s0a * inva, c1a = s1a * inva, c0b = s0b * invb, c1b = s1b * invb;
 #pragma unroll
                 for (int nt = 0; nt < kPVTiles; ++nt) {
@@ -835,11 +1066,11 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense>& sh, int 
     if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
 }
 
-template <bool kDense>
+template <bool kDense, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __grid_constant__ TcMaps maps,
                                                                        const PartialParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SharedStorage<kDense>& sh = *reinterpret_cast<SharedStorage<kDense>*>(
+    SharedStorage<kDense, kFp8>& sh = *reinterpret_cast<SharedStorage<kDense, kFp8>*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -852,6 +1083,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         mbar_init(&sh.q_empty, kComputeWarps);
         mbar_init(&sh.stall_bar, 1);
         mbar_init(&sh.patch_bar, 1);
+        if constexpr (kFp8) {
+            for (int i = 0; i < kSlots; ++i) mbar_init(&sh.fp8.full[i], 1);
+        }
         sh.abort_flag = 0;
         mbar_init_fence();
     }
@@ -871,7 +1105,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
             if (warp == kProducerWarp + 1 && lane == 0) prefetch_first_slots(maps, p);
         }
         if (warp == kProducerWarp + 2 && lane == 0) prefetch_first_inputs(maps, p);
-        if (warp == kProducerWarp || !kDense) {
+        if constexpr (kFp8) {
+            // all four warps widen the E4M3 rows; one thread also stages them
+            grid_dependency_wait();
+            allow_dependent_launch();
+            producer_fp8(maps, p, sh, warp - kProducerWarp, lane);
+        } else if (warp == kProducerWarp || !kDense) {
             grid_dependency_wait();
             allow_dependent_launch();
             producer<kDense>(maps, p, sh, warp - kProducerWarp, lane);
@@ -880,38 +1119,43 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         warpgroup_regs_increase<kMmaRegs>();
         grid_dependency_wait();
         allow_dependent_launch();
-        consumer<kDense>(p, sh, warp, lane);
+        consumer<kDense, kFp8>(p, sh, warp, lane);
     }
 }
 
-template <bool kDense>
+template <bool kDense, bool kFp8 = false>
 size_t smem_bytes() {
-    return sizeof(SharedStorage<kDense>) + 1024;
+    return sizeof(SharedStorage<kDense, kFp8>) + 1024;
 }
 static_assert(sizeof(SharedStorage<true>) + 1024 <= 227 * 1024, "dense shared memory");
 static_assert(sizeof(SharedStorage<false>) + 1024 <= 227 * 1024, "sparse shared memory");
+static_assert(sizeof(SharedStorage<true, true>) + 1024 <= 227 * 1024, "E4M3 dense shared memory");
 
 }  // namespace
 
-size_t partial_mma_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
+size_t partial_mma_smem_bytes(bool fp8) {
+    if (fp8) return smem_bytes<true, true>();
+    return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>();
+}
 int partial_mma_block_threads() { return kThreads; }
 
-template <bool kDense>
+template <bool kDense, bool kFp8 = false>
 cudaError_t prepare_one() {
     // the register split assumes kLaunchRegs per thread at launch: with fewer,
     // the MMA warpgroups' increase could never be granted
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, mla_partial_mma_kernel<kDense>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, mla_partial_mma_kernel<kDense, kFp8>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(mla_partial_mma_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_bytes<kDense>()));
+    return cudaFuncSetAttribute(mla_partial_mma_kernel<kDense, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes<kDense, kFp8>()));
 }
 
 cudaError_t partial_mma_prepare(int /*device*/) {
     cudaError_t e = prepare_one<true>();
-    if (e != cudaSuccess) return e;
-    return prepare_one<false>();
+    if (e == cudaSuccess) e = prepare_one<false>();
+    if (e == cudaSuccess) e = prepare_one<true, true>();
+    return e;
 }
 
 cudaError_t partial_mma_occupancy(int* ctas_per_sm) {
@@ -924,7 +1168,7 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = p.sparse ? smem_bytes<false>() : smem_bytes<true>();
+    cfg.dynamicSmemBytes = p.sparse ? smem_bytes<false>() : p.kv_fp8 ? smem_bytes<true, true>() : smem_bytes<true>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -932,6 +1176,7 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     if (p.sparse) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<false>, maps, p);
+    if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, true>, maps, p);
     return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true>, maps, p);
 }
 

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 2
+#define MLA_DECODE_ABI_VERSION 3
 #define MLA_D_LATENT 512
 #define MLA_D_ROPE 64
 #define MLA_D_ROW 576        /* elements per cache row */
@@ -67,7 +67,7 @@ typedef enum {
                                or a dense cache of 2^31 rows or more: TMA row coordinates
                                are 32-bit) */
     MLA_ESCRATCH = -3,      /* scratch missing, misaligned or smaller than plan->scratch_bytes */
-    MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 */
+    MLA_EALIGN = -4,        /* q, kv, out or lse misaligned, or row stride not a multiple of 8 (16 bytes for E4M3) */
     MLA_ECUDA = -5,         /* the CUDA runtime reported an error for a launch or query */
     MLA_EDEVICE = -6,       /* a kernel's bounded wait ran out (see the scratch status word) */
     MLA_ENOTREADY = -7,     /* kernels not prepared on this device and the stream is capturing */
@@ -101,6 +101,9 @@ typedef struct {
                              path runs for real: the CTA aborts, drains its copies and MMAs,
                              frees its tensor memory and leaves MLA_EDEVICE in the status word;
                              the outputs of that call are undefined, the context stays usable */
+    int kv_fp8;           /* 0 = bf16 cache rows (576 x 2 bytes); 1 = OCP FP8 E4M3 cache rows (576
+                             bytes), value = e4m3(byte) * args.kv_scale: dense decode on the
+                             warp-MMA kernel (variant 0 or 1; otherwise MLA_EUNSUPPORTED) */
 } mla_decode_shape;
 
 /* Launch plan (plain data; copy freely).  The plan is the capture key of a
@@ -138,6 +141,9 @@ typedef struct {
     const int *indices;          /* (device) sparse: int32 [B][topk] request-local row ids */
     float *out;                  /* (device) fp32 [B][H][512], 16-byte aligned */
     float *lse;                  /* (device) fp32 [B][H], natural log; -inf if no row is attended */
+    float kv_scale;              /* E4M3 caches (shape.kv_fp8 = 1): the cache's one scale, finite and > 0;
+                                    kv then holds bytes, row_stride counts bytes (>= 576, a multiple
+                                    of 16); ignored for bf16 caches */
 } mla_decode_args;
 
 /* Version of this ABI (MLA_DECODE_ABI_VERSION). */

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     L = ctypes.CDLL(mla.LIB_PATH)
     for n in sorted(names):
         assert hasattr(L, n), f"{n} declared but not exported"
-    assert mla.abi_version() == 2
+    assert mla.abi_version() == 3
     assert "scratch" in mla.strerror(mla.ESCRATCH)
 
 
@@ -369,3 +369,31 @@ def test_forward_step_argument_checks():
     bad = mla.Plan.from_buffer_copy(p)
     bad.magic = 0
     assert call(bad, a, rows, 1) == mla.EINVAL
+
+
+def test_fp8_cache_plan_and_argument_checks():
+    """E4M3 caches: dense on the warp-MMA kernel only; the scale and the byte
+    row stride are checked before any launch."""
+    p = _plan(max_ctx=4096, kv_fp8=True)
+    assert p.variant == 1 and p.shape.kv_fp8 == 1
+    assert 0 < p.smem_bytes <= 227 * 1024
+    assert _plan(heads=128, max_ctx=131072, kv_fp8=True).variant == 1   # the warp-MMA kernel at any width
+    L = mla.lib()
+    s = mla.Shape(batch=1, heads=16, d_latent=512, d_rope=64, sparse=0, max_ctx=64, topk=0, scale=SCALE,
+                  num_sms=152, splits_override=0, variant=0, pdl=0, stall_test=0, kv_fp8=2)
+    out = mla.Plan()
+    assert L.mla_decode_plan(ctypes.byref(s), ctypes.byref(out)) == mla.EINVAL
+    for kw, rc in [(dict(sparse=1, topk=64), mla.EUNSUPPORTED), (dict(variant=2), mla.EUNSUPPORTED),
+                   (dict(variant=4, heads=64), mla.EUNSUPPORTED)]:
+        s = mla.Shape(batch=1, heads=kw.get("heads", 16), d_latent=512, d_rope=64, sparse=kw.get("sparse", 0),
+                      max_ctx=64, topk=kw.get("topk", 0), scale=SCALE, num_sms=152, splits_override=0,
+                      variant=kw.get("variant", 0), pdl=0, stall_test=0, kv_fp8=1)
+        assert L.mla_decode_plan(ctypes.byref(s), ctypes.byref(out)) == rc, kw
+    for a, rc in [(_args(kv_scale=0.0), mla.EINVAL), (_args(kv_scale=float("nan")), mla.EINVAL),
+                  (_args(kv_scale=-1.0), mla.EINVAL), (_args(kv_scale=float("inf")), mla.EINVAL),
+                  (_args(kv_scale=0.5, row_stride=584), mla.EALIGN)]:
+        for fn in ("mla_decode_run", "mla_decode_combine", "mla_decode_forward"):
+            assert _call(fn, p, a) == rc, (fn, a.kv_scale, a.row_stride)
+    rows = ctypes.c_void_p(0x70000)
+    assert L.mla_decode_forward_step(ctypes.byref(p), ctypes.byref(_args(kv_scale=1.0)), ctypes.c_void_p(0x100000),
+                                     p.scratch_bytes, rows, 1, None) == mla.EUNSUPPORTED

@@ -48,7 +48,8 @@ class Plan(ctypes.Structure):
                 ("block", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("combine_grid_x", ctypes.c_int),
                 ("combine_grid_y", ctypes.c_int), ("combine_block", ctypes.c_int),
                 ("scratch_bytes", ctypes.c_size_t), ("o_part_offset", ctypes.c_size_t),
-                ("lse_part_offset", ctypes.c_size_t), ("status_offset", ctypes.c_size_t)]
+                ("lse_part_offset", ctypes.c_size_t), ("status_offset", ctypes.c_size_t),
+                ("flat_ranges", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {k: getattr(self, k) for k, _ in self._fields_ if k != "shape"}

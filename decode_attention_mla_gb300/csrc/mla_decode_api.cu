@@ -185,6 +185,21 @@ int check_plan(const mla_decode_plan_t* pl) {
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
     if (pl->grid_x < 1 || pl->grid_x > items || pl->grid_y != 1 || pl->grid_z != 1) return MLA_EINVAL;
     if (items > 0x7fffffffLL) return MLA_EINVAL;
+    if (pl->flat_ranges < 0) return MLA_EINVAL;
+    if (pl->flat_ranges > 0) {
+        // flat split: batched sparse decode on the warp-MMA kernel, whole slots per range,
+        // at most two requests per range, one CTA per range and head group
+        if (!pl->shape.sparse || pl->variant != kVariantWarpMma || pl->shape.batch < 2) return MLA_EINVAL;
+        const long long per = pl->entries_per_split;
+        if (per < mla::kStageRows || per % mla::kStageRows != 0 || per > pl->shape.topk) return MLA_EINVAL;
+        if (static_cast<long long>(pl->flat_ranges) * per <
+                static_cast<long long>(pl->shape.batch) * pl->shape.topk ||
+            static_cast<long long>(pl->flat_ranges - 1) * per >=
+                static_cast<long long>(pl->shape.batch) * pl->shape.topk)
+            return MLA_EINVAL;
+        if (static_cast<long long>(pl->grid_x) != static_cast<long long>(pl->flat_ranges) * pl->n_head_groups)
+            return MLA_EINVAL;
+    }
     if (pl->combine_grid_x != mla::combine_grid_rows(pl->shape.batch * pl->shape.heads, pl->splits) ||
         pl->combine_grid_y != MLA_D_LATENT / mla::kCombineChunk || pl->combine_block != mla::combine_block_threads())
         return MLA_EINVAL;
@@ -259,6 +274,9 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.sparse = pl->shape.sparse;
     p.n_groups = pl->n_head_groups;
     p.n_items = pl->shape.batch * pl->n_head_groups * pl->splits;
+    p.flat_ranges = pl->flat_ranges;
+    p.flat_per = pl->entries_per_split;
+    if (pl->flat_ranges > 0) p.n_items = 2 * pl->flat_ranges * pl->n_head_groups;
     p.granule = variant_granule(pl->variant);
     p.scale_log2 = pl->shape.scale * 1.4426950408889634f;
     p.kv_fp8 = pl->shape.kv_fp8;
@@ -386,6 +404,46 @@ int auto_variant(bool sparse, bool fp8, int batch, int heads, long long rows, lo
     return heads % 64 == 0 ? kVariantTc64 : kVariantTc32;
 }
 
+// Flat split of batched sparse decode (warp-MMA kernel).  The uniform split
+// gives every request S slices; B * S items either leave SMs idle or run in
+// waves.  The flat split cuts the B * topk list entries (request after
+// request) into one range per CTA and head group, a whole number of 32-row
+// slots each and at most topk (so a range touches at most two requests: two
+// items, the second often empty).  Modelled time: slots per range + 2 (two
+// item set-ups) against the uniform waves * (slots per slice + 1); the flat
+// split is taken only when strictly cheaper.
+struct FlatSplit {
+    int ranges, per, s_max;
+    long long cost;
+};
+bool derive_flat(int batch, int topk, int n_groups, long long grid_cap, FlatSplit* out) {
+    if (batch < 2 || n_groups < 1) return false;
+    const long long G = grid_cap / n_groups;
+    if (G < 2) return false;
+    const long long total = static_cast<long long>(batch) * topk;
+    long long per = ceil_div(total, G);
+    per = ceil_div(per, mla::kStageRows) * mla::kStageRows;
+    if (per > topk || per > 0x7fffffffLL) return false;
+    const long long ranges = ceil_div(total, per);
+    long long s_max = 1;
+    for (long long b = 0; b < batch; ++b) {
+        const long long first = b * topk / per, last = ((b + 1) * topk - 1) / per;
+        s_max = std::max(s_max, last - first + 1);
+    }
+    if (s_max > MLA_MAX_SPLITS) return false;
+    out->ranges = static_cast<int>(ranges);
+    out->per = static_cast<int>(per);
+    out->s_max = static_cast<int>(s_max);
+    out->cost = per / mla::kStageRows + 2;
+    return true;
+}
+long long uniform_cost(long long rows, long long pairs, long long grid_cap, int variant, long long S) {
+    const long long per = mla::slice_entries(rows, static_cast<int>(S), variant_granule(variant));
+    const long long items = pairs * ceil_div(rows, per);
+    const long long waves = ceil_div(items, std::min(items, grid_cap));
+    return waves * (ceil_div(per, variant_tile_rows(variant)) + 1);
+}
+
 }  // namespace
 
 extern "C" {
@@ -427,6 +485,16 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.entries_per_split = static_cast<int>(mla::slice_entries(rows, pl.splits, variant_granule(pl.variant)));
     const long long items = static_cast<long long>(s.batch) * pl.n_head_groups * pl.splits;
     pl.grid_x = static_cast<int>(std::min(items, grid_cap));
+    pl.flat_ranges = 0;
+    FlatSplit fs{};
+    if (s.sparse && pl.variant == kVariantWarpMma && s.splits_override == 0 &&
+        derive_flat(s.batch, s.topk, pl.n_head_groups, grid_cap, &fs) &&
+        fs.cost < uniform_cost(rows, static_cast<long long>(s.batch) * pl.n_head_groups, grid_cap, pl.variant, S)) {
+        pl.flat_ranges = fs.ranges;
+        pl.splits = fs.s_max;
+        pl.entries_per_split = fs.per;
+        pl.grid_x = fs.ranges * pl.n_head_groups;
+    }
     pl.grid_y = 1;
     pl.grid_z = 1;
     const bool tc = variant_is_tc(pl.variant);

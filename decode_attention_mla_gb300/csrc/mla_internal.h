@@ -37,6 +37,15 @@ struct PartialParams {
     int n_groups;               // heads / head group
     int granule;                // slices are whole multiples of this many entries
     int n_items;                // batch * n_groups * splits work items, walked round-robin by the CTAs
+                                // (flat split: 2 * flat_ranges * n_groups)
+    // Flat split (batched sparse decode, warp-MMA kernel): the B * topk list
+    // entries are cut into flat_ranges contiguous ranges of flat_per entries
+    // (a multiple of 32, at most topk), one per CTA and head group; a range
+    // holds pieces of at most two requests (two items), and request b's piece
+    // in range r is its slice r - floor(b * topk / flat_per).  0 = the uniform
+    // split of every request into `splits` slices.
+    int flat_ranges;
+    int flat_per;
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units
     float* o_part;              // [B][H][S][512]
     float* lse_part;            // [B][H][S]

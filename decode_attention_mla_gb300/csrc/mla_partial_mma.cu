@@ -187,7 +187,57 @@ struct Item {
     int b, hg, s, n_slots;
     long long base;
     uint32_t e0, e1;                       // entries [e0, e1) of the request
+    bool skip;                             // flat split: no such piece (nothing to write)
+    bool last_piece;                       // flat split: holds the request's last entry
 };
+
+// Where an item sits, from the split alone (no device reads): request b, head
+// group hg, slice s and, for the flat split, the piece's entries [e0, e1)
+// (exists = false for the second piece of a range that holds one request).
+struct ItemCoords {
+    int b, hg, s;
+    uint32_t e0, e1;
+    bool exists, last_piece;
+};
+__device__ __forceinline__ ItemCoords item_coords(const PartialParams& p, int item) {
+    ItemCoords c;
+    const uint32_t ui = static_cast<uint32_t>(item);
+    const uint32_t rest = ui / static_cast<uint32_t>(p.n_groups);
+    c.hg = static_cast<int>(ui - rest * static_cast<uint32_t>(p.n_groups));
+    c.e0 = c.e1 = 0;
+    c.exists = true;
+    c.last_piece = false;
+    if (p.flat_ranges == 0) {
+        const uint32_t b = rest / static_cast<uint32_t>(p.splits);
+        c.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
+        c.b = static_cast<int>(b);
+        return c;
+    }
+    // flat: item = (part, range, head group); the range's entries in the
+    // concatenated lists, and the request(s) they belong to
+    const uint32_t G = static_cast<uint32_t>(p.flat_ranges);
+    const uint32_t part = rest / G;
+    const uint32_t r = rest - part * G;
+    const uint32_t k = static_cast<uint32_t>(p.topk), P = static_cast<uint32_t>(p.flat_per);
+    const uint32_t total = static_cast<uint32_t>(p.batch) * k;
+    const uint32_t start = r * P;
+    const uint32_t end = start + P < total ? start + P : total;
+    uint32_t b = start / k;
+    if (part == 1) ++b;
+    const uint32_t lo = b * k, hi = lo + k;
+    c.b = static_cast<int>(b);
+    if (start >= total || b >= static_cast<uint32_t>(p.batch) || end <= lo) {
+        c.exists = false;
+        c.s = 0;
+        c.b = 0;
+        return c;
+    }
+    c.e0 = (start > lo ? start : lo) - lo;
+    c.e1 = (end < hi ? end : hi) - lo;
+    c.s = static_cast<int>(r - lo / P);
+    c.last_piece = end >= hi;
+    return c;
+}
 
 // The request fields an item's slice depends on (dense: d_pos[b] and the
 // segment's first row), read ahead of their use by the caller.
@@ -202,18 +252,25 @@ __device__ __forceinline__ RequestRead read_request(const PartialParams& p, int 
     return r;
 }
 __device__ __forceinline__ int request_of(const PartialParams& p, int item) {
-    return static_cast<int>(static_cast<uint32_t>(item) / static_cast<uint32_t>(p.n_groups) /
-                            static_cast<uint32_t>(p.splits));
+    return item_coords(p, item).b;
 }
 
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item, const RequestRead* pre = nullptr) {
     Item it;
-    const uint32_t ui = static_cast<uint32_t>(item);
-    const uint32_t rest = ui / static_cast<uint32_t>(p.n_groups);
-    it.hg = static_cast<int>(ui - rest * static_cast<uint32_t>(p.n_groups));
-    const uint32_t b = rest / static_cast<uint32_t>(p.splits);
-    it.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
-    it.b = static_cast<int>(b);
+    const ItemCoords c = item_coords(p, item);
+    it.hg = c.hg;
+    it.s = c.s;
+    it.b = c.b;
+    it.skip = !c.exists;
+    it.last_piece = c.last_piece;
+    if (p.flat_ranges > 0) {
+        // flat split (sparse only): the piece's entries are known without reads
+        it.base = pre ? pre->base : (c.exists && p.row_offset ? p.row_offset[c.b] : 0);
+        it.e0 = c.e0;
+        it.e1 = c.e1;
+        it.n_slots = c.exists ? static_cast<int>((c.e1 - c.e0 + kStageRows - 1) / kStageRows) : 0;
+        return it;
+    }
     // entry counts are below 2^31 (d_pos and the list length are int32), so
     // the slice arithmetic runs in 32 bits (64-bit division is slow); dense
     // entries are already clamped to the rows that exist in the cache
@@ -244,9 +301,8 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item, co
 
 // Query tile of the CTA's first item: known without the context length.
 __device__ __forceinline__ int first_key(const PartialParams& p) {
-    const int item = static_cast<int>(blockIdx.x);
-    const int rest = item / p.n_groups;
-    return (rest / p.splits) * p.n_groups + (item - rest * p.n_groups);
+    const ItemCoords c = item_coords(p, static_cast<int>(blockIdx.x));
+    return c.b * p.n_groups + c.hg;
 }
 
 template <class S>
@@ -267,10 +323,8 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 __device__ void prefetch_first_inputs(const TcMaps& maps, const PartialParams& p) {
     const int item = static_cast<int>(blockIdx.x);
     if (item >= p.n_items) return;
-    const int rest = item / p.n_groups;
-    const int hg = item - rest * p.n_groups;
-    const int b = rest / p.splits;
-    const int s = rest - b * p.splits;
+    const ItemCoords c = item_coords(p, item);
+    const int hg = c.hg, b = c.b, s = c.s;
     tma_prefetch_3d(&maps.q, 0, b * p.heads + hg * kHeadGroup, 0);
     if (!p.sparse) prefetch_l2(p.d_pos + b);
     if (p.row_offset) prefetch_l2(p.row_offset + b);
@@ -779,10 +833,15 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
 
     for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
         const Item it = decode_item(p, item);
+        const long long row_b = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits;
+        if (it.last_piece) {
+            // flat split: the request has no pieces past this one; its remaining
+            // slices are written empty so that the merge can read every slice
+            for (int s2 = it.s + 1; s2 < p.splits; ++s2)
+                write_empty_partial(p.o_part, p.lse_part, row_b + s2, p.splits, w * 32 + lane, kMmaThreads);
+        }
         if (it.n_slots == 0) {
-            write_empty_partial(p.o_part, p.lse_part,
-                                (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s,
-                                p.splits, w * 32 + lane, kMmaThreads);
+            if (!it.skip) write_empty_partial(p.o_part, p.lse_part, row_b + it.s, p.splits, w * 32 + lane, kMmaThreads);
             continue;
         }
         const int key = it.b * p.n_groups + it.hg;

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 3
+#define MLA_DECODE_ABI_VERSION 4
 #define MLA_D_LATENT 512
 #define MLA_D_ROPE 64
 #define MLA_D_ROW 576        /* elements per cache row */
@@ -126,6 +126,14 @@ typedef struct {
     size_t o_part_offset;      /* fp32 [B][H][S][512] normalised slice outputs */
     size_t lse_part_offset;    /* fp32 [B][H][S] slice log-sum-exp (-inf for an empty slice) */
     size_t status_offset;      /* int32 status word: 0 healthy, else an mla_status */
+    int flat_ranges;           /* 0: every request cut into `splits` slices of entries_per_split entries.
+                                  > 0 (batched sparse decode, chosen when the cost model prefers it):
+                                  the B * topk list entries, request after request, cut into
+                                  flat_ranges ranges of entries_per_split entries, one CTA per range
+                                  and head group, so no SM idles when B * S slices would not fill
+                                  the GPU; a range holds pieces of at most two requests, and
+                                  `splits` = the most pieces any request has (the merge reads that
+                                  many slices per request, missing ones written empty) */
 } mla_decode_plan_t;
 
 /* Per-call tensors. */

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     L = ctypes.CDLL(mla.LIB_PATH)
     for n in sorted(names):
         assert hasattr(L, n), f"{n} declared but not exported"
-    assert mla.abi_version() == 3
+    assert mla.abi_version() == 4
     assert "scratch" in mla.strerror(mla.ESCRATCH)
 
 
@@ -71,7 +71,7 @@ def _model_split(rows, pairs, sms, variant=2, max_splits=256):
     (dict(max_ctx=256), 1, 8, 32),
     (dict(max_ctx=8192), 1, 128, 64),
     (dict(sparse=True, topk=2048), 1, 64, 32),
-    (dict(batch=64, sparse=True, topk=2048), 1, 2, 1024),
+    (dict(batch=64, sparse=True, topk=2048), 1, 4, 864),         # flat split: 152 ranges of 864 entries
     (dict(heads=128, max_ctx=32768 + 64), 4, 74, 448),
     (dict(heads=128, max_ctx=32768 + 64, variant=3), 3, 37, 896),
     (dict(heads=64, max_ctx=32768), 4, 128, 256),
@@ -88,10 +88,14 @@ def test_plan_derivation_for_the_workloads(kw, variant, splits, entries):
     assert (p.variant, p.splits, p.entries_per_split) == (variant, splits, entries)
     rows = kw.get("topk") or kw.get("max_ctx")
     B, H = kw.get("batch", 1), kw.get("heads", 16)
-    assert p.splits * p.entries_per_split >= rows
-    assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
+    if not p.flat_ranges:
+        assert p.splits * p.entries_per_split >= rows
+        assert (p.splits - 1) * p.entries_per_split < rows + p.entries_per_split
     assert p.n_head_groups == H // HEADS[variant] and p.ctas_per_sm == 1
-    assert p.grid_x == min(B * p.n_head_groups * p.splits, 152) and p.grid_y == 1 and p.grid_z == 1
+    if p.flat_ranges:
+        assert p.grid_x == p.flat_ranges * p.n_head_groups <= 152 and p.grid_y == 1 and p.grid_z == 1
+    else:
+        assert p.grid_x == min(B * p.n_head_groups * p.splits, 152) and p.grid_y == 1 and p.grid_z == 1
     assert p.combine_grid_x == -(-B * H // (8 // _unit_warps(p.splits))) and p.combine_grid_y == 4
     assert p.combine_block == 256
     # scratch layout: status word, then o_part, then lse_part, 256-byte aligned
@@ -137,7 +141,11 @@ def test_plan_split_rule_matches_model(variant, rows, batch, heads, sms):
     p = _plan(max_ctx=rows, batch=batch, heads=heads, num_sms=sms, variant=variant)
     assert p.splits == _model_split(rows, batch * heads // 16, sms, variant)
     ps = _plan(sparse=True, topk=rows, batch=batch, heads=heads, num_sms=sms, variant=variant)
-    assert ps.splits == p.splits
+    if ps.flat_ranges:   # batched sparse on the warp-MMA kernel may take the flat split instead
+        assert variant == 1 and batch > 1
+        assert (ps.flat_ranges, ps.entries_per_split, ps.splits) == _model_flat(rows, batch, heads // 16, sms)[:3]
+    else:
+        assert ps.splits == p.splits
 
 
 def _model_auto(sparse, rows, batch, heads, sms):
@@ -162,7 +170,79 @@ def test_plan_automatic_kernel_choice(rows, batch, heads, sparse):
     p = _plan(batch=batch, heads=heads, **kw)
     v = _model_auto(sparse, rows, batch, heads, 152)
     assert p.variant == v
-    assert p.splits == _model_split(rows, batch * heads // HEADS[v], 152, v)
+    S = _model_split(rows, batch * heads // HEADS[v], 152, v)
+    flat = _model_flat(rows, batch, heads // HEADS[v], 152) if (sparse and v == 1) else None
+    if flat and flat[3] < _model_uniform_cost(rows, batch * heads // HEADS[v], 152, v, S):
+        assert (p.flat_ranges, p.entries_per_split, p.splits) == flat[:3]
+    else:
+        assert p.flat_ranges == 0 and p.splits == S
+
+
+def _model_uniform_cost(rows, pairs, sms, variant, S):
+    tile, gran = TILE[variant], GRANULE[variant]
+    per = -(-(-(-rows // S)) // gran) * gran
+    items = pairs * -(-rows // per)
+    return -(-items // min(items, sms)) * (-(-per // tile) + 1)
+
+
+def _model_flat(topk, batch, groups, sms):
+    """The flat split restated: (ranges, entries per range, most pieces per
+    request, modelled cost), or None where it does not apply."""
+    G = sms // groups
+    if batch < 2 or G < 2:
+        return None
+    total = batch * topk
+    per = -(-(-(-total // G)) // 32) * 32
+    if per > topk:
+        return None
+    ranges = -(-total // per)
+    s_max = max(((b + 1) * topk - 1) // per - (b * topk) // per + 1 for b in range(batch))
+    return ranges, per, s_max, per // 32 + 2
+
+
+def _flat_pieces(topk, batch, ranges, per):
+    """The kernel's flat item coordinates, restated: for every (part, range)
+    the request, slice, entries and whether the piece exists / is the last."""
+    out = []
+    total = batch * topk
+    for part in (0, 1):
+        for r in range(ranges):
+            start, end = r * per, min(r * per + per, total)
+            b = start // topk + part
+            lo, hi = b * topk, b * topk + topk
+            if start >= total or b >= batch or end <= lo:
+                out.append(None)
+                continue
+            out.append((b, r - lo // per, max(start, lo) - lo, min(end, hi) - lo, end >= hi))
+    return out
+
+
+@pytest.mark.parametrize("batch,topk,sms,heads", [(64, 2048, 152, 16), (3, 700, 4, 16), (17, 96, 152, 16),
+                                                  (64, 2048, 132, 32), (5, 4096, 8, 16), (2, 64, 3, 16)])
+def test_plan_flat_split_covers_every_entry_once(batch, topk, sms, heads):
+    """Where the planner takes the flat split, its pieces cover every list
+    entry of every request exactly once, each request's pieces are its
+    slices 0 .. n-1 in order, and n <= splits (the rest are written empty)."""
+    p = _plan(batch=batch, heads=heads, sparse=True, topk=topk, num_sms=sms)
+    model = _model_flat(topk, batch, heads // 16, sms)
+    if not p.flat_ranges:
+        assert model is None or model[3] >= _model_uniform_cost(
+            topk, batch * heads // 16, sms, 1, _model_split(topk, batch * heads // 16, sms, 1))
+        return
+    assert (p.flat_ranges, p.entries_per_split, p.splits) == model[:3]
+    assert p.entries_per_split % 32 == 0 and p.entries_per_split <= topk
+    seen = {b: [] for b in range(batch)}
+    for piece in _flat_pieces(topk, batch, p.flat_ranges, p.entries_per_split):
+        if piece:
+            b, s, e0, e1, last = piece
+            assert 0 <= s < p.splits and e0 < e1
+            seen[b].append((s, e0, e1, last))
+    for b, pieces in seen.items():
+        pieces.sort()
+        assert [s for s, _, _, _ in pieces] == list(range(len(pieces)))
+        assert pieces[0][1] == 0 and pieces[-1][2] == topk and pieces[-1][3]
+        assert all(pieces[i][2] == pieces[i + 1][1] for i in range(len(pieces) - 1))
+        assert sum(1 for q in pieces if q[3]) == 1
 
 
 def _unit_warps(splits):

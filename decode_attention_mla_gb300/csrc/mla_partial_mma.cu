@@ -194,11 +194,13 @@ struct Item {
 // Where an item sits, from the split alone (no device reads): request b, head
 // group hg, slice s and, for the flat split, the piece's entries [e0, e1)
 // (exists = false for the second piece of a range that holds one request).
+// The flat split is sparse only: the dense instantiations compile without it.
 struct ItemCoords {
     int b, hg, s;
     uint32_t e0, e1;
     bool exists, last_piece;
 };
+template <bool kDense>
 __device__ __forceinline__ ItemCoords item_coords(const PartialParams& p, int item) {
     ItemCoords c;
     const uint32_t ui = static_cast<uint32_t>(item);
@@ -207,7 +209,7 @@ __device__ __forceinline__ ItemCoords item_coords(const PartialParams& p, int it
     c.e0 = c.e1 = 0;
     c.exists = true;
     c.last_piece = false;
-    if (p.flat_ranges == 0) {
+    if (kDense || p.flat_ranges == 0) {
         const uint32_t b = rest / static_cast<uint32_t>(p.splits);
         c.s = static_cast<int>(rest - b * static_cast<uint32_t>(p.splits));
         c.b = static_cast<int>(b);
@@ -245,25 +247,28 @@ struct RequestRead {
     int d_pos;
     long long base;
 };
+template <bool kDense>
 __device__ __forceinline__ RequestRead read_request(const PartialParams& p, int b) {
     RequestRead r;
-    r.d_pos = p.sparse ? 0 : p.d_pos[b];
+    r.d_pos = kDense ? p.d_pos[b] : 0;
     r.base = p.row_offset ? p.row_offset[b] : 0;
     return r;
 }
+template <bool kDense>
 __device__ __forceinline__ int request_of(const PartialParams& p, int item) {
-    return item_coords(p, item).b;
+    return item_coords<kDense>(p, item).b;
 }
 
+template <bool kDense>
 __device__ __forceinline__ Item decode_item(const PartialParams& p, int item, const RequestRead* pre = nullptr) {
     Item it;
-    const ItemCoords c = item_coords(p, item);
+    const ItemCoords c = item_coords<kDense>(p, item);
     it.hg = c.hg;
     it.s = c.s;
     it.b = c.b;
     it.skip = !c.exists;
     it.last_piece = c.last_piece;
-    if (p.flat_ranges > 0) {
+    if (!kDense && p.flat_ranges > 0) {
         // flat split (sparse only): the piece's entries are known without reads
         it.base = pre ? pre->base : (c.exists && p.row_offset ? p.row_offset[c.b] : 0);
         it.e0 = c.e0;
@@ -278,15 +283,15 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item, co
     if (pre) {
         // the same count as request_entries, from values read earlier
         it.base = pre->base;
-        long long m = p.sparse ? p.topk : static_cast<long long>(pre->d_pos) + 1;
-        if (!p.sparse) {
+        long long m = kDense ? static_cast<long long>(pre->d_pos) + 1 : p.topk;
+        if (kDense) {
             const long long cap = p.kv_rows - it.base;
             if (m > cap) m = cap;
             if (m < 0) m = 0;
         }
         n = static_cast<uint32_t>(m);
     } else {
-        n = static_cast<uint32_t>(request_entries(p.sparse, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
+        n = static_cast<uint32_t>(request_entries(!kDense, p.topk, p.d_pos, p.row_offset, p.kv_rows, it.b, &it.base));
     }
     const uint32_t per = slice_entries_u32(n, static_cast<uint32_t>(p.splits), kStageRows);
     uint32_t e0 = static_cast<uint32_t>(it.s) * per;
@@ -300,8 +305,9 @@ __device__ __forceinline__ Item decode_item(const PartialParams& p, int item, co
 }
 
 // Query tile of the CTA's first item: known without the context length.
+template <bool kDense>
 __device__ __forceinline__ int first_key(const PartialParams& p) {
-    const ItemCoords c = item_coords(p, static_cast<int>(blockIdx.x));
+    const ItemCoords c = item_coords<kDense>(p, static_cast<int>(blockIdx.x));
     return c.b * p.n_groups + c.hg;
 }
 
@@ -320,15 +326,16 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const PartialParams& 
 // request fields and the first row of its partial output into L2 (with their
 // address translations).  Hints only: everything is read again after the
 // grid dependency.
+template <bool kDense>
 __device__ void prefetch_first_inputs(const TcMaps& maps, const PartialParams& p) {
     const int item = static_cast<int>(blockIdx.x);
     if (item >= p.n_items) return;
-    const ItemCoords c = item_coords(p, item);
+    const ItemCoords c = item_coords<kDense>(p, item);
     const int hg = c.hg, b = c.b, s = c.s;
     tma_prefetch_3d(&maps.q, 0, b * p.heads + hg * kHeadGroup, 0);
-    if (!p.sparse) prefetch_l2(p.d_pos + b);
+    if (kDense) prefetch_l2(p.d_pos + b);
     if (p.row_offset) prefetch_l2(p.row_offset + b);
-    if (p.sparse) {
+    if (!kDense) {
         prefetch_l2(p.cache_len + b);
         prefetch_l2(p.indices + static_cast<long long>(b) * p.topk);
     }
@@ -370,14 +377,14 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     // needs no context length); the MMA warps follow the same sequence of keys
     // (a new tile whenever a busy item's key differs) and release a tile
     // through q_empty, read or not
-    int q_key = first_key(p);
+    int q_key = first_key<kDense>(p);
     int q_loads = 0;          // query tiles staged so far
     int patch_uses = 0;       // fused append: slots patched so far (phase of patch_bar)
     // the first item's request fields are read before the query tile is
     // requested, so that the two latencies overlap
     RequestRead first{0, 0};
     if (wp == 0) {
-        first = read_request(p, blockIdx.x < p.n_items ? request_of(p, blockIdx.x) : 0);
+        first = read_request<kDense>(p, blockIdx.x < p.n_items ? request_of<kDense>(p, blockIdx.x) : 0);
         load_q(maps, p, sh, q_key, lane);
         q_loads = 1;
     }
@@ -385,7 +392,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
     bool ok = !(wp == 0 && p.stall_test && !mbar_wait_bounded(&sh.stall_bar, 0, &sh.abort_flag, kStallTestCycles));
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const Item it =
-            decode_item(p, item, (wp == 0 && item == static_cast<int>(blockIdx.x)) ? &first : nullptr);
+            decode_item<kDense>(p, item, (wp == 0 && item == static_cast<int>(blockIdx.x)) ? &first : nullptr);
         if (it.n_slots == 0) continue;
         const int key = it.b * p.n_groups + it.hg;
         if (wp == 0 && key != q_key) {
@@ -548,7 +555,7 @@ struct SlotCursor {
 };
 __device__ __forceinline__ void slot_cursor_next_item(const PartialParams& p, SlotCursor& c, int from) {
     for (int i = from; i < p.n_items; i += gridDim.x) {
-        const Item it = decode_item(p, i);
+        const Item it = decode_item<true>(p, i);
         if (it.n_slots > 0) {
             c.item = i;
             c.st = 0;
@@ -595,7 +602,7 @@ __device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, SharedS
     const bool issuer = ct == 0;                  // issues the loads, prefetches ahead, loads the query tiles
     constexpr int kPrefetchAhead = 6;             // slots of L2 prefetch ahead of the loads
     volatile int never = 0;
-    int q_key = first_key(p);
+    int q_key = first_key<true>(p);
     int q_loads = 0;
     int issued = 0;                               // slot loads issued (issuer)
     SlotCursor ic{}, pc{};                        // issue and prefetch cursors (issuer)
@@ -615,7 +622,7 @@ __device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, SharedS
     }
     int stage = 0;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const Item it = decode_item(p, item);
+        const Item it = decode_item<true>(p, item);
         if (it.n_slots == 0) continue;
         bool qw = true;                            // the query tile's buffer was free (warp 0)
         if (wp == 0) {
@@ -826,22 +833,22 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
     int stage = 0;                          // slots of earlier items (ring position of this item's slot 0)
     int pbuf = 0;                           // this group's P buffer for its next slot
     int q_phase = 0;                        // query tiles consumed (q_full phases)
-    int q_key = first_key(p);               // key of the tile the producer loaded last
+    int q_key = first_key<kDense>(p);               // key of the tile the producer loaded last
     bool q_in_regs = false;                 // that tile is in registers (and released)
     bool failed = false;                    // a wait of this warp ran out
     bool stop = false;                      // every MMA warp saw a failure at the same barrier: leave
 
     for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
-        const Item it = decode_item(p, item);
+        const Item it = decode_item<kDense>(p, item);
         const long long row_b = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits;
-        if (it.last_piece) {
+        if (!kDense && it.last_piece) {
             // flat split: the request has no pieces past this one; its remaining
             // slices are written empty so that the merge can read every slice
             for (int s2 = it.s + 1; s2 < p.splits; ++s2)
                 write_empty_partial(p.o_part, p.lse_part, row_b + s2, p.splits, w * 32 + lane, kMmaThreads);
         }
         if (it.n_slots == 0) {
-            if (!it.skip) write_empty_partial(p.o_part, p.lse_part, row_b + it.s, p.splits, w * 32 + lane, kMmaThreads);
+            if (kDense || !it.skip) write_empty_partial(p.o_part, p.lse_part, row_b + it.s, p.splits, w * 32 + lane, kMmaThreads);
             continue;
         }
         const int key = it.b * p.n_groups + it.hg;
@@ -1163,7 +1170,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         if constexpr (kDense) {
             if (warp == kProducerWarp + 1 && lane == 0) prefetch_first_slots(maps, p);
         }
-        if (warp == kProducerWarp + 2 && lane == 0) prefetch_first_inputs(maps, p);
+        if (warp == kProducerWarp + 2 && lane == 0) prefetch_first_inputs<kDense>(maps, p);
         if constexpr (kFp8) {
             // all four warps widen the E4M3 rows; one thread also stages them
             grid_dependency_wait();

@@ -67,6 +67,23 @@ def test_fp8_more_heads(H):
     _gpu.assert_parity(out, lse, ro, rl, f"E4M3 H={H}")
 
 
+@pytest.mark.parametrize("T", [32768, 131072])
+def test_fp8_context_sweep_workloads(T):
+    """The E4M3 rows of the bench at full size (the planner's S, PDL on)."""
+    x = workloads.dense(1, 16, T, seed=T + 13)
+    kv8, kv_scale = workloads.to_e4m3(x.kv)
+    d = _gpu.dev()
+    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, kv_fp8=True, pdl=True)
+    scratch = mla.alloc_scratch(plan)
+    out = torch.full((1, 16, 512), float("nan"), device=d)
+    lse = torch.full((1, 16), float("nan"), device=d)
+    mla.forward(plan, x.q.to(d), kv8.to(d), out, lse, scratch, d_pos=x.d_pos.to(d), kv_scale=kv_scale)
+    torch.cuda.synchronize()
+    ro, rl = _oracle(x, kv8, kv_scale)
+    _gpu.assert_parity(out, lse, ro, rl, f"E4M3 T={T} S={plan.splits}")
+    assert mla.status_word(plan, scratch) == 0
+
+
 def test_fp8_partials_match_oracle_split_emulation():
     x = workloads.dense(1, 16, 2000, seed=720)
     kv8, kv_scale = workloads.to_e4m3(x.kv)

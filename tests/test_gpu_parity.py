@@ -60,6 +60,20 @@ def test_dense_t8192_split_sweep(variant):
             assert (np.abs(results[a][1] - results[b][1]) / np.maximum(np.abs(rl), 1)).max() <= 2 * _gpu.LSE_RTOL
 
 
+@pytest.mark.parametrize("T", [16384, 32768, 65536, 131072])
+def test_dense_context_sweep_workloads(T):
+    """The H = 16 context sweep at full size, in the launch configuration the
+    bench times (the planner's S and kernel, PDL on): every output against the
+    fp64 oracle.  At T = 32768 and 65536 (S = 147, 7 slots per CTA) the two
+    MMA groups hold 4 and 3 slots of an item."""
+    x = workloads.dense(1, 16, T, seed=T + 11)
+    out, lse, plan, scratch = _gpu.run_dense(x, pdl=True)
+    assert plan.variant == 1
+    ro, rl = _gpu.oracle_dense(x)
+    _gpu.assert_parity(out, lse, ro, rl, f"dense H=16 T={T} S={plan.splits}")
+    assert mla.status_word(plan, scratch) == 0
+
+
 @pytest.mark.parametrize("variant", _gpu.VARIANTS)
 def test_dense_partials_match_oracle_split_emulation(variant):
     """The partial kernel's scratch (o_s, lse_s) against the oracle's fp64 emulation

@@ -10,9 +10,12 @@ from HBM.  The calls of one step are captured as one CUDA graph and replayed.
 Prints ONE JSON line: metric/value (achieved HBM GB/s of the whole call,
 algorithmic bytes / time per call), us_per_call, the roofline of the partial
 kernel (live CUDA-event timing), the end-to-end number through the C ABI with
-host buffers, the oracle timed on the host cores, and the SM clocks seen during
-the timed region.  ``--impl reference`` times the fp64 CPU oracle instead.
-``--details PATH`` also writes every workload and a context sweep to PATH.
+host buffers, the oracle timed on the host cores (all threads and one), the SM
+clocks seen during the timed region, a `sweep` of the five workloads and the
+context sweep at H=16 (us per call, the partial kernel alone, fractions of the
+roofline) and a PDL on/off A/B (`pdl_ab`).  ``--impl reference`` times the fp64
+CPU oracle instead.  ``--details PATH`` also writes a longer table (split sweep,
+E4M3 cache, fused step, projection) to PATH.
 
 Multi-GPU: replicas only (each rank runs its own copy of the workload; no
 collective on the data path; max time over ranks).
@@ -187,20 +190,39 @@ class DenseBench:
     def combine(self, c, stream=None):
         self.mla.combine(self.plan, self.args[c], self.scratch, stream)
 
+    def replan(self, pdl):
+        """The same plan (split count, kernel) launched with or without PDL."""
+        self.plan = self.mla.plan(batch=1, heads=self.H, max_ctx=self.T, scale=self.host.scale,
+                                  splits=self.plan.splits, pdl=pdl, variant=self.plan.variant,
+                                  kv_fp8=bool(self.plan.shape.kv_fp8))
+
 
 class SparseBench:
     """Sparse decode; `copies` distinct caches when one cache is below 3x L2."""
 
-    def __init__(self, name, copies, splits, pdl, seed=0, variant=0):
+    def __init__(self, name, copies, splits, pdl, seed=0, variant=0, device_cache=False):
         import decode_attention_mla_gb300 as mla
         self.mla = mla
         d = torch.device("cuda")
-        x = workloads.make(name, seed=seed)
+        if device_cache:
+            # timing only: the recipe's lengths, offsets, queries and index lists,
+            # with the cache rows drawn N(0,1) bf16 on the device (drawing ~5 GB on
+            # the host takes tens of seconds); the parity tests use the host draw
+            x = sparse_recipe_without_cache(name, seed)
+            total = int(x.cache_len.to(torch.int64).sum())
+            gen = torch.Generator(device=d).manual_seed(seed)
+            kv0 = torch.empty(total, 576, dtype=torch.bfloat16, device=d)
+            for r0 in range(0, total, 1 << 20):
+                r1 = min(total, r0 + (1 << 20))
+                kv0[r0:r1] = torch.randn(r1 - r0, 576, generator=gen, device=d).to(torch.bfloat16)
+        else:
+            x = workloads.make(name, seed=seed)
+            kv0 = x.kv.to(d)
         self.host = x
         B, H, _ = x.q.shape
         topk = x.indices.shape[1]
         self.copies = copies
-        self.kv = [x.kv.to(d)]
+        self.kv = [kv0]
         for c in range(1, copies):
             self.kv.append(torch.roll(self.kv[0], shifts=c * 37, dims=0))
         self.q = x.q.to(d)
@@ -226,6 +248,24 @@ class SparseBench:
 
     def combine(self, c, stream=None):
         self.mla.combine(self.plan, self.args[c], self.scratch, stream)
+
+
+def sparse_recipe_without_cache(name, seed):
+    """The sparse workload's lengths, offsets, queries and index lists as the
+    input recipe draws them, with an empty cache (rows drawn elsewhere)."""
+    w = workloads.WORKLOADS[name]
+    B, H, topk = w["B"], w["H"], w["topk"]
+    if "cache" in w:
+        lens = torch.full((B,), w["cache"], dtype=torch.int32)
+    else:
+        lens = workloads.ragged_lengths(B, w["len_lo"], w["len_hi"], seed=seed)
+    offs = torch.zeros(B, dtype=torch.int64)
+    if B > 1:
+        offs[1:] = torch.cumsum(lens.to(torch.int64), 0)[:-1]
+    q = workloads.randn_bf16(B * H, 576, seed=seed, stream=1).view(B, H, 576)
+    idx = torch.stack([workloads.unique_indices(int(lens[b]), topk, seed=seed, stream=3, chunk=b) for b in range(B)])
+    return workloads.SparseInputs(q=q, kv=torch.empty(0, 576, dtype=torch.bfloat16), indices=idx.contiguous(),
+                                  cache_len=lens, row_offset=offs)
 
 
 class GraphBench:
@@ -256,10 +296,15 @@ class GraphBench:
         self.scratch = mla.alloc_scratch(self.plan)
         self.args = [[mla.make_args(self.q[k], self.kv[l], self.out[l][k], self.lse[l][k], d_pos=self.d_pos)
                       for k in range(steps)] for l in range(layers)]
+        self.g_scale = g.scale
         mean_rows = T0 + 1 + (steps - 1) / 2.0
         self.alg_bytes = mean_rows * ROW_BYTES + H * 576 * 2 + H * 512 * 4 + H * 4 + 2 * ROW_BYTES + 8
         self.flops = mean_rows * H * FLOP_PER_ROW_HEAD
         self.calls = steps * layers
+
+    def replan(self, pdl):
+        self.plan = self.mla.plan(batch=1, heads=self.H, max_ctx=self.T0 + self.steps, scale=self.g_scale,
+                                  splits=self.plan.splits, pdl=pdl, variant=self.plan.variant)
 
     def loop(self, _c=0, stream=None):
         mla = self.mla
@@ -342,13 +387,43 @@ def oracle_time_dense(x, budget_s, threads=0):
             return el / n, n
 
 
+def cpu_model():
+    """The host CPU's model name (x86 'model name', else lscpu's, else the Arm part id)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        text = ""
+    for line in text.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    parts = [line.split(":", 1)[1].strip() for line in text.splitlines()
+             if line.lower().startswith(("cpu implementer", "cpu part"))][:2]
+    return "implementer/part " + "/".join(parts) if parts else "unknown"
+
+
 def cpu_baseline(bench, budget_s):
+    """The oracle on the host cores, on the bench's own dense workload: all
+    hardware threads (parallel over request and head) and one thread."""
     import oracle
     threads = oracle.hardware_threads()
     per_call, n = oracle_time_dense(bench.host, budget_s, threads)
+    per_call_1, n1 = oracle_time_dense(bench.host, budget_s / 2, 1)
     return {"value": bench.alg_bytes / per_call / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "us_per_call": per_call * 1e6,
+            "single_thread": {"value": bench.alg_bytes / per_call_1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "us_per_call": per_call_1 * 1e6, "calls": n1},
             "sample": f"{n} full calls of the dense T={bench.T} H={bench.H} workload (fp64 oracle, "
-                      f"{threads} threads), {per_call * 1e3:.1f} ms/call"}
+                      f"{threads} threads), {per_call * 1e3:.1f} ms/call; single thread: {n1} calls, "
+                      f"{per_call_1 * 1e3:.1f} ms/call"}
 
 
 # --------------------------------------------------------------------------- e2e
@@ -427,6 +502,20 @@ def whole_job_gbs(alg_bytes_per_call: int, calls_per_rank: int, world: int, elap
 
 
 # --------------------------------------------------------------------------- main arms
+class CpuSide:
+    """What the oracle timing needs of a bench (its host inputs and sizes)."""
+
+    def __init__(self, bench):
+        self.host, self.T, self.H, self.alg_bytes = bench.host, bench.T, bench.H, bench.alg_bytes
+
+
+def workload_config(world):
+    """The timed workload, the same keys in both arms."""
+    return {"workload": "dense_t8192", "batch": 1, "heads": 16, "d_latent": 512, "d_rope": 64, "context": 8192,
+            "l2": "inputs larger than L2: every step reads distinct caches totalling more than 3x L2",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_ours(args, rank, world):
     import decode_attention_mla_gb300 as mla
     from decode_attention_mla_gb300 import build as mla_build
@@ -464,23 +553,23 @@ def run_ours(args, rank, world):
     t_part = time_graph(gp, max(10, steps // 2), warm) / (max(10, steps // 2) * copies)
     part_bytes = T * ROW_BYTES + H * 576 * 2 + 4      # KV rows + q + d_pos read by the partial kernel
     achieved = part_bytes / t_part / 1e9
-    kname = "mla_partial_tc_kernel" if bench.plan.variant == 2 else "mla_partial_mma_kernel"
+    kname = "mla_partial_mma_kernel" if bench.plan.variant == 1 else "mla_partial_tc_kernel"
     traffic = ncu_traffic(kname, "dense_t8192")
     reps = per_rep_times(g, 20)
     per_call_reps = [r / copies * 1e6 for r in reps]
+    cpu_bench = CpuSide(bench)
     clocks = clk.summary()
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": round(elapsed / steps * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "dense_t8192", "batch": 1, "heads": H, "d_latent": 512, "d_rope": 64,
-                   "context": T, "splits": bench.plan.splits, "pdl": bool(args.pdl),
-                   "kernel": "tcgen05" if bench.plan.variant == 2 else "warp-mma",
+        "config": workload_config(world),
+        "launch": {"splits": bench.plan.splits, "pdl": bool(args.pdl),
+                   "kernel": KERNEL_NAMES.get(bench.plan.variant, str(bench.plan.variant)),
                    "calls_per_step": copies,
-                   "l2": f"inputs larger than L2: {copies} distinct caches x {T * ROW_BYTES / 1e6:.2f} MB "
-                         f"= {copies * T * ROW_BYTES / 1e6:.0f} MB (> 3x L2 {l2_bytes() / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}"},
+                   "l2_detail": f"{copies} distinct caches x {T * ROW_BYTES / 1e6:.2f} MB "
+                                f"= {copies * T * ROW_BYTES / 1e6:.0f} MB per step (> 3x L2 {l2_bytes() / 1e6:.0f} MB)"},
         "us_per_call": round(us_call, 4),
         "us_per_call_reps": [round(x, 4) for x in per_call_reps],
         "us_per_call_sd": round(statistics.pstdev(per_call_reps), 4),
@@ -497,8 +586,15 @@ def run_ours(args, rank, world):
     }
     if rank == 0:
         result["e2e"] = e2e_dense(bench, calls=2000)
+        del g, gp, bench
+        torch.cuda.empty_cache()
+        if not args.no_sweep:
+            t0 = time.perf_counter()
+            result["sweep"] = sweep_rows(args, P)
+            result["pdl_ab"] = pdl_ab(args, P)
+            result["sweep_seconds"] = round(time.perf_counter() - t0, 1)
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(bench, args.cpu_seconds)
+            result["cpu_baseline"] = cpu_baseline(cpu_bench, args.cpu_seconds)
         if args.details:
             result["details_file"] = args.details
             write_details(args, P)
@@ -522,9 +618,10 @@ def run_reference(args):
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "dense_t8192", "batch": 1, "heads": H, "context": T, "calls_per_step": 1},
+            "config": workload_config(int(os.environ.get("WORLD_SIZE", "1"))),
             "us_per_call": round(el / steps * 1e6, 1),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(), "nproc": os.cpu_count(),
                              "sample": f"{steps} full calls of dense T={T} H={H}"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -571,6 +668,105 @@ def project_timing(H, V, reps=50):
     del ws
     torch.cuda.empty_cache()
     return {"us": us, "copies": copies, "bytes": wbytes + H * 512 * 4 + H * V * 4}
+
+
+KERNEL_NAMES = {1: "warp-mma", 2: "tcgen05-16", 3: "tcgen05-32", 4: "tcgen05-64"}
+
+
+def sweep_row(name, bench, us, us_part, reps, P, per="call", tensor_bound=False):
+    """One workload's figures: us per call (partial + combine), the partial
+    kernel alone, and both against the roofline (the slower of the bytes at
+    the measured HBM copy bandwidth and, where it binds, the flops at the
+    sustained bf16 tensor rate)."""
+    hbm_us = bench.alg_bytes / (P["hbm_gbs"] * 1e9) * 1e6
+    tensor_us = bench.flops / (P["bf16_tflops_sustained"] * 1e12) * 1e6
+    roof_us = max(hbm_us, tensor_us) if tensor_bound else hbm_us
+    r = {"workload": name, "per": per, "kernel": KERNEL_NAMES.get(bench.plan.variant, str(bench.plan.variant)),
+         "splits": bench.plan.splits, "copies": bench.copies,
+         "us_per_call": round(us, 3), "us_per_call_sd": round(statistics.pstdev(reps), 3),
+         "alg_bytes": int(bench.alg_bytes), "gbs": round(bench.alg_bytes / (us * 1e-6) / 1e9, 1),
+         "roofline_us": round(roof_us, 3), "frac": round(roof_us / us, 4),
+         "frac_8tbs": round(bench.alg_bytes / 8e12 / (us * 1e-6), 4)}
+    if getattr(bench.plan, "flat_ranges", 0):
+        r["flat_ranges"] = bench.plan.flat_ranges
+    if tensor_bound:
+        r["roofline_us_hbm"] = round(hbm_us, 3)
+        r["roofline_us_tensor_sustained"] = round(tensor_us, 3)
+    if us_part is not None:
+        r["us_partial"] = round(us_part, 3)
+        r["partial_gbs"] = round(bench.alg_bytes / (us_part * 1e-6) / 1e9, 1)
+        r["partial_frac"] = round(hbm_us / us_part, 4)
+    return r
+
+
+def sweep_rows(args, P):
+    """The five workloads and the context sweep at H = 16, timed the way the
+    headline is (CUDA graphs of back-to-back calls over distinct inputs that
+    together exceed 3x L2; CUDA events on the launching stream)."""
+    rows = []
+    pdl = bool(args.pdl)
+    for T in (256, 8192, 32768, 65536, 131072):
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, pdl, variant=args.variant)
+        us, usp, reps = time_bench(b, reps=100 if T <= 8192 else 40)
+        rows.append(sweep_row(f"dense_h16_t{T}", b, us, usp, reps, P))
+        del b
+    torch.cuda.empty_cache()
+    b = SparseBench("sparse_k2048", copies_for(2048 * ROW_BYTES), args.splits, pdl, variant=args.variant)
+    us, usp, reps = time_bench(b, reps=100)
+    rows.append(sweep_row("sparse_k2048", b, us, usp, reps, P))
+    del b
+    b = SparseBench("sparse_b64", copies_for(64 * 2048 * ROW_BYTES), args.splits, pdl, variant=args.variant,
+                    device_cache=True)
+    us, usp, reps = time_bench(b, reps=30)
+    rows.append(sweep_row("sparse_b64", b, us, usp, reps, P))
+    del b
+    torch.cuda.empty_cache()
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, pdl, variant=args.variant)
+    us, _, reps = time_graph_bench(gb, reps=5)
+    rows.append(sweep_row("graph_h128", gb, us, None, reps, P, per="decode step per layer (append, partial, "
+                          "combine, advance; 64 steps in one graph)", tensor_bound=True))
+    del gb
+    torch.cuda.empty_cache()
+    return rows
+
+
+def alternate(graphs, calls, reps, inner):
+    """Time each graph `reps` times, the arms alternating; us per call, mean and sem per arm."""
+    out = {k: [] for k in graphs}
+    for g in graphs.values():
+        time_graph(g, 3, 2)
+    for _ in range(reps):
+        for k, g in graphs.items():
+            out[k].append(time_graph(g, inner, 1) / (inner * calls) * 1e6)
+    res = {}
+    for k, v in out.items():
+        res[k] = {"us_per_call": round(statistics.mean(v), 3),
+                  "sem": round(statistics.pstdev(v) / math.sqrt(len(v)), 4), "reps": len(v)}
+    return res
+
+
+def pdl_ab(args, P, reps=12):
+    """Programmatic dependent launch on and off, same plan and inputs, arms
+    alternating in one process: the timing half of the PDL leave-one-out."""
+    rows = []
+    b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), args.splits, True, variant=args.variant)
+    g_on = capture(b.call, b.copies)
+    b.replan(False)
+    g_off = capture(b.call, b.copies)
+    r = alternate({"pdl_on": g_on, "pdl_off": g_off}, b.copies, reps, 20)
+    rows.append({"workload": "dense_h16_t8192", "splits": b.plan.splits, **r,
+                 "pdl_saves_us": round(r["pdl_off"]["us_per_call"] - r["pdl_on"]["us_per_call"], 3)})
+    del b, g_on, g_off
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, True, variant=args.variant)
+    g_on = capture(gb.loop, 1)
+    gb.replan(False)
+    g_off = capture(gb.loop, 1)
+    r = alternate({"pdl_on": g_on, "pdl_off": g_off}, gb.calls, reps, 1)
+    rows.append({"workload": "graph_h128", "per": "decode step per layer", "splits": gb.plan.splits, **r,
+                 "pdl_saves_us": round(r["pdl_off"]["us_per_call"] - r["pdl_on"]["us_per_call"], 3)})
+    del gb, g_on, g_off
+    torch.cuda.empty_cache()
+    return rows
 
 
 def write_details(args, P):
@@ -681,9 +877,11 @@ def main():
     ap.add_argument("--splits", type=int, default=int(os.environ.get("MLA_DECODE_SPLITS", "0")))
     ap.add_argument("--pdl", type=int, default=int(os.environ.get("MLA_DECODE_PDL", "1")))
     ap.add_argument("--variant", type=int, default=int(os.environ.get("MLA_DECODE_VARIANT", "0")),
-                    help="0 = auto (tcgen05), 1 = warp-MMA kernel, 2 = tcgen05 kernel")
+                    help="0 = the planner's choice (warp-MMA for this shape), 1 = warp-MMA kernel, "
+                         "2 / 3 / 4 = tcgen05 kernel with 16 / 32 / 64 heads per CTA")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep and the PDL A/B")
     ap.add_argument("--details", default=None)
     ap.add_argument("--ncu-case", default=None,
                     help="profiling helper: dense_t<T> | dense_h<H>_t<T> | sparse_k2048 | sparse_b64: run --calls eager calls of "

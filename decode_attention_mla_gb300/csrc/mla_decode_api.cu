@@ -174,6 +174,21 @@ int check_shape(const mla_decode_shape* s) {
     return MLA_OK;
 }
 
+// Scratch layout of a plan: the status word at 0, then o_part fp32
+// [B][H][S][512] and lse_part fp32 [B][H][S], each 256-byte aligned.
+struct ScratchLayout {
+    size_t status, o_part, lse_part, bytes;
+};
+ScratchLayout scratch_layout(int batch, int heads, int splits) {
+    const size_t bhs = static_cast<size_t>(batch) * heads * splits;
+    ScratchLayout l;
+    l.status = 0;
+    l.o_part = kScratchAlign;
+    l.lse_part = align_up(l.o_part + bhs * MLA_D_LATENT * sizeof(float), kScratchAlign);
+    l.bytes = align_up(l.lse_part + bhs * sizeof(float), kScratchAlign);
+    return l;
+}
+
 int check_plan(const mla_decode_plan_t* pl) {
     if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
@@ -202,6 +217,12 @@ int check_plan(const mla_decode_plan_t* pl) {
     }
     if (pl->combine_grid_x != mla::combine_grid_rows(pl->shape.batch * pl->shape.heads, pl->splits) ||
         pl->combine_grid_y != MLA_D_LATENT / mla::kCombineChunk || pl->combine_block != mla::combine_block_threads())
+        return MLA_EINVAL;
+    // the kernels write B*H*S partial rows at these offsets: a plan whose
+    // layout does not match its split count would write past the region
+    const ScratchLayout l = scratch_layout(pl->shape.batch, pl->shape.heads, pl->splits);
+    if (pl->status_offset != l.status || pl->o_part_offset != l.o_part || pl->lse_part_offset != l.lse_part ||
+        pl->scratch_bytes != l.bytes)
         return MLA_EINVAL;
     return MLA_OK;
 }
@@ -505,11 +526,11 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
     pl.combine_block = mla::combine_block_threads();
 
-    const size_t bh = static_cast<size_t>(s.batch) * s.heads;
-    pl.status_offset = 0;
-    pl.o_part_offset = kScratchAlign;
-    pl.lse_part_offset = align_up(pl.o_part_offset + bh * pl.splits * MLA_D_LATENT * sizeof(float), kScratchAlign);
-    pl.scratch_bytes = align_up(pl.lse_part_offset + bh * pl.splits * sizeof(float), kScratchAlign);
+    const ScratchLayout l = scratch_layout(s.batch, s.heads, pl.splits);
+    pl.status_offset = l.status;
+    pl.o_part_offset = l.o_part;
+    pl.lse_part_offset = l.lse_part;
+    pl.scratch_bytes = l.bytes;
     *plan = pl;
     return MLA_OK;
 }

@@ -20,7 +20,8 @@ constexpr int kTcGranule = 16;                 // slice granule of the tcgen05 k
 constexpr int kHeadGroup = 16;                 // heads per CTA (warp-MMA kernel; tcgen05 kernel: 16 or 32)
 constexpr int kCombineChunk = 128;             // features per combine CTA
 // Size of the library's own scratch array used by mla_decode_forward_static
-// (8 MiB: e.g. 16 heads x 256 slices x 2 KiB partial rows fits with room).
+// (8 MiB: the status word, B*H*S partial rows of 2 KiB and B*H*S lse values,
+// each region 256-byte aligned; e.g. B = 1, H = 16 up to S = 255).
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 
 // Everything the split partial kernel needs; passed by value.

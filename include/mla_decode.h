@@ -109,7 +109,10 @@ typedef struct {
 /* Launch plan (plain data; copy freely).  The plan is the capture key of a
  * graph: a graph stays valid as long as the plan it was captured with does
  * ("Graph-resident decode", Lecture 08, s.2: splits sizes the grid, so it is
- * decided on the host by the same function the launcher uses). */
+ * decided on the host by the same function the launcher uses).  Every launch
+ * re-derives the grids and the scratch layout from the shape and the split
+ * count and rejects a plan that differs (MLA_EINVAL): edit a plan only through
+ * mla_decode_plan. */
 typedef struct {
     mla_decode_shape shape;
     int magic;                 /* set by mla_decode_plan; checked by every launch */
@@ -223,18 +226,27 @@ MLA_API int mla_decode_forward_step(const mla_decode_plan_t *plan, const mla_dec
 
 /* mla_decode_forward without a caller scratch buffer and without allocating.
  * The pages that define the method have no counterpart of this call: it
- * exists for callers that may not allocate device memory.  The partial and
- * combine kernels run exactly as in mla_decode_forward (same plan, same
- * results bit for bit), but their scratch is an 8 MiB (MLA_STATIC_SCRATCH_BYTES)
- * file-scope __device__ array of the library, one per device; the call makes
- * no cudaMalloc/cudaFree or other allocating call.
+ * exists for callers that may not allocate device memory (code running under
+ * an allocator it does not own, e.g. inside another framework's memory pool
+ * or a plug-in with a fixed memory budget, has no scratch buffer to pass).
+ * The partial and combine kernels run exactly as in mla_decode_forward (same
+ * plan, same results bit for bit), but their scratch is an 8 MiB
+ * (MLA_STATIC_SCRATCH_BYTES) file-scope __device__ array of the library, one
+ * per device context; the call makes no cudaMalloc/cudaFree or other
+ * allocating call.
  *   - Set-up: the first call on a device looks the array's address up
  *     (cudaGetSymbolAddress, with that device current, its return code
- *     checked) and keeps it; make that first call before any stream capture
- *     (a first call on a capturing stream returns MLA_ENOTREADY).
+ *     checked) and keeps it with the id of the current CUDA context; make that
+ *     first call before any stream capture (a first call on a capturing stream
+ *     returns MLA_ENOTREADY).  A call made in another context than the one of
+ *     the lookup (e.g. after cudaDeviceReset, which ends the primary context
+ *     and with it the array) looks the address up again, so it too must be
+ *     made outside capture.
  *   - Size: a plan whose scratch_bytes exceeds MLA_STATIC_SCRATCH_BYTES is
  *     rejected with MLA_ESTATICLIMIT before anything is launched; use
- *     mla_decode_forward with a caller buffer for such plans.
+ *     mla_decode_forward with a caller buffer for such plans.  scratch_bytes
+ *     is 256 + align256(B*H*S*2048) + align256(B*H*S*4): e.g. B = 1, H = 16
+ *     fits up to S = 255, H = 128 up to S = 31.
  *   - Zero start: only the status word (offset 0) must start at zero; the
  *     array is zero when the library's module is loaded.  A device-side
  *     wait timeout sets it and nothing here clears it or reports it.  The

@@ -386,6 +386,26 @@ def test_launch_argument_checks(fn):
     assert _call(fn, ps, _args(indices=0x70002, cache_len=0x71000, row_offset=0x72000)) == mla.EALIGN
 
 
+@pytest.mark.parametrize("fn", ["mla_decode_run", "mla_decode_combine", "mla_decode_forward"])
+def test_launch_rejects_a_plan_whose_scratch_layout_is_stale(fn):
+    """A plan edited to hold more slices (its grids updated to match) but whose
+    scratch layout was left as planned would make the kernels write partial
+    rows past the region it claims: every launch re-derives the layout."""
+    p = _plan(max_ctx=8192, splits=64)
+    q = _plan(max_ctx=8192, splits=128)
+    bad = mla.Plan.from_buffer_copy(p)
+    bad.splits, bad.grid_x, bad.combine_grid_x = q.splits, q.grid_x, q.combine_grid_x
+    assert bad.scratch_bytes < q.scratch_bytes
+    assert _call(fn, bad, _args(), nbytes=q.scratch_bytes) == mla.EINVAL
+    for field in ("scratch_bytes", "o_part_offset", "lse_part_offset", "status_offset"):
+        bad = mla.Plan.from_buffer_copy(p)
+        setattr(bad, field, getattr(bad, field) + 256)
+        assert _call(fn, bad, _args(), nbytes=1 << 30) == mla.EINVAL, field
+    # the same edit with the layout re-derived as the planner does is a valid plan
+    ok = mla.Plan.from_buffer_copy(q)
+    assert _call(fn, ok, _args(), scratch=0, nbytes=q.scratch_bytes) == mla.ESCRATCH
+
+
 def test_append_advance_argument_checks():
     L = mla.lib()
     assert L.mla_decode_append(None, 10, 576, ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), None, 1, None) == mla.EINVAL

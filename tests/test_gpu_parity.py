@@ -202,19 +202,19 @@ def test_sparse_equals_dense_on_permutation():
     assert ((ld - ls).abs() / ld.abs().clamp(min=1)).max().item() <= 2 * _gpu.LSE_RTOL
 
 
-def test_sparse_b64_workload_sampled():
-    """Full-size ragged batch (~5 GB cache) on the GPU; the oracle checks a sample of requests."""
+def test_sparse_b64_workload_all_requests():
+    """Full-size ragged batch (~5 GB cache, 64 requests of top-2048 lists) on the
+    GPU, every request of the batch against the oracle, element by element, for
+    each kernel variant."""
     x = workloads.make("sparse_b64")
     d = _gpu.dev()
     kv_dev = x.kv.to(d)
-    sample = [0, 1, 17, 31, 42, 63]
-    sub = workloads.SparseInputs(q=x.q[sample], kv=x.kv, indices=x.indices[sample], cache_len=x.cache_len[sample],
-                                 row_offset=x.row_offset[sample])
-    ro, rl = _gpu.oracle_sparse(sub)
+    ro, rl = _gpu.oracle_sparse(x)
+    assert ro.shape == (64, 16, 512)
     for variant in _gpu.VARIANTS:
         out, lse, plan, scratch = _gpu.run_sparse(x, kv_dev=kv_dev, variant=variant)
         assert mla.status_word(plan, scratch) == 0
-        _gpu.assert_parity(out[sample], lse[sample], ro, rl, f"sparse_b64 sample, variant {variant}")
+        _gpu.assert_parity(out, lse, ro, rl, f"sparse_b64 all 64 requests, variant {variant}")
     del kv_dev
 
 

@@ -36,6 +36,31 @@ def test_static_rejects_plans_beyond_the_limit():
     assert _static(big, _fake_args(q=0x10002)) == mla.EALIGN
 
 
+def test_static_limit_boundary():
+    """256 + align256(B*H*S*2048) + align256(B*H*S*4) bytes: B = 1, H = 16 fits up
+    to S = 255; S = 256 is refused on the host, before any CUDA call."""
+    fits = mla.plan(batch=1, heads=16, max_ctx=131072, scale=0.05, splits=255, num_sms=152)
+    over = mla.plan(batch=1, heads=16, max_ctx=131072, scale=0.05, splits=256, num_sms=152)
+    assert fits.scratch_bytes == 256 + 255 * 16 * 2048 + -(-255 * 16 * 4 // 256) * 256
+    assert fits.scratch_bytes <= mla.STATIC_SCRATCH_BYTES < over.scratch_bytes
+    assert _static(over, _fake_args()) == mla.ESTATICLIMIT
+    h128 = [mla.plan(batch=1, heads=128, max_ctx=131072, scale=0.05, splits=s, num_sms=152, variant=1)
+            for s in (31, 32)]
+    assert h128[0].scratch_bytes <= mla.STATIC_SCRATCH_BYTES < h128[1].scratch_bytes
+    assert _static(h128[1], _fake_args()) == mla.ESTATICLIMIT
+
+
+def test_static_rejects_a_stale_plan_layout():
+    """A plan whose split count (and grids) grew while scratch_bytes stayed as
+    planned is refused before the size check could let it write past the array."""
+    small = mla.plan(batch=1, heads=16, max_ctx=8192, scale=0.05, splits=64, num_sms=152)
+    big = mla.plan(batch=1, heads=16, max_ctx=8192, scale=0.05, splits=256, num_sms=152)
+    bad = mla.Plan.from_buffer_copy(small)
+    bad.splits, bad.grid_x, bad.combine_grid_x = big.splits, big.grid_x, big.combine_grid_x
+    assert bad.scratch_bytes <= mla.STATIC_SCRATCH_BYTES < big.scratch_bytes
+    assert _static(bad, _fake_args()) == mla.EINVAL
+
+
 def test_static_limit_matches_the_header():
     import re
     from pathlib import Path

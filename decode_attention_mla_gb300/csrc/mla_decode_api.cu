@@ -28,13 +28,15 @@ constexpr int kVariantWarpMma = 1;           // mma.sync head-group-16 kernel, 6
 constexpr int kVariantTc = 2;                // tcgen05 head-group-16 kernel, 80-row tiles
 constexpr int kVariantTc32 = 3;              // tcgen05 head-group-32 kernel, 64-row tiles (dense)
 constexpr int kVariantTc64 = 4;              // tcgen05 head-group-64 kernel, 64-row tiles (dense)
+constexpr int kVariantMmaTcPv = 5;           // warp-MMA kernel with P . V on tcgen05 (dense bf16)
 
 int variant_tile_rows(int v) {
     // warp-MMA: the model counts 32-row slots (a 64-row step costs about two)
     return v == kVariantTc ? mla::kTcTileRows : (v == kVariantTc32 || v == kVariantTc64) ? mla::kTcTileRows32
                                                                                           : mla::kStageRows;
 }
-int variant_granule(int v) { return v == kVariantWarpMma ? mla::kStageRows : mla::kTcGranule; }
+bool variant_is_mma(int v) { return v == kVariantWarpMma || v == kVariantMmaTcPv; }
+int variant_granule(int v) { return variant_is_mma(v) ? mla::kStageRows : mla::kTcGranule; }
 int variant_head_group(int v) { return v == kVariantTc64 ? 64 : v == kVariantTc32 ? 32 : mla::kHeadGroup; }
 bool variant_is_tc(int v) { return v == kVariantTc || v == kVariantTc32 || v == kVariantTc64; }
 
@@ -158,7 +160,7 @@ int check_shape(const mla_decode_shape* s) {
     if (s->pdl != 0 && s->pdl != 1) return MLA_EINVAL;
     if (s->stall_test != 0 && s->stall_test != 1) return MLA_EINVAL;
     if (s->kv_fp8 != 0 && s->kv_fp8 != 1) return MLA_EINVAL;
-    if (s->variant < 0 || s->variant > 4) return MLA_EINVAL;
+    if (s->variant < 0 || s->variant > 5) return MLA_EINVAL;
     if (s->num_sms < 0 || s->splits_override < 0 || s->splits_override > MLA_MAX_SPLITS) return MLA_EINVAL;
     if (!(s->scale > 0.f) || !std::isfinite(s->scale)) return MLA_EINVAL;
     if (!s->sparse && s->max_ctx < 1) return MLA_EINVAL;
@@ -171,6 +173,8 @@ int check_shape(const mla_decode_shape* s) {
     if (s->variant == kVariantTc64 && (s->sparse || s->heads % 64 != 0)) return MLA_EUNSUPPORTED;
     // E4M3 cache: dense decode on the warp-MMA kernel
     if (s->kv_fp8 && (s->sparse || (s->variant != 0 && s->variant != kVariantWarpMma))) return MLA_EUNSUPPORTED;
+    // P . V on tcgen05 reads V in place from the swizzled dense slots: dense bf16 only
+    if (s->variant == kVariantMmaTcPv && (s->sparse || s->kv_fp8)) return MLA_EUNSUPPORTED;
     return MLA_OK;
 }
 
@@ -193,8 +197,11 @@ int check_plan(const mla_decode_plan_t* pl) {
     if (!pl || pl->magic != kPlanMagic) return MLA_EINVAL;
     if (check_shape(&pl->shape) != MLA_OK) return MLA_EINVAL;
     if (pl->splits < 1 || pl->splits > MLA_MAX_SPLITS) return MLA_EINVAL;
-    if (pl->variant != kVariantWarpMma && !variant_is_tc(pl->variant)) return MLA_EINVAL;
-    if ((pl->variant == kVariantTc32 || pl->variant == kVariantTc64) && pl->shape.sparse) return MLA_EINVAL;
+    if (!variant_is_mma(pl->variant) && !variant_is_tc(pl->variant)) return MLA_EINVAL;
+    if ((pl->variant == kVariantTc32 || pl->variant == kVariantTc64 || pl->variant == kVariantMmaTcPv) &&
+        pl->shape.sparse)
+        return MLA_EINVAL;
+    if (pl->variant == kVariantMmaTcPv && pl->shape.kv_fp8) return MLA_EINVAL;
     if (pl->head_group != variant_head_group(pl->variant) || pl->n_head_groups * pl->head_group != pl->shape.heads)
         return MLA_EINVAL;
     const long long items = static_cast<long long>(pl->shape.batch) * pl->n_head_groups * pl->splits;
@@ -313,6 +320,7 @@ int do_run(const mla_decode_plan_t* pl, const mla_decode_args* a, void* scratch,
     p.status = reinterpret_cast<int*>(base + pl->status_offset);
     p.stall_test = pl->shape.stall_test;
     p.new_rows = up ? up->new_rows : nullptr;
+    p.tc_pv = pl->variant == kVariantMmaTcPv ? 1 : 0;
     const dim3 grid(pl->grid_x, pl->grid_y, pl->grid_z);
     if (variant_is_tc(pl->variant)) {
         // TMA coordinates are 32-bit: the cache must be addressable by them
@@ -521,7 +529,7 @@ int mla_decode_plan(const mla_decode_shape* shape, mla_decode_plan_t* plan) {
     const bool tc = variant_is_tc(pl.variant);
     pl.block = tc ? mla::partial_tc_block_threads(pl.head_group) : mla::partial_mma_block_threads();
     pl.smem_bytes = static_cast<int>(tc ? mla::partial_tc_smem_bytes(pl.head_group)
-                                        : mla::partial_mma_smem_bytes(s.kv_fp8 != 0));
+                                        : mla::partial_mma_smem_bytes(s.kv_fp8 != 0, pl.variant == kVariantMmaTcPv));
     pl.combine_grid_x = mla::combine_grid_rows(s.batch * s.heads, pl.splits);
     pl.combine_grid_y = MLA_D_LATENT / mla::kCombineChunk;
     pl.combine_block = mla::combine_block_threads();

@@ -60,6 +60,9 @@ struct PartialParams {
     // multiplies O by it.  v_scale = 1 for bf16 caches.
     int kv_fp8;
     float v_scale;
+    // dense bf16 cache on the warp-MMA kernel: 1 = P . V on the tcgen05 tensor
+    // cores (O in tensor memory), 0 = P . V on the warps (mma.sync)
+    int tc_pv;
 };
 
 struct CombineParams {
@@ -117,7 +120,7 @@ struct TcMaps {
 
 // Launch helpers (each returns the cudaError_t of the launch).
 cudaError_t partial_mma_prepare(int device);
-size_t partial_mma_smem_bytes(bool fp8 = false);
+size_t partial_mma_smem_bytes(bool fp8 = false, bool tc_pv = false);
 int partial_mma_block_threads();
 cudaError_t partial_mma_occupancy(int* ctas_per_sm);
 cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 grid, bool pdl, cudaStream_t stream);

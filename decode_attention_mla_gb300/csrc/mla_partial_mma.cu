@@ -47,6 +47,7 @@
 // its copies before it exits.
 #include <cfloat>
 #include <cmath>
+#include <cstddef>
 #include <type_traits>
 
 #include "device_utils.cuh"
@@ -132,11 +133,31 @@ struct Fp8Stage {
 };
 struct NoFp8Stage {};
 
-template <bool kDense, bool kFp8 = false>
+// P . V on the 5th-generation tensor cores (dense bf16 cache): per group, P^T
+// of its slot as the K-major B operand ([P_hi | P_lo]: 32 lines of 128 bytes,
+// line h = P_hi of head h, line 16 + h = P_lo; the two P buffers of a group
+// are K positions 0-31 and 32-63 of the same lines, 128-byte swizzled), and
+// the tensor-memory bookkeeping.  O^T of group g, feature block j (features
+// 128j .. 128j+127 = tensor-memory lanes 0-127) is columns 128g + 32j ..
+// +31: [O_hi | O_lo] of the 16 heads.
+constexpr int kPtBytes = 32 * 128;
+constexpr uint32_t kTmemCols = 256;
+struct __align__(1024) TcPvStage {
+    uint8_t pt[kGroups][kPtBytes];                         // P^T per group (1024-byte aligned)
+    uint64_t pv_done[kGroups][2];                          // a group's P . V MMAs of P buffer b completed
+    uint64_t drain[kGroups];                               // every MMA of the group completed (exit)
+    float merge_m[kGroups][kHeadGroup];                    // each group's reference and row sum, per head
+    float merge_l[kGroups][kHeadGroup];
+    uint32_t tmem_base;
+};
+struct NoTcPvStage {};
+
+template <bool kDense, bool kFp8 = false, bool kTcPv = false>
 struct __align__(1024) SharedStorage {
     static constexpr int kSlotBytes = kDense ? kDenseSlotBytes : kSparseSlotBytes;
     uint8_t q[kChunks * kQChunkBytes];                     // the item's 16 query rows (1024-byte aligned)
     uint8_t kv[kSlots][kSlotBytes];                        // ring of 32-row slots
+    std::conditional_t<kTcPv, TcPvStage, NoTcPvStage> tc;  // dense bf16 cache, P . V on tcgen05
     uint4 p[kGroups][2][kSlotTiles][32];                   // P of a group's slot as mma A fragments, double-buffered
     float4 red[kGroups][2][2][32];                         // half-contraction scores exchanged in each pair
     float mx[kGroups][kGroupWarps][kHeadGroup];            // per-warp head maxima (reference moves)
@@ -379,8 +400,8 @@ __device__ void prefetch_first_slots(const TcMaps& maps, const PartialParams& p)
 
 // wp: producer warp (0 .. kProdWarps-1); dense slices use warp 0 alone, which
 // also stages the query tiles.
-template <bool kDense>
-__device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStorage<kDense>& sh, int wp, int lane) {
+template <bool kDense, class S>
+__device__ void producer(const TcMaps& maps, const PartialParams& p, S& sh, int wp, int lane) {
     const uint64_t policy = l2_policy_evict_first();
     int stage = 0;            // slots issued so far (ring position)
     // the first query tile is requested before the item is decoded (its key
@@ -463,6 +484,7 @@ __device__ void producer(const TcMaps& maps, const PartialParams& p, SharedStora
                         st_shared_v4(row + (u >> 3) * kDenseChunkBytes + (((u & 7) ^ (patch_r & 7)) << 4), v.x, v.y,
                                      v.z, v.w);
                     }
+                    fence_proxy_async_smem();   // the tensor cores may read the slot next
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.full[slot][0]);
                 } else {
@@ -1142,18 +1164,412 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
     if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
 }
 
-template <bool kDense, bool kFp8 = false>
+// ---- dense bf16 cache: scores on the warps, P . V on tcgen05 ---------------
+// The MMA warps compute the scores and the softmax exactly as above, write P
+// of their slot as the bf16 pair [P_hi | P_lo]^T into the group's P^T buffer,
+// and one thread of the group issues the slot's P . V on the tensor cores:
+//   O^T[512 x 32] += V_slot^T[512 x 32 rows] . [P_hi | P_lo]^T
+// as 4 feature blocks (M = 128) x 2 k-steps of 16 rows (N = 32), V read in
+// place from the slot (MN-major: 64-feature atoms one 4096-byte chunk apart),
+// O in tensor memory.  The MMAs' completion releases the slot to the
+// producer and the P buffer to the group, so the warps never wait for P . V
+// within an item.  At the end of an item every MMA warp merges both groups'
+// O straight from tensor memory (its own lane quarter, two feature blocks).
+__device__ __forceinline__ uint32_t pt_off(int n, int k) {
+    return static_cast<uint32_t>((n >> 3) * 1024 + (n & 7) * 128 + ((((k >> 3) ^ (n & 7))) << 4) + (k & 7) * 2);
+}
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+template <class S>
+__device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
+    constexpr uint32_t kSlotBytes = kDenseSlotBytes;
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    const int grp = w / kGroupWarps;
+    const int gw = w % kGroupWarps;          // also this warp's tensor-memory lane quarter (w % 4)
+    const int pr = gw >> 1;
+    const int kh = gw & 1;
+    const int my_tile = 2 * pr + kh;
+    const int r_own = 8 * my_tile + 2 * tq;
+    const int lrow = lane & 7;
+    const int lmat = lane >> 3;
+    const int bar_pair = kBarPair0 + 2 * grp + pr;
+    const int bar_group = kBarGroup0 + grp;
+    const uint32_t q_base = smem_u32(sh.q);
+    const uint32_t kv_base = smem_u32(sh.kv[0]);
+    const int qk_row = 16 * pr + lrow + ((lmat >> 1) << 3);
+    const uint32_t qk_off[2] = {qk_lane_off<true>(qk_row, kh, 0, lmat), qk_lane_off<true>(qk_row, kh, 1, lmat)};
+    const bool issuer = gw == 0 && lane == 0;   // issues the group's P . V
+
+    // tensor memory: kTmemCols columns for the CTA (one CTA per SM)
+    if (w == 0) {
+        tmem_alloc(&sh.tc.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    named_barrier_sync(kBarMma, kMmaThreads);
+    tc_fence_after_sync();
+    const uint32_t tmem = sh.tc.tmem_base;
+    const uint32_t tmem_lane = static_cast<uint32_t>(32 * gw) << 16;
+    const uint32_t tmem_grp = tmem + 128u * static_cast<uint32_t>(grp);
+
+    const uint32_t pt_base = smem_u32(sh.tc.pt[grp]);
+    // lines g, 8 + g, 16 + g, 24 + g (P_hi of heads g and g + 8, then P_lo) share
+    // a swizzle and lie 1024 bytes apart; K position 32 * buffer + r_own
+    const uint32_t pt_lane0 = pt_base + pt_off(g, r_own);
+    const uint32_t pt_lane1 = pt_base + pt_off(g, 32 + r_own);
+    const uint32_t idesc = make_idesc_bf16(128, 32, 1, 0);
+    const uint64_t v_desc0 = make_sdesc(kv_base, kDenseChunkBytes, 1024, kLayoutSw128);
+    const uint64_t p_desc0 = make_sdesc(pt_base, 16, 1024, kLayoutSw128);
+
+    uint32_t qa[kKHalf][4];
+    int stage = 0;
+    int q_phase = 0;
+    int q_key = first_key<true>(p);
+    bool q_in_regs = false;
+    bool failed = false;
+    bool stop = false;
+    int issued = 0;                         // P . V batches this warp's group issued so far
+    int issued_other = 0;                   // ... and the other group
+
+    for (int item = blockIdx.x; item < p.n_items && !stop; item += gridDim.x) {
+        const Item it = decode_item<true>(p, item);
+        const long long row_b = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits;
+        if (it.n_slots == 0) {
+            write_empty_partial(p.o_part, p.lse_part, row_b + it.s, p.splits, w * 32 + lane, kMmaThreads);
+            continue;
+        }
+        const int key = it.b * p.n_groups + it.hg;
+        if (key != q_key) {
+            if (!q_in_regs && !failed) {
+                if (warp_wait(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
+                    if (lane == 0) mbar_arrive(&sh.q_empty);
+                } else {
+                    failed = true;
+                }
+            }
+            ++q_phase;
+            q_key = key;
+            q_in_regs = false;
+        }
+        if (!q_in_regs && !failed) {
+            if (warp_wait(&sh.q_full, q_phase & 1, &sh.abort_flag)) {
+#pragma unroll
+                for (int kk = 0; kk < kKHalf; ++kk)
+                    ldmatrix_x4(qa[kk], q_base + sw_off(lrow + ((lmat & 1) << 3),
+                                                         (4 * (kk >> 1) + 2 * kh + (kk & 1)) * 32 + ((lmat >> 1) << 4),
+                                                         kQChunkBytes));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.q_empty);
+                q_in_regs = true;
+            } else {
+                failed = true;
+            }
+        }
+
+        float m_ref[2] = {-INFINITY, -INFINITY};
+        float l_own[2] = {0.f, 0.f};
+        const int my_slots = it.n_slots > grp ? (it.n_slots - grp + 1) / 2 : 0;
+        bool gstop = false;
+        for (int k = 0; k < my_slots && !gstop; ++k) {
+            const int j = grp + 2 * k;
+            const int st = stage + j;
+            const int slot = st % kSlots;
+            if (!failed && !warp_wait(&sh.full[slot][0], (st / kSlots) & 1, &sh.abort_flag)) failed = true;
+            const uint32_t e_slot = it.e0 + static_cast<uint32_t>(j * kStageRows);
+            const int v_hi = static_cast<int>(min(it.e1 - e_slot, static_cast<uint32_t>(kStageRows)));
+            const long long first_row = it.base + e_slot;
+            const int v_lo =
+                first_row >= 0 ? 0 : first_row <= -kStageRows ? kStageRows : static_cast<int>(-first_row);
+            const uint32_t sbase = kv_base + static_cast<uint32_t>(slot) * kSlotBytes;
+            const int pb = issued & 1;
+            const uint32_t pt_w = pb ? pt_lane1 : pt_lane0;
+            const int ksteps = (v_hi + 15) >> 4;
+
+            // ---- scores of this warp's 8-row tile: two contraction halves ------
+            float acc[2][4];
+            qk_scores<true>(acc, qa, sbase, qk_off, !failed);
+            sh.red[grp][pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
+            named_barrier_sync(bar_pair, 64);
+            const float4 other = sh.red[grp][pr][kh][lane];
+            const float4 mine = kh ? as_float4(acc[1]) : as_float4(acc[0]);
+            const bool v0 = r_own >= v_lo && r_own < v_hi;
+            const bool v1 = r_own + 1 >= v_lo && r_own + 1 < v_hi;
+            float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (!failed) {
+                sc[0] = v0 ? (mine.x + other.x) * p.scale_log2 : -INFINITY;
+                sc[1] = v1 ? (mine.y + other.y) * p.scale_log2 : -INFINITY;
+                sc[2] = v0 ? (mine.z + other.z) * p.scale_log2 : -INFINITY;
+                sc[3] = v1 ? (mine.w + other.w) * p.scale_log2 : -INFINITY;
+            }
+            float mx0 = fmaxf(sc[0], sc[1]);
+            float mx1 = fmaxf(sc[2], sc[3]);
+
+            // the P buffer's batch before last must have been read by the tensor cores
+            if (issued >= 2 && !failed && !warp_wait(&sh.tc.pv_done[grp][pb], ((issued >> 1) - 1) & 1, &sh.abort_flag))
+                failed = true;
+            // rows past the slice end that the P . V k-steps read may hold anything
+            // (NaN too): zero their latent features (their scores are masked, so a
+            // score computed from half-zeroed bytes is discarded)
+            if (v_hi < 16 * ksteps) {
+                const int n_units = (16 * ksteps - v_hi) * 64;   // 8 chunks x 8 units per row
+                for (int u = gw * 32 + lane; u < n_units; u += kGroupThreads) {
+                    const int r = v_hi + (u >> 6);
+                    st_shared_v4_zero(sbase + ((u >> 3) & 7) * kDenseChunkBytes + r * 128 + (u & 7) * 16);
+                }
+                fence_proxy_async_smem();
+            }
+
+            // ---- P against the group's reference; move it only when needed ----
+            float pv[4];
+            bool need = true;
+            if (k > 0) {
+                const float ref0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
+                const float ref1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
+                pv[0] = ex2_approx(sc[0] - ref0);
+                pv[1] = ex2_approx(sc[1] - ref0);
+                pv[2] = ex2_approx(sc[2] - ref1);
+                pv[3] = ex2_approx(sc[3] - ref1);
+                uint32_t hi0, lo0, hi1, lo1;
+                split_bf16x2(pv[0], pv[1], hi0, lo0);
+                split_bf16x2(pv[2], pv[3], hi1, lo1);
+                st_shared_b32(pt_w, hi0);
+                st_shared_b32(pt_w + 1024, hi1);
+                st_shared_b32(pt_w + 2048, lo0);
+                st_shared_b32(pt_w + 3072, lo1);
+                fence_proxy_async_smem();
+                const bool over = mx0 > m_ref[0] + kRescaleThreshold || mx1 > m_ref[1] + kRescaleThreshold;
+                need = named_barrier_or(bar_group, kGroupThreads, over || failed);
+            }
+            if (need) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                if (tq == 0) {
+                    sh.mx[grp][gw][g] = mx0;
+                    sh.mx[grp][gw][g + 8] = mx1;
+                }
+                if (named_barrier_or(bar_group, kGroupThreads, failed)) {
+                    gstop = true;
+                    break;
+                }
+                float n0 = m_ref[0], n1 = m_ref[1];
+#pragma unroll
+                for (int v = 0; v < kGroupWarps; ++v) {
+                    n0 = fmaxf(n0, sh.mx[grp][v][g]);
+                    n1 = fmaxf(n1, sh.mx[grp][v][g + 8]);
+                }
+                if (k > 0) {
+                    // what was accumulated against the old reference, scaled to the new
+                    // one: O^T in tensor memory once the group's last batch is done
+                    const float a0 = m_ref[0] == -INFINITY ? 0.f : ex2_approx(m_ref[0] - n0);
+                    const float a1 = m_ref[1] == -INFINITY ? 0.f : ex2_approx(m_ref[1] - n1);
+                    l_own[0] *= a0;
+                    l_own[1] *= a1;
+                    const int last = issued - 1;
+                    if (!warp_wait(&sh.tc.pv_done[grp][last & 1], (last >> 1) & 1, &sh.abort_flag)) failed = true;
+                    tc_fence_after_sync();
+                    if (!failed) {
+                        float al[kHeadGroup];
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) {
+                            al[h] = __shfl_sync(0xffffffffu, a0, 4 * h);
+                            al[h + 8] = __shfl_sync(0xffffffffu, a1, 4 * h);
+                        }
+#pragma unroll 1
+                        for (int blk = 0; blk < 4; ++blk) {
+                            float v[32];
+                            const uint32_t ta = tmem_grp + tmem_lane + 32u * blk;
+                            tmem_ld32(ta, v);
+                            float v_hi16[16], v_lo16[16];
+#pragma unroll
+                            for (int h = 0; h < kHeadGroup; ++h) {
+                                v_hi16[h] = v[h] * al[h];
+                                v_lo16[h] = v[16 + h] * al[h];
+                            }
+                            tmem_st16(ta, v_hi16);
+                            tmem_st16(ta + 16, v_lo16);
+                        }
+                    }
+                    tc_fence_before_sync();
+                }
+                m_ref[0] = n0;
+                m_ref[1] = n1;
+                const float ref0 = n0 == -INFINITY ? 0.f : n0;
+                const float ref1 = n1 == -INFINITY ? 0.f : n1;
+                pv[0] = ex2_approx(sc[0] - ref0);
+                pv[1] = ex2_approx(sc[1] - ref0);
+                pv[2] = ex2_approx(sc[2] - ref1);
+                pv[3] = ex2_approx(sc[3] - ref1);
+                uint32_t hi0, lo0, hi1, lo1;
+                split_bf16x2(pv[0], pv[1], hi0, lo0);
+                split_bf16x2(pv[2], pv[3], hi1, lo1);
+                st_shared_b32(pt_w, hi0);
+                st_shared_b32(pt_w + 1024, hi1);
+                st_shared_b32(pt_w + 2048, lo0);
+                st_shared_b32(pt_w + 3072, lo1);
+                fence_proxy_async_smem();
+                if (named_barrier_or(bar_group, kGroupThreads, failed)) {
+                    gstop = true;
+                    break;
+                }
+            }
+            l_own[0] += pv[0] + pv[1];
+            l_own[1] += pv[2] + pv[3];
+
+            // ---- O^T += V^T . [P_hi | P_lo]^T on the tensor cores ---------------
+            if (issuer) {
+                tc_fence_after_sync();
+                const uint64_t vb = v_desc0 + ((static_cast<uint32_t>(slot) * kSlotBytes) >> 4);
+                const uint64_t pbd = p_desc0 + ((static_cast<uint32_t>(pb) * 64u) >> 4);
+#pragma unroll
+                for (int jb = 0; jb < 4; ++jb) {
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        if (kk < ksteps)
+                            umma_bf16(tmem_grp + 32u * jb,
+                                      vb + ((static_cast<uint32_t>(2 * jb * kDenseChunkBytes + kk * 2048)) >> 4),
+                                      pbd + ((static_cast<uint32_t>(kk) * 32u) >> 4), idesc,
+                                      (k == 0 && kk == 0) ? 0u : 1u);
+                    }
+                }
+                umma_commit(&sh.empty[slot]);
+                umma_commit(&sh.tc.pv_done[grp][pb]);
+            }
+            __syncwarp();
+            ++issued;
+        }
+        // the other group's batches of this item (every thread follows both counts)
+        issued_other += grp == 0 ? it.n_slots / 2 : (it.n_slots + 1) / 2;
+
+        // ---- epilogue ---------------------------------------------------------
+        float l0 = l_own[0], l1 = l_own[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (tq == 0) {
+            sh.lsum[grp][gw][g] = l0;
+            sh.lsum[grp][gw][g + 8] = l1;
+        }
+        if (named_barrier_or(kBarMma, kMmaThreads, failed || gstop)) {
+            stop = true;
+            break;
+        }
+        if (gw == 0 && tq == 0) {
+            float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+            for (int v = 0; v < kGroupWarps; ++v) {
+                L0 += sh.lsum[grp][v][g];
+                L1 += sh.lsum[grp][v][g + 8];
+            }
+            sh.tc.merge_m[grp][g] = m_ref[0];
+            sh.tc.merge_m[grp][g + 8] = m_ref[1];
+            sh.tc.merge_l[grp][g] = L0;
+            sh.tc.merge_l[grp][g + 8] = L1;
+        }
+        named_barrier_sync(kBarMma, kMmaThreads);
+        // merge weights of head (lane & 15): group 1 holds rows only with two or more slots
+        const bool two = it.n_slots > 1;
+        const long long row_h0 = row_b + it.s;
+        float c0_l, c1_l;
+        {
+            const int h = lane & 15;
+            const float m0 = sh.tc.merge_m[0][h];
+            const float m1 = two ? sh.tc.merge_m[1][h] : -INFINITY;
+            const float mm = fmaxf(m0, m1);
+            const float s0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+            const float s1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+            const float L = sh.tc.merge_l[0][h] * s0 + (two ? sh.tc.merge_l[1][h] * s1 : 0.f);
+            const float inv = L > 0.f ? rcp_approx(L) * p.v_scale : 0.f;
+            c0_l = s0 * inv;
+            c1_l = s1 * inv;
+            if (w == 0 && lane < 16)
+                p.lse_part[row_h0 + static_cast<long long>(h) * p.splits] =
+                    L > 0.f ? (mm + lg2_approx(L)) * kLn2 : -INFINITY;
+        }
+        // every P . V batch of both groups has completed (group 0 has at least one)
+        if (!failed) {
+            const int last0 = (grp == 0 ? issued : issued_other) - 1;
+            if (!warp_wait(&sh.tc.pv_done[0][last0 & 1], (last0 >> 1) & 1, &sh.abort_flag)) failed = true;
+        }
+        if (two && !failed) {
+            const int last1 = (grp == 1 ? issued : issued_other) - 1;
+            if (!warp_wait(&sh.tc.pv_done[1][last1 & 1], (last1 >> 1) & 1, &sh.abort_flag)) failed = true;
+        }
+        tc_fence_after_sync();
+        if (!failed) {
+            // this warp: lane quarter gw of feature blocks 2 grp, 2 grp + 1
+#pragma unroll 1
+            for (int jj = 0; jj < 2; ++jj) {
+                const int jb = 2 * grp + jj;
+                float a[32], b[32];
+                tmem_ld32(tmem + tmem_lane + 32u * jb, a);
+                if (two) {
+                    tmem_ld32(tmem + 128u + tmem_lane + 32u * jb, b);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) b[i] = 0.f;
+                }
+                float* dst = p.o_part + row_h0 * kDLatent + 128 * jb + 32 * gw + lane;
+#pragma unroll
+                for (int h = 0; h < kHeadGroup; ++h) {
+                    const float c0 = __shfl_sync(0xffffffffu, c0_l, h);
+                    const float c1 = __shfl_sync(0xffffffffu, c1_l, h);
+                    dst[static_cast<long long>(h) * p.splits * kDLatent] =
+                        (a[h] + a[16 + h]) * c0 + (b[h] + b[16 + h]) * c1;
+                }
+            }
+        }
+        // every tensor-memory read of this item precedes the next item's MMAs
+        tc_fence_before_sync();
+        if (named_barrier_or(kBarMma, kMmaThreads, failed)) {
+            stop = true;
+            break;
+        }
+        stage += it.n_slots;
+    }
+    if ((stop || failed) && lane == 0) raise_device_error(sh, p.status);
+    // no MMA in flight once the CTA frees its tensor memory
+    if (issuer) {
+        umma_commit(&sh.tc.drain[grp]);
+        volatile int never = 0;
+        if (!mbar_wait_bounded(&sh.tc.drain[grp], 0, &never)) raise_device_error(sh, p.status);
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    named_barrier_sync(kBarMma, kMmaThreads);
+    if (w == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool kDense, bool kFp8 = false, bool kTcPv = false>
 __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __grid_constant__ TcMaps maps,
                                                                        const PartialParams p) {
+    static_assert(!kTcPv || (kDense && !kFp8), "tcgen05 P . V: dense bf16 cache");
+    using S = SharedStorage<kDense, kFp8, kTcPv>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SharedStorage<kDense, kFp8>& sh = *reinterpret_cast<SharedStorage<kDense, kFp8>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    S& sh = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
             for (int q = 0; q < (kDense ? 1 : kProdWarps); ++q) mbar_init(&sh.full[i][q], 1);
-            mbar_init(&sh.empty[i], kGroupWarps);   // the group that consumed the slot
+            // released by the group that consumed the slot (its four warps, or
+            // the commit of its P . V MMAs)
+            mbar_init(&sh.empty[i], kTcPv ? 1 : kGroupWarps);
+        }
+        if constexpr (kTcPv) {
+            for (int gg = 0; gg < kGroups; ++gg) {
+                mbar_init(&sh.tc.pv_done[gg][0], 1);
+                mbar_init(&sh.tc.pv_done[gg][1], 1);
+                mbar_init(&sh.tc.drain[gg], 1);
+            }
         }
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, kComputeWarps);
@@ -1195,42 +1611,51 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         warpgroup_regs_increase<RegSplit<kFp8>::kMma>();
         grid_dependency_wait();
         allow_dependent_launch();
-        consumer<kDense, kFp8>(p, sh, warp, lane);
+        if constexpr (kTcPv)
+            consumer_tcpv(p, sh, warp, lane);
+        else
+            consumer<kDense, kFp8>(p, sh, warp, lane);
     }
 }
 
-template <bool kDense, bool kFp8 = false>
+template <bool kDense, bool kFp8 = false, bool kTcPv = false>
 size_t smem_bytes() {
-    return sizeof(SharedStorage<kDense, kFp8>) + 1024;
+    return sizeof(SharedStorage<kDense, kFp8, kTcPv>) + 1024;
 }
 static_assert(sizeof(SharedStorage<true>) + 1024 <= 227 * 1024, "dense shared memory");
+static_assert(sizeof(SharedStorage<true, false, true>) + 1024 <= 227 * 1024, "dense shared memory (tcgen05 P . V)");
+using TcPvStorage = SharedStorage<true, false, true>;
+static_assert(offsetof(TcPvStorage, tc) % 1024 == 0, "P^T buffers 1024-byte aligned");
 static_assert(sizeof(SharedStorage<false>) + 1024 <= 227 * 1024, "sparse shared memory");
 static_assert(sizeof(SharedStorage<true, true>) + 1024 <= 227 * 1024, "E4M3 dense shared memory");
 
 }  // namespace
 
-size_t partial_mma_smem_bytes(bool fp8) {
+size_t partial_mma_smem_bytes(bool fp8, bool tc_pv) {
     if (fp8) return smem_bytes<true, true>();
+    if (tc_pv) return smem_bytes<true, false, true>();
     return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>();
 }
 int partial_mma_block_threads() { return kThreads; }
 
-template <bool kDense, bool kFp8 = false>
+template <bool kDense, bool kFp8 = false, bool kTcPv = false>
 cudaError_t prepare_one() {
     // the register split assumes kLaunchRegs per thread at launch: with fewer,
     // the MMA warpgroups' increase could never be granted
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, mla_partial_mma_kernel<kDense, kFp8>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, mla_partial_mma_kernel<kDense, kFp8, kTcPv>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(mla_partial_mma_kernel<kDense, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_bytes<kDense, kFp8>()));
+    return cudaFuncSetAttribute(mla_partial_mma_kernel<kDense, kFp8, kTcPv>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes<kDense, kFp8, kTcPv>()));
 }
 
 cudaError_t partial_mma_prepare(int /*device*/) {
     cudaError_t e = prepare_one<true>();
     if (e == cudaSuccess) e = prepare_one<false>();
     if (e == cudaSuccess) e = prepare_one<true, true>();
+    if (e == cudaSuccess) e = prepare_one<true, false, true>();
     return e;
 }
 
@@ -1244,7 +1669,10 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = p.sparse ? smem_bytes<false>() : p.kv_fp8 ? smem_bytes<true, true>() : smem_bytes<true>();
+    cfg.dynamicSmemBytes = p.sparse   ? smem_bytes<false>()
+                           : p.kv_fp8 ? smem_bytes<true, true>()
+                           : p.tc_pv  ? smem_bytes<true, false, true>()
+                                      : smem_bytes<true>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1253,6 +1681,7 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cfg.numAttrs = pdl ? 1 : 0;
     if (p.sparse) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<false>, maps, p);
     if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, true>, maps, p);
+    if (p.tc_pv) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, false, true>, maps, p);
     return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true>, maps, p);
 }
 

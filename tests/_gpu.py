@@ -17,8 +17,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-VARIANTS = [1, 2]      # warp-MMA kernel, tcgen05 kernel
-GRANULE = {1: 32, 2: 16}
+VARIANTS = [1, 2]      # warp-MMA kernel, tcgen05 kernel (dense and sparse)
+# dense bf16 decode also runs on the warp-MMA kernel with P . V on tcgen05
+DENSE_VARIANTS = [1, 2, 5]
+GRANULE = {1: 32, 2: 16, 5: 32}
 
 
 def run_dense(x, *, splits=0, pdl=False, num_sms=0, heads=None, scratch=None, plan=None, max_ctx=None, variant=0,

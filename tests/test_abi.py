@@ -303,7 +303,8 @@ def test_plan_override():
     (dict(max_ctx=16, splits=-1), mla.EINVAL),
     (dict(max_ctx=16, num_sms=-5), mla.EINVAL),
     (dict(max_ctx=16, variant=7), mla.EINVAL),
-    (dict(max_ctx=16, variant=5), mla.EINVAL),
+    (dict(max_ctx=16, variant=6), mla.EINVAL),
+    (dict(sparse=True, topk=64, variant=5), mla.EUNSUPPORTED),        # P . V on tcgen05: dense only
     (dict(max_ctx=16, heads=32, variant=4), mla.EUNSUPPORTED),         # 64 heads per CTA: H = 32 is too few
     (dict(heads=64, sparse=True, topk=64, variant=4), mla.EUNSUPPORTED),  # dense only
     (dict(max_ctx=16, variant=3), mla.EUNSUPPORTED),                 # 32 heads per CTA: H = 16 is too few
@@ -497,3 +498,21 @@ def test_fp8_cache_plan_and_argument_checks():
     rows = ctypes.c_void_p(0x70000)
     assert L.mla_decode_forward_step(ctypes.byref(p), ctypes.byref(_args(kv_scale=1.0)), ctypes.c_void_p(0x100000),
                                      p.scratch_bytes, rows, 1, None) == mla.EUNSUPPORTED
+
+
+def test_plan_warp_mma_with_tcgen05_pv():
+    """Variant 5 (scores on the warps, P . V on tcgen05) plans like the warp-MMA
+    kernel: 16 heads per CTA, 32-row granule and modelled step, the same split
+    rule; dense bf16 caches only."""
+    for T in (256, 8192, 131072):
+        a = _plan(max_ctx=T, variant=1)
+        b = _plan(max_ctx=T, variant=5)
+        assert b.variant == 5 and b.head_group == 16 and b.block == a.block
+        assert (b.splits, b.entries_per_split, b.grid_x, b.combine_grid_x) == \
+            (a.splits, a.entries_per_split, a.grid_x, a.combine_grid_x)
+        assert b.scratch_bytes == a.scratch_bytes
+    assert _plan(max_ctx=8192, heads=64, variant=5).n_head_groups == 4
+    with pytest.raises(mla.MLADecodeError) as e:
+        _plan(max_ctx=64, variant=5, kv_fp8=True)
+    assert e.value.status == mla.EUNSUPPORTED
+

@@ -26,7 +26,7 @@ def _setup():
 
 
 @pytest.mark.parametrize("variant,heads,sparse", [(1, 16, False), (1, 16, True), (2, 16, False), (2, 16, True),
-                                                  (3, 32, False), (4, 64, False)])
+                                                  (3, 32, False), (4, 64, False), (5, 16, False)])
 def test_wait_timeout_sets_status_and_context_survives(variant, heads, sparse):
     d = _gpu.dev()
     if sparse:

@@ -26,7 +26,7 @@ def _setup():
 
 
 # ---- dense, small shapes: several stages, ragged tails, many split counts ----
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 @pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 79, 80, 81, 100, 160, 256, 1000, 2049])
 @pytest.mark.parametrize("splits", [0, 1, 3, 8])
 def test_dense_small(T, splits, variant):
@@ -44,7 +44,7 @@ def test_dense_t256_workload():
     _gpu.assert_parity(out, lse, ro, rl, "dense_t256")
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_dense_t8192_split_sweep(variant):
     x = workloads.make("dense_t8192")
     ro, rl = _gpu.oracle_dense(x)
@@ -74,7 +74,7 @@ def test_dense_context_sweep_workloads(T):
     assert mla.status_word(plan, scratch) == 0
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_dense_partials_match_oracle_split_emulation(variant):
     """The partial kernel's scratch (o_s, lse_s) against the oracle's fp64 emulation
     of the same slices (cut at the kernel's granule, as the plan cuts them)."""
@@ -92,7 +92,7 @@ def test_dense_partials_match_oracle_split_emulation(variant):
     assert (np.abs(l_gpu[fin] - lp[fin]) / np.maximum(np.abs(lp[fin]), 1)).max() <= _gpu.LSE_RTOL
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_dense_batch_ragged(variant):
     B, H, cap = 3, 16, 1500
     x = workloads.dense(B, H, cap, seed=21)
@@ -102,7 +102,7 @@ def test_dense_batch_ragged(variant):
     _gpu.assert_parity(out, lse, ro, rl, "dense batch 3 ragged")
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 @pytest.mark.parametrize("H", [32, 64, 128])
 def test_dense_more_heads(H, variant):
     x = workloads.dense(1, H, 2000, seed=H)
@@ -112,7 +112,7 @@ def test_dense_more_heads(H, variant):
     _gpu.assert_parity(out, lse, ro, rl, f"dense H={H}")
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_dense_row_stride_and_capacity(variant):
     """Rows padded to a 640-element stride; d_pos beyond the cache is clamped."""
     T = 700
@@ -135,7 +135,7 @@ def test_dense_row_stride_and_capacity(variant):
     _gpu.assert_parity(out, lse, ro, rl, "d_pos clamped to the cache")
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_uniform_scores_closed_form(variant):
     """q = 0: every score is 0, so out = mean of the attended latent rows and lse = ln n."""
     T = 777
@@ -219,7 +219,7 @@ def test_sparse_b64_workload_all_requests():
 
 
 # ---- determinism, A/A, PDL, guards -------------------------------------------
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_fixed_split_is_bit_identical_across_runs(variant):
     x = workloads.dense(1, 16, 8192, seed=41)
     ref = None
@@ -241,7 +241,7 @@ def test_aa_control_sparse(variant):
     assert torch.equal(_gpu.bits(a[0]), _gpu.bits(b[0])) and torch.equal(_gpu.bits(a[1]), _gpu.bits(b[1]))
 
 
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_pdl_on_off_bit_identical(variant):
     x = workloads.dense(1, 16, 4096, seed=43)
     a = _gpu.run_dense(x, splits=16, pdl=False, variant=variant)

@@ -14,8 +14,9 @@ import workloads
 
 pytestmark = pytest.mark.gpu
 
-# (variant, heads): warp-MMA, tcgen05 with 16, 32 and 64 heads per CTA
-KERNELS = [(1, 16), (2, 16), (3, 32), (4, 64), (4, 128)]
+# (variant, heads): warp-MMA, tcgen05 with 16, 32 and 64 heads per CTA, warp-MMA
+# with P . V on tcgen05
+KERNELS = [(1, 16), (2, 16), (3, 32), (4, 64), (4, 128), (5, 16), (5, 64)]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -84,7 +84,7 @@ def _nan_like(out, lse):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("variant", _gpu.VARIANTS)
+@pytest.mark.parametrize("variant", _gpu.DENSE_VARIANTS)
 def test_static_dense_matches_forward_twice(gpu, variant):
     x = workloads.dense(3, 16, 1000, seed=21)
     x.d_pos = torch.tensor([999, 76, 512], dtype=torch.int32)

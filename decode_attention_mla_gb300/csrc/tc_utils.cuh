@@ -58,6 +58,15 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, int a_mn, i
            | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
+// The same with f16 A/B (format code 0).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int m, int n, int a_mn, int b_mn) {
+    return (1u << 4)                                   // D format: f32
+           | (static_cast<uint32_t>(a_mn) << 15)       // A major-ness
+           | (static_cast<uint32_t>(b_mn) << 16)       // B major-ness
+           | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), fixed version bits 0b001 at 46..48, swizzle mode
 // at 61..63 (2 = 128-byte swizzle).

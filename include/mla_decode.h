@@ -92,9 +92,12 @@ typedef struct {
                                  heads a multiple of 32);
                              4 = tcgen05/TMEM kernel, 64-row tiles, 64 heads per CTA (dense,
                                  heads a multiple of 64);
-                             0 = auto (measured crossovers): sparse or H = 16 -> 1; dense
-                                 H >= 32 -> 1 while its slices hold <= 768 rows, else 4
-                                 (H a multiple of 64) or 3 */
+                             5 = the warp-MMA kernel with P . V on tcgen05: scores and softmax
+                                 on the warps (mma.sync), P . V issued by one thread per warp
+                                 group into tensor memory (dense only);
+                             0 = auto (measured crossovers): E4M3 cache -> 5; sparse or H = 16
+                                 -> 1; dense H >= 32 -> 1 while its slices hold <= 768 rows,
+                                 else 4 (H a multiple of 64) or 3 */
     int pdl;              /* 1 = launch with programmatic dependent launch */
     int stall_test;       /* test hook, 0 in normal use.  1 = one thread of the partial kernel
                              waits (about 1 ms) on a barrier nothing arrives at, so the timeout
@@ -103,7 +106,7 @@ typedef struct {
                              the outputs of that call are undefined, the context stays usable */
     int kv_fp8;           /* 0 = bf16 cache rows (576 x 2 bytes); 1 = OCP FP8 E4M3 cache rows (576
                              bytes), value = e4m3(byte) * args.kv_scale: dense decode on the
-                             warp-MMA kernel (variant 0 or 1; otherwise MLA_EUNSUPPORTED) */
+                             warp-MMA kernel (variant 0, 1 or 5; otherwise MLA_EUNSUPPORTED) */
 } mla_decode_shape;
 
 /* Launch plan (plain data; copy freely).  The plan is the capture key of a

@@ -473,12 +473,13 @@ def test_forward_step_argument_checks():
 
 
 def test_fp8_cache_plan_and_argument_checks():
-    """E4M3 caches: dense on the warp-MMA kernel only; the scale and the byte
-    row stride are checked before any launch."""
+    """E4M3 caches: dense on the warp-MMA kernel only (P . V on the warps or on
+    tcgen05); the scale and the byte row stride are checked before any launch."""
     p = _plan(max_ctx=4096, kv_fp8=True)
-    assert p.variant == 1 and p.shape.kv_fp8 == 1
+    assert p.variant == 5 and p.shape.kv_fp8 == 1            # automatic: P . V on tcgen05
     assert 0 < p.smem_bytes <= 227 * 1024
-    assert _plan(heads=128, max_ctx=131072, kv_fp8=True).variant == 1   # the warp-MMA kernel at any width
+    assert _plan(heads=128, max_ctx=131072, kv_fp8=True).variant == 5   # the warp-MMA kernel at any width
+    assert _plan(max_ctx=4096, kv_fp8=True, variant=1).variant == 1
     L = mla.lib()
     s = mla.Shape(batch=1, heads=16, d_latent=512, d_rope=64, sparse=0, max_ctx=64, topk=0, scale=SCALE,
                   num_sms=152, splits_override=0, variant=0, pdl=0, stall_test=0, kv_fp8=2)
@@ -503,7 +504,7 @@ def test_fp8_cache_plan_and_argument_checks():
 def test_plan_warp_mma_with_tcgen05_pv():
     """Variant 5 (scores on the warps, P . V on tcgen05) plans like the warp-MMA
     kernel: 16 heads per CTA, 32-row granule and modelled step, the same split
-    rule; dense bf16 caches only."""
+    rule; dense caches (bf16 or E4M3) only."""
     for T in (256, 8192, 131072):
         a = _plan(max_ctx=T, variant=1)
         b = _plan(max_ctx=T, variant=5)
@@ -512,7 +513,9 @@ def test_plan_warp_mma_with_tcgen05_pv():
             (a.splits, a.entries_per_split, a.grid_x, a.combine_grid_x)
         assert b.scratch_bytes == a.scratch_bytes
     assert _plan(max_ctx=8192, heads=64, variant=5).n_head_groups == 4
+    f = _plan(max_ctx=8192, variant=5, kv_fp8=True)
+    assert f.variant == 5 and f.shape.kv_fp8 == 1 and 0 < f.smem_bytes <= 227 * 1024
     with pytest.raises(mla.MLADecodeError) as e:
-        _plan(max_ctx=64, variant=5, kv_fp8=True)
+        _plan(sparse=True, topk=64, variant=5, kv_fp8=True)
     assert e.value.status == mla.EUNSUPPORTED
 

@@ -1,7 +1,9 @@
 """GPU parity of the E4M3 (FP8) cache path (dense decode, warp-MMA kernel:
 E4M3 rows staged by TMA and widened to f16 in shared memory, f16 products,
 the cache's scale folded into the scores and the output) against the fp64
-oracle over the same bytes and scale; the same bar as the bf16 cache."""
+oracle over the same bytes and scale; the same bar as the bf16 cache.  Every
+test runs on both forms of the kernel: P . V on the warps (variant 1) and on
+tcgen05 (variant 5)."""
 import numpy as np
 import pytest
 import torch
@@ -24,12 +26,22 @@ def _setup():
     yield
 
 
+_VARIANT = [1]          # the kernel form under test (set per test by the fixture below)
+
+
+@pytest.fixture(params=[1, 5], autouse=True)
+def _variant(request):
+    _VARIANT[0] = request.param
+    yield request.param
+
+
 def _run(x, kv8, kv_scale, *, splits=0, max_ctx=None, plan=None, scratch=None, num_sms=0, kv_dev=None):
     d = _gpu.dev()
     B, H, _ = x.q.shape
     if plan is None:
         mc = max_ctx or int(x.d_pos.max()) + 1
-        plan = mla.plan(batch=B, heads=H, max_ctx=mc, scale=x.scale, splits=splits, kv_fp8=True, num_sms=num_sms)
+        plan = mla.plan(batch=B, heads=H, max_ctx=mc, scale=x.scale, splits=splits, kv_fp8=True, num_sms=num_sms,
+                        variant=_VARIANT[0])
     if scratch is None:
         scratch = mla.alloc_scratch(plan)
     out = torch.full((B, H, 512), float("nan"), device=d)
@@ -52,7 +64,7 @@ def test_fp8_dense_matches_oracle(T, splits):
     x = workloads.dense(1, 16, T, seed=700 + T)
     kv8, kv_scale = workloads.to_e4m3(x.kv)
     out, lse, plan, scratch = _run(x, kv8, kv_scale, splits=splits)
-    assert plan.variant == 1
+    assert plan.variant == _VARIANT[0]
     ro, rl = _oracle(x, kv8, kv_scale)
     _gpu.assert_parity(out, lse, ro, rl, f"E4M3 T={T} S={plan.splits}")
     assert mla.status_word(plan, scratch) == 0
@@ -73,7 +85,7 @@ def test_fp8_context_sweep_workloads(T):
     x = workloads.dense(1, 16, T, seed=T + 13)
     kv8, kv_scale = workloads.to_e4m3(x.kv)
     d = _gpu.dev()
-    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, kv_fp8=True, pdl=True)
+    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, kv_fp8=True, pdl=True, variant=_VARIANT[0])
     scratch = mla.alloc_scratch(plan)
     out = torch.full((1, 16, 512), float("nan"), device=d)
     lse = torch.full((1, 16), float("nan"), device=d)
@@ -162,7 +174,7 @@ def test_fp8_padded_row_stride():
     padded = torch.zeros((T, 640), dtype=torch.uint8)
     padded[:, :576] = kv8
     d = _gpu.dev()
-    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, kv_fp8=True)
+    plan = mla.plan(batch=1, heads=16, max_ctx=T, scale=x.scale, kv_fp8=True, variant=_VARIANT[0])
     scratch = mla.alloc_scratch(plan)
     out = torch.empty(1, 16, 512, device=d)
     lse = torch.empty(1, 16, device=d)

@@ -857,6 +857,44 @@ def ncu_case(args):
         fields = dict((f[0], int(f[1:])) for f in args.ncu_case[len("dense_"):].split("_"))
         T, H = fields["t"], fields.get("h", 16)
         b = DenseBench(T, H, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
+    elif args.ncu_case.startswith("project_h"):
+        # project_h<H>: the wv_b projection (v_dim 128) over distinct weight copies
+        import decode_attention_mla_gb300 as mla
+        H = int(args.ncu_case[len("project_h"):])
+        d = torch.device("cuda")
+        g = torch.Generator().manual_seed(5)
+        w0 = (torch.randn(H, 128, 512, generator=g) / 512 ** 0.5).to(torch.bfloat16).to(d)
+        ws = [w0] + [torch.roll(w0, shifts=c, dims=2) for c in range(1, copies_for(H * 128 * 512 * 2))]
+        lat = torch.randn(1, H, 512, generator=g).to(d)
+        y = torch.empty(1, H, 128, device=d)
+        for c in range(args.calls):
+            mla.project(lat, ws[c % len(ws)], y, pdl=True)
+        torch.cuda.synchronize()
+        log(f"ncu case {args.ncu_case}: {args.calls} calls over {len(ws)} weight copies")
+        return
+    elif args.ncu_case.startswith("step_"):
+        # step_h<H>_t<T>: the fused decode step (append + partial + combine, no
+        # advance, so every call attends the same rows) over distinct caches
+        fields = dict((f[0], int(f[1:])) for f in args.ncu_case[len("step_"):].split("_"))
+        T, H = fields["t"], fields.get("h", 16)
+        b = DenseBench(T, H, copies_for(T * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
+        rows = workloads.randn_bf16(1, 576, seed=9, stream=4).to(torch.device("cuda"))
+        for c in range(args.calls):
+            b.mla.forward_step_args(b.plan, b.args[c % b.copies], b.scratch, rows, advance=False)
+        torch.cuda.synchronize()
+        log(f"ncu case {args.ncu_case}: {args.calls} fused steps, splits {b.plan.splits}, variant {b.plan.variant}")
+        return
+    elif args.ncu_case.startswith("loop_"):
+        # loop_h<H>_t<T>: one eager pass of the multi-step loop (two steps of
+        # append, partial + combine per layer, advance) over distinct caches
+        fields = dict((f[0], int(f[1:])) for f in args.ncu_case[len("loop_"):].split("_"))
+        T, H = fields["t"], fields.get("h", 128)
+        gb = GraphBench(H, T, 2, copies_for((T + 2) * ROW_BYTES), args.splits, bool(args.pdl), variant=args.variant)
+        for _ in range(max(1, args.calls // (2 * gb.copies))):
+            gb.loop()
+        torch.cuda.synchronize()
+        log(f"ncu case {args.ncu_case}: {gb.copies} layers x 2 steps, splits {gb.plan.splits}")
+        return
     elif args.ncu_case == "sparse_k2048":
         b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl),
                         variant=args.variant)
@@ -884,8 +922,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep and the PDL A/B")
     ap.add_argument("--details", default=None)
     ap.add_argument("--ncu-case", default=None,
-                    help="profiling helper: dense_t<T> | dense_h<H>_t<T> | sparse_k2048 | sparse_b64: run --calls eager calls of "
-                         "that workload and exit (no JSON)")
+                    help="profiling helper: dense_t<T> | dense_h<H>_t<T> | dense_fp8_t<T> | sparse_k2048 | sparse_b64 | "
+                         "project_h<H> | step_h<H>_t<T>: run --calls eager calls of that workload and exit (no JSON)")
     ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

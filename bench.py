@@ -187,9 +187,6 @@ class DenseBench:
     def partial(self, c, stream=None):
         self.mla.run(self.plan, self.args[c], self.scratch, stream)
 
-    def combine(self, c, stream=None):
-        self.mla.combine(self.plan, self.args[c], self.scratch, stream)
-
     def replan(self, pdl):
         """The same plan (split count, kernel) launched with or without PDL."""
         self.plan = self.mla.plan(batch=1, heads=self.H, max_ctx=self.T, scale=self.host.scale,
@@ -246,8 +243,6 @@ class SparseBench:
     def partial(self, c, stream=None):
         self.mla.run(self.plan, self.args[c], self.scratch, stream)
 
-    def combine(self, c, stream=None):
-        self.mla.combine(self.plan, self.args[c], self.scratch, stream)
 
 
 def sparse_recipe_without_cache(name, seed):
@@ -592,6 +587,7 @@ def run_ours(args, rank, world):
             t0 = time.perf_counter()
             result["sweep"] = sweep_rows(args, P)
             result["pdl_ab"] = pdl_ab(args, P)
+            result["floor"] = floor_rows(args, P)
             result["sweep_seconds"] = round(time.perf_counter() - t0, 1)
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cpu_bench, args.cpu_seconds)
@@ -627,19 +623,14 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- details (all workloads)
-def time_bench(bench, reps=200, warm=5, with_combine=False):
+def time_bench(bench, reps=200, warm=5):
     g = capture(bench.call, bench.copies)
     gp = capture(bench.partial, bench.copies)
     el = time_graph(g, reps, warm)
     elp = time_graph(gp, reps, warm)
     rep_list = per_rep_times(g, 20)
     us = el / (reps * bench.copies) * 1e6
-    res = (us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list])
-    if with_combine:
-        # the combines alone, on the partials the last replay left in scratch
-        gc = capture(bench.combine, bench.copies)
-        res = res + (time_graph(gc, reps, warm) / (reps * bench.copies) * 1e6,)
-    return res
+    return us, elp / (reps * bench.copies) * 1e6, [r / bench.copies * 1e6 for r in rep_list]
 
 
 def time_graph_bench(gb, reps=10, warm=3):
@@ -767,6 +758,58 @@ def pdl_ab(args, P, reps=12):
     del gb, g_on, g_off
     torch.cuda.empty_cache()
     return rows
+
+
+# the combine kernel reserves this much shared memory per CTA when its grid
+# fits the GPU (one CTA per SM), which its empty stand-in copies
+COMBINE_SPREAD_SMEM = 120 * 1024
+
+
+def floor_rows(args, P, reps=12):
+    """What a dense T = 8192 call costs with no decode work in it, timed like
+    the calls (graphs over the same distinct caches, arms alternating):
+    two empty kernels with the partial and combine kernels' launch shapes
+    (PDL on and off), one kernel that only reads a call's cache rows with
+    bulk copies (over every SM and over the partial's grid), and that read
+    followed by the real combine kernel."""
+    import decode_attention_mla_gb300 as mla
+    d = torch.device("cuda")
+    b = DenseBench(8192, 16, copies_for(8192 * ROW_BYTES), args.splits, True, variant=args.variant)
+    pl = b.plan
+    part = (pl.grid_x, pl.block, pl.smem_bytes)
+    cgrid = pl.combine_grid_x * pl.combine_grid_y
+    comb = (cgrid, pl.combine_block, COMBINE_SPREAD_SMEM if cgrid <= pl.num_sms else 0)
+    nbytes = 8192 * ROW_BYTES
+    sms = pl.num_sms
+    sink = torch.zeros(max(sms, pl.grid_x), dtype=torch.int32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    graphs = {
+        "empty_pair": capture(lambda c: mla.floor_empty_pair(part, comb, pdl=True), b.copies),
+        "empty_pair_no_pdl": capture(lambda c: mla.floor_empty_pair(part, comb, pdl=False), b.copies),
+        "read_all_sms": capture(lambda c: mla.floor_read(b.kv[c], nbytes, sms, sink, status), b.copies),
+        "read_partial_grid": capture(lambda c: mla.floor_read(b.kv[c], nbytes, pl.grid_x, sink, status),
+                                     b.copies),
+    }
+
+    def read_then_combine(c):
+        mla.floor_read(b.kv[c], nbytes, pl.grid_x, sink, status)
+        mla.combine(pl, b.args[c], b.scratch)
+
+    graphs["read_then_combine"] = capture(read_then_combine, b.copies)
+    graphs["call"] = capture(b.call, b.copies)
+    r = alternate(graphs, b.copies, reps, 20)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("floor read kernel reported a wait timeout")
+    out = {"workload": "dense_h16_t8192", "read_bytes": nbytes, "partial_launch": list(part),
+           "combine_launch": list(comb)}
+    for k, v in r.items():
+        out[k] = v
+    for k in ("read_all_sms", "read_partial_grid"):
+        out[k]["gbs"] = round(nbytes / (r[k]["us_per_call"] * 1e-6) / 1e9, 1)
+    del b, graphs
+    torch.cuda.empty_cache()
+    return out
 
 
 def write_details(args, P):

@@ -75,7 +75,8 @@ _lib = None
 
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
-            "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project", "mla_decode_forward_step")
+            "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project", "mla_decode_forward_step",
+            "mla_floor_empty_pair", "mla_floor_read")
 
 
 def lib():
@@ -111,6 +112,10 @@ def lib():
         L.mla_decode_scratch_init.argtypes = [P, SZ, P]
         L.mla_decode_strerror.restype = ctypes.c_char_p
         L.mla_decode_strerror.argtypes = [I]
+        L.mla_floor_empty_pair.restype = I
+        L.mla_floor_empty_pair.argtypes = [I, I, I, I, I, I, I, P]
+        L.mla_floor_read.restype = I
+        L.mla_floor_read.argtypes = [P, SZ, I, P, P, I, P]
         _lib = L
         return L
 
@@ -273,6 +278,20 @@ def project(latent, wv_b, y, *, pdl: bool = False, stream=None) -> None:
 def advance(d_pos, stream=None) -> None:
     """``mla_decode_advance``: d_pos += 1 on the device."""
     _check(lib().mla_decode_advance(_ptr(d_pos), int(d_pos.numel()), _stream(stream)), "mla_decode_advance")
+
+
+def floor_empty_pair(a, b, *, pdl: bool = True, stream=None) -> None:
+    """``mla_floor_empty_pair``: two empty kernels with launch shapes a and b,
+    each a (grid, block, dynamic shared bytes) triple."""
+    _check(lib().mla_floor_empty_pair(int(a[0]), int(a[1]), int(a[2]), int(b[0]), int(b[1]), int(b[2]),
+                                      int(bool(pdl)), _stream(stream)), "mla_floor_empty_pair")
+
+
+def floor_read(src, nbytes: int, ctas: int, sink, status, *, pdl: bool = True, stream=None) -> None:
+    """``mla_floor_read``: one kernel of ``ctas`` CTAs reading ``nbytes`` of ``src`` with bulk copies;
+    ``sink``: uint32/int32 [ctas], ``status``: int32 [1] (zeroed by the caller)."""
+    _check(lib().mla_floor_read(_ptr(src), int(nbytes), int(ctas), _ptr(sink), _ptr(status), int(bool(pdl)),
+                                _stream(stream)), "mla_floor_read")
 
 
 def abi_version() -> int:

@@ -519,3 +519,28 @@ def test_plan_warp_mma_with_tcgen05_pv():
         _plan(sparse=True, topk=64, variant=5, kv_fp8=True)
     assert e.value.status == mla.EUNSUPPORTED
 
+
+
+def test_floor_probes_reject_bad_arguments():
+    """The floor probes check every argument before anything is launched."""
+    L = mla.lib()
+    pair = L.mla_floor_empty_pair
+    ok = (128, 384, 200000)
+    assert pair(*ok, *ok, 2, None) == mla.EINVAL
+    for bad in ((0, 384, 0), (65536, 384, 0), (128, 16, 0), (128, 33, 0), (128, 2048, 0), (128, 384, -1),
+                (128, 384, 227 * 1024 + 1)):
+        assert pair(*bad, *ok, 1, None) == mla.EINVAL, bad
+        assert pair(*ok, *bad, 1, None) == mla.EINVAL, bad
+    read = L.mla_floor_read
+    p16 = ctypes.c_void_p(0x10000)
+    assert read(None, 4096, 8, p16, p16, 1, None) == mla.EINVAL
+    assert read(p16, 0, 8, p16, p16, 1, None) == mla.EINVAL
+    assert read(p16, 4096, 0, p16, p16, 1, None) == mla.EINVAL
+    assert read(p16, 4096, 65536, p16, p16, 1, None) == mla.EINVAL
+    assert read(p16, 4096, 8, None, p16, 1, None) == mla.EINVAL
+    assert read(p16, 4096, 8, p16, None, 1, None) == mla.EINVAL
+    assert read(p16, 4096, 8, p16, p16, 3, None) == mla.EINVAL
+    assert read(p16, 4100, 8, p16, p16, 1, None) == mla.EALIGN
+    assert read(ctypes.c_void_p(0x10008), 4096, 8, p16, p16, 1, None) == mla.EALIGN
+    assert read(p16, 4096, 8, ctypes.c_void_p(0x10002), p16, 1, None) == mla.EALIGN
+    assert read(p16, 4096, 8, p16, ctypes.c_void_p(0x10001), 1, None) == mla.EALIGN

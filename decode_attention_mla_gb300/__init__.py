@@ -76,7 +76,7 @@ _lib = None
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
             "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project", "mla_decode_forward_step",
-            "mla_floor_empty_pair", "mla_floor_read")
+            "mla_floor_empty_pair", "mla_floor_read", "mla_decode_static_status", "mla_decode_static_reset")
 
 
 def lib():
@@ -112,6 +112,10 @@ def lib():
         L.mla_decode_scratch_init.argtypes = [P, SZ, P]
         L.mla_decode_strerror.restype = ctypes.c_char_p
         L.mla_decode_strerror.argtypes = [I]
+        L.mla_decode_static_status.restype = I
+        L.mla_decode_static_status.argtypes = [P, P]
+        L.mla_decode_static_reset.restype = I
+        L.mla_decode_static_reset.argtypes = [P]
         L.mla_floor_empty_pair.restype = I
         L.mla_floor_empty_pair.argtypes = [I, I, I, I, I, I, I, P]
         L.mla_floor_read.restype = I
@@ -252,6 +256,17 @@ def forward_static(p: Plan, q, kv, out, lse, *, d_pos=None, row_offset=None, cac
                   kv_rows=kv_rows, row_stride=row_stride)
     _check(lib().mla_decode_forward_static(ctypes.byref(p), ctypes.byref(a), _stream(stream)),
            "mla_decode_forward_static")
+
+
+def static_status(dst, stream=None) -> None:
+    """``mla_decode_static_status``: stream-ordered copy of the static scratch's status word into
+    ``dst`` (a CUDA int32 tensor of at least one element)."""
+    _check(lib().mla_decode_static_status(_ptr(dst), _stream(stream)), "mla_decode_static_status")
+
+
+def static_reset(stream=None) -> None:
+    """``mla_decode_static_reset``: clear the static scratch's status word."""
+    _check(lib().mla_decode_static_reset(_stream(stream)), "mla_decode_static_reset")
 
 
 def append(kv, new_rows, d_pos, *, row_offset=None, kv_rows=None, row_stride=None, stream=None) -> None:

@@ -476,6 +476,25 @@ long long uniform_cost(long long rows, long long pairs, long long grid_cap, int 
     return waves * (ceil_div(per, variant_tile_rows(variant)) + 1);
 }
 
+// The static array of the current device (looked up on first use, outside capture).
+int static_scratch_for(void* stream, void** out) {
+    int dev = 0;
+    const int rc = current_device(&dev);
+    if (rc != MLA_OK) return rc;
+    void* scratch = mla::static_scratch_if_ready(dev);
+    if (!scratch) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return MLA_ECUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return MLA_ENOTREADY;
+        if (mla::static_scratch_set_up(dev, &scratch) != cudaSuccess) return MLA_ECUDA;
+    }
+    *out = scratch;
+    return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -620,23 +639,29 @@ int mla_decode_forward_static(const mla_decode_plan_t* plan, const mla_decode_ar
     if (rc == MLA_OK) rc = check_args(plan, args);
     if (rc != MLA_OK) return rc;
     if (plan->scratch_bytes > mla::kStaticScratchBytes) return MLA_ESTATICLIMIT;
-    int dev = 0;
-    rc = current_device(&dev);
+    void* scratch = nullptr;
+    rc = static_scratch_for(stream, &scratch);
     if (rc != MLA_OK) return rc;
-    void* scratch = mla::static_scratch_if_ready(dev);
-    if (!scratch) {
-        // first call on this device: look the array up (not while capturing)
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
-            cudaGetLastError();
-            return MLA_ECUDA;
-        }
-        if (cs != cudaStreamCaptureStatusNone) return MLA_ENOTREADY;
-        if (mla::static_scratch_set_up(dev, &scratch) != cudaSuccess) return MLA_ECUDA;
-    }
     rc = do_run(plan, args, scratch, mla::kStaticScratchBytes, stream);
     if (rc != MLA_OK) return rc;
     return do_combine(plan, args, scratch, mla::kStaticScratchBytes, stream);
+}
+
+int mla_decode_static_status(int* status, void* stream) {
+    if (!status) return MLA_EINVAL;
+    if (misaligned(status, 4)) return MLA_EALIGN;
+    void* scratch = nullptr;
+    const int rc = static_scratch_for(stream, &scratch);
+    if (rc != MLA_OK) return rc;
+    return launch_status(cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDefault,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_static_reset(void* stream) {
+    void* scratch = nullptr;
+    const int rc = static_scratch_for(stream, &scratch);
+    if (rc != MLA_OK) return rc;
+    return launch_status(cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)));
 }
 
 int mla_decode_scratch_init(void* scratch, size_t scratch_bytes, void* stream) {

@@ -252,7 +252,8 @@ MLA_API int mla_decode_forward_step(const mla_decode_plan_t *plan, const mla_dec
  *     fits up to S = 255, H = 128 up to S = 31.
  *   - Zero start: only the status word (offset 0) must start at zero; the
  *     array is zero when the library's module is loaded.  A device-side
- *     wait timeout sets it and nothing here clears it or reports it.  The
+ *     wait timeout sets it (MLA_EDEVICE) and it stays set until
+ *     mla_decode_static_reset; mla_decode_static_status reads it.  The
  *     partial and LSE arrays need no initial value.
  *   - Races: every call on a device shares the one array, so calls that can
  *     overlap (on different streams, or from several host threads without
@@ -260,6 +261,22 @@ MLA_API int mla_decode_forward_step(const mla_decode_plan_t *plan, const mla_dec
  *     ordered and safe.
  * Errors: as mla_decode_forward, minus MLA_ESCRATCH, plus MLA_ESTATICLIMIT. */
 MLA_API int mla_decode_forward_static(const mla_decode_plan_t *plan, const mla_decode_args *args, void *stream);
+
+/* The static array's status word (0 healthy, else an mla_status such as
+ * MLA_EDEVICE after a wait timeout), for the current device: a stream-ordered
+ * copy of the 4-byte word into *status, which may be device memory or
+ * host memory the device can write (pinned or managed), 4-byte aligned; read
+ * it after `stream` has reached this point.  Like mla_decode_forward_static,
+ * the first use on a device looks the array up and must be outside stream
+ * capture (MLA_ENOTREADY otherwise); nothing is allocated.
+ * Errors: MLA_EINVAL (null status), MLA_EALIGN, MLA_ENOTREADY, MLA_ECUDA. */
+MLA_API int mla_decode_static_status(int *status, void *stream);
+
+/* Clear the static array's status word on the current device (a
+ * stream-ordered 4-byte memset), so that a later timeout can be told apart
+ * from an earlier one.  Same first-use rule as mla_decode_static_status.
+ * Errors: MLA_ENOTREADY, MLA_ECUDA. */
+MLA_API int mla_decode_static_reset(void *stream);
 
 /* Write the new token's cache row from device memory: for each request b,
  * copy new_rows[b] (bf16 [576]) to row base_b + d_pos[b] of kv, where base_b

@@ -133,3 +133,49 @@ def test_static_near_limit_plan(gpu):
     torch.cuda.synchronize()
     assert torch.equal(_gpu.bits(out), _gpu.bits(out_ref))
     assert torch.equal(_gpu.bits(lse), _gpu.bits(lse_ref))
+
+
+def test_static_status_rejects_bad_arguments():
+    """Checked on the host before any CUDA call."""
+    L = mla.lib()
+    assert L.mla_decode_static_status(None, None) == mla.EINVAL
+    assert L.mla_decode_static_status(ctypes.c_void_p(0x10002), None) == mla.EALIGN
+
+
+@pytest.mark.gpu
+def test_static_status_reports_a_timeout_until_reset(gpu):
+    """A wait timeout inside mla_decode_forward_static is visible through
+    mla_decode_static_status until mla_decode_static_reset clears it; the next
+    healthy call still matches mla_decode_forward."""
+    x = workloads.dense(1, 16, 4000, seed=62)
+    q, kv, dp = x.q.to(gpu), x.kv.to(gpu), x.d_pos.to(gpu)
+    out = torch.zeros(1, 16, 512, device=gpu)
+    lse = torch.zeros(1, 16, device=gpu)
+    st = torch.full((1,), -99, dtype=torch.int32, device=gpu)
+    pinned = torch.full((1,), -99, dtype=torch.int32).pin_memory()
+
+    mla.static_reset()
+    mla.static_status(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+    stalled = mla.plan(batch=1, heads=16, max_ctx=4000, scale=x.scale, variant=1, stall_test=True)
+    mla.forward_static(stalled, q, kv, out, lse, d_pos=dp)
+    mla.static_status(st)
+    mla.lib().mla_decode_static_status(ctypes.c_void_p(pinned.data_ptr()),
+                                       mla._stream(torch.cuda.current_stream()))
+    torch.cuda.synchronize()
+    assert int(st.item()) == mla.EDEVICE
+    assert int(pinned.item()) == mla.EDEVICE
+
+    mla.static_reset()
+    healthy = mla.plan(batch=1, heads=16, max_ctx=4000, scale=x.scale, variant=1)
+    out_ref, lse_ref, _, _ = _gpu.run_dense(x, plan=healthy)
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    mla.forward_static(healthy, q, kv, out, lse, d_pos=dp)
+    mla.static_status(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(_gpu.bits(out), _gpu.bits(out_ref))
+    assert torch.equal(_gpu.bits(lse), _gpu.bits(lse_ref))

@@ -938,6 +938,25 @@ def ncu_case(args):
         torch.cuda.synchronize()
         log(f"ncu case {args.ncu_case}: {gb.copies} layers x 2 steps, splits {gb.plan.splits}")
         return
+    elif args.ncu_case.startswith("floor_t"):
+        # floor_t<T>: the floor probes on a T-row dense call's caches (the read
+        # kernel over every SM, then the empty pair with the plan's launch shapes)
+        import decode_attention_mla_gb300 as mla
+        T = int(args.ncu_case[len("floor_t"):])
+        b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, True, variant=args.variant)
+        pl = b.plan
+        cgrid = pl.combine_grid_x * pl.combine_grid_y
+        comb = (cgrid, pl.combine_block, COMBINE_SPREAD_SMEM if cgrid <= pl.num_sms else 0)
+        sink = torch.zeros(pl.num_sms, dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for c in range(args.calls):
+            mla.floor_read(b.kv[c % b.copies], T * ROW_BYTES, pl.num_sms, sink, status)
+            mla.floor_empty_pair((pl.grid_x, pl.block, pl.smem_bytes), comb)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("floor read kernel reported a wait timeout")
+        log(f"ncu case {args.ncu_case}: {args.calls} reads of {T * ROW_BYTES} B over {pl.num_sms} CTAs + empty pairs")
+        return
     elif args.ncu_case == "sparse_k2048":
         b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl),
                         variant=args.variant)
@@ -962,11 +981,12 @@ def main():
                          "2 / 3 / 4 = tcgen05 kernel with 16 / 32 / 64 heads per CTA")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep and the PDL A/B")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep, the PDL A/B and the floor")
     ap.add_argument("--details", default=None)
     ap.add_argument("--ncu-case", default=None,
                     help="profiling helper: dense_t<T> | dense_h<H>_t<T> | dense_fp8_t<T> | sparse_k2048 | sparse_b64 | "
-                         "project_h<H> | step_h<H>_t<T>: run --calls eager calls of that workload and exit (no JSON)")
+                         "project_h<H> | step_h<H>_t<T> | loop_h<H>_t<T> | floor_t<T>: run --calls eager calls of "
+                         "that workload and exit (no JSON)")
     ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

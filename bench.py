@@ -809,7 +809,62 @@ def floor_rows(args, P, reps=12):
         out[k]["gbs"] = round(nbytes / (r[k]["us_per_call"] * 1e-6) / 1e9, 1)
     del b, graphs
     torch.cuda.empty_cache()
+    out["stream_t131072"] = stream_floor(131072, args, reps)
+    out["gather"] = [gather_floor(name, args, reps) for name in ("sparse_k2048", "sparse_b64")]
     return out
+
+
+def stream_floor(T, args, reps):
+    """A long dense call's cache rows read by the bulk-copy kernel over every
+    SM, beside the partial kernel alone and the whole call, same caches."""
+    import decode_attention_mla_gb300 as mla
+    d = torch.device("cuda")
+    b = DenseBench(T, 16, copies_for(T * ROW_BYTES), args.splits, True, variant=args.variant)
+    nbytes = T * ROW_BYTES
+    sink = torch.zeros(b.plan.num_sms, dtype=torch.int32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    graphs = {"read": capture(lambda c: mla.floor_read(b.kv[c], nbytes, b.plan.num_sms, sink, status), b.copies),
+              "partial": capture(b.partial, b.copies), "call": capture(b.call, b.copies)}
+    r = alternate(graphs, b.copies, reps, 5)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("floor read kernel reported a wait timeout")
+    res = {"workload": f"dense_h16_t{T}", "read_bytes": nbytes, **r}
+    res["read"]["gbs"] = round(nbytes / (r["read"]["us_per_call"] * 1e-6) / 1e9, 1)
+    del b, graphs
+    torch.cuda.empty_cache()
+    return res
+
+
+def gather_floor(name, args, reps):
+    """The sparse workload's listed rows gathered by a kernel that computes
+    nothing (one bulk copy per row, over the partial's grid), beside the
+    sparse call itself, on the same caches and index lists."""
+    import decode_attention_mla_gb300 as mla
+    d = torch.device("cuda")
+    if name == "sparse_b64":
+        b = SparseBench(name, copies_for(64 * 2048 * ROW_BYTES), args.splits, True, variant=args.variant,
+                        device_cache=True)
+    else:
+        b = SparseBench(name, copies_for(2048 * ROW_BYTES), args.splits, True, variant=args.variant)
+    idx, ln, off = b.idx.to(torch.int64), b.len.to(torch.int64), b.off
+    valid = (idx >= 0) & (idx < ln[:, None])
+    rows = (off[:, None] + idx)[valid].contiguous()
+    ctas = b.plan.grid_x
+    sink = torch.zeros(ctas, dtype=torch.int32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    graphs = {"gather": capture(lambda c: mla.floor_gather(b.kv[c], rows, ctas, sink, status), b.copies),
+              "call": capture(b.call, b.copies)}
+    r = alternate(graphs, b.copies, reps, 5 if name == "sparse_b64" else 20)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("floor gather kernel reported a wait timeout")
+    nbytes = int(rows.numel()) * ROW_BYTES
+    res = {"workload": name, "rows": int(rows.numel()), "ctas": ctas, "gather_bytes": nbytes, **r}
+    res["gather"]["gbs"] = round(nbytes / (r["gather"]["us_per_call"] * 1e-6) / 1e9, 1)
+    del b, graphs, rows
+    torch.cuda.empty_cache()
+    return res
 
 
 def write_details(args, P):

@@ -76,7 +76,7 @@ _lib = None
 EXPORTED = ("mla_decode_abi_version", "mla_decode_plan", "mla_decode_run", "mla_decode_combine",
             "mla_decode_forward", "mla_decode_append", "mla_decode_advance", "mla_decode_scratch_init",
             "mla_decode_strerror", "mla_decode_forward_static", "mla_decode_project", "mla_decode_forward_step",
-            "mla_floor_empty_pair", "mla_floor_read", "mla_decode_static_status", "mla_decode_static_reset")
+            "mla_floor_empty_pair", "mla_floor_read", "mla_floor_gather", "mla_decode_static_status", "mla_decode_static_reset")
 
 
 def lib():
@@ -120,6 +120,8 @@ def lib():
         L.mla_floor_empty_pair.argtypes = [I, I, I, I, I, I, I, P]
         L.mla_floor_read.restype = I
         L.mla_floor_read.argtypes = [P, SZ, I, P, P, I, P]
+        L.mla_floor_gather.restype = I
+        L.mla_floor_gather.argtypes = [P, LL, LL, I, P, LL, I, P, P, I, P]
         _lib = L
         return L
 
@@ -307,6 +309,17 @@ def floor_read(src, nbytes: int, ctas: int, sink, status, *, pdl: bool = True, s
     ``sink``: uint32/int32 [ctas], ``status``: int32 [1] (zeroed by the caller)."""
     _check(lib().mla_floor_read(_ptr(src), int(nbytes), int(ctas), _ptr(sink), _ptr(status), int(bool(pdl)),
                                 _stream(stream)), "mla_floor_read")
+
+
+def floor_gather(kv, rows, ctas: int, sink, status, *, row_bytes: int | None = None, pdl: bool = True,
+                 stream=None) -> None:
+    """``mla_floor_gather``: one kernel of ``ctas`` CTAs gathering the cache rows listed in ``rows``
+    (int64) with one bulk copy per row; ``kv``: [kv_rows, row_stride] (bf16 or bytes)."""
+    stride = kv.stride(0) * kv.element_size()
+    rb = int(row_bytes) if row_bytes is not None else kv.shape[1] * kv.element_size()
+    _check(lib().mla_floor_gather(_ptr(kv), int(kv.shape[0]), int(stride), rb, _ptr(rows), int(rows.numel()),
+                                  int(ctas), _ptr(sink), _ptr(status), int(bool(pdl)), _stream(stream)),
+           "mla_floor_gather")
 
 
 def abi_version() -> int:

@@ -4,11 +4,13 @@
  *
  * A dense decode call is two kernels chained by programmatic dependent launch
  * (the split partial kernel and the log-sum-exp combine, "Graph-resident
- * decode", Lecture 08, s.6 and s.7) that stream the cache once.  The two
- * probes below measure the parts of that call no kernel body can remove:
- * two kernels with empty bodies launched with the partial and combine
- * kernels' launch shapes, and one kernel that does nothing but read a region
- * of device memory over the whole GPU.  They compute nothing of the method.
+ * decode", Lecture 08, s.6 and s.7) that stream the cache once (or gather
+ * its indexed rows, "The Commit That Changed Direction").  The probes below
+ * measure the parts of that call no kernel body can remove: two kernels with
+ * empty bodies launched with the partial and combine kernels' launch shapes,
+ * one kernel that does nothing but read a region of device memory over the
+ * whole GPU, and one that does nothing but gather listed rows.  They compute
+ * nothing of the method.
  *
  * Conventions as in mla_decode.h: (device) pointers are owned by the caller,
  * nothing is allocated, freed or synchronised, arguments are checked on the
@@ -48,6 +50,23 @@ MLA_API int mla_floor_empty_pair(int grid_a, int block_a, int smem_a, int grid_b
  * as above.  Errors: MLA_EINVAL, MLA_EALIGN, MLA_ENOTREADY, MLA_ECUDA. */
 MLA_API int mla_floor_read(const void *src, size_t bytes, int ctas, unsigned *sink, int *status, int pdl,
                            void *stream);
+
+/* One kernel of `ctas` single-warp CTAs that gathers listed rows of a cache
+ * into shared memory, one bulk copy per row (as the sparse decode's producer
+ * warps fetch indexed rows), and computes nothing: rows[] holds n_rows row
+ * numbers of the cache at `kv` (kv_rows rows, row_stride bytes apart, each
+ * row_bytes long); CTA i takes the i-th of `ctas` equal runs of the list, in
+ * rounds of up to 96 KiB, two rounds in flight.  Entries outside [0, kv_rows)
+ * are skipped.  One 32-bit word of what a CTA read goes to sink[i]; waits are
+ * bounded as for mla_floor_read (MLA_EDEVICE in *status).
+ * kv: (device) 16-byte aligned; row_stride, row_bytes: multiples of 16,
+ * 16 <= row_bytes <= 98304 and row_bytes <= row_stride; rows: (device)
+ * int64 [n_rows], 8-byte aligned; n_rows >= 1; ctas: 1..65535; sink: (device)
+ * uint32 [ctas]; status: (device) int32; pdl: 0 or 1.
+ * Errors: MLA_EINVAL, MLA_EALIGN, MLA_ENOTREADY, MLA_ECUDA. */
+MLA_API int mla_floor_gather(const void *kv, long long kv_rows, long long row_stride, int row_bytes,
+                             const long long *rows, long long n_rows, int ctas, unsigned *sink, int *status, int pdl,
+                             void *stream);
 
 #ifdef __cplusplus
 }

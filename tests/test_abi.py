@@ -544,3 +544,25 @@ def test_floor_probes_reject_bad_arguments():
     assert read(ctypes.c_void_p(0x10008), 4096, 8, p16, p16, 1, None) == mla.EALIGN
     assert read(p16, 4096, 8, ctypes.c_void_p(0x10002), p16, 1, None) == mla.EALIGN
     assert read(p16, 4096, 8, p16, ctypes.c_void_p(0x10001), 1, None) == mla.EALIGN
+
+
+def test_floor_gather_rejects_bad_arguments():
+    g = mla.lib().mla_floor_gather
+    p16, p8 = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+    ok = dict(kv=p16, kv_rows=100, row_stride=1152, row_bytes=1152, rows=p8, n_rows=10, ctas=4, sink=p16,
+              status=p16, pdl=1)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return g(a["kv"], a["kv_rows"], a["row_stride"], a["row_bytes"], a["rows"], a["n_rows"], a["ctas"],
+                 a["sink"], a["status"], a["pdl"], None)
+
+    for bad in (dict(kv=None), dict(rows=None), dict(sink=None), dict(status=None), dict(kv_rows=0),
+                dict(n_rows=0), dict(ctas=0), dict(ctas=65536), dict(row_bytes=0), dict(row_bytes=98320),
+                dict(row_stride=1136), dict(pdl=2)):
+        assert call(**bad) == mla.EINVAL, bad
+    for bad in (dict(row_bytes=1160, row_stride=1168), dict(row_stride=1160), dict(kv=p8),
+                dict(rows=ctypes.c_void_p(0x10004)), dict(sink=ctypes.c_void_p(0x10002)),
+                dict(status=ctypes.c_void_p(0x10001))):
+        assert call(**bad) == mla.EALIGN, bad

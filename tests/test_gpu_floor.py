@@ -54,3 +54,48 @@ def test_read_covers_its_piece(nbytes, ctas):
     want = _expected_sink(host.numpy(), nbytes, ctas)
     got = sink.cpu().numpy().view(np.uint32)
     assert np.array_equal(got, want)
+
+
+def _expected_gather(rows: np.ndarray, n: int, ctas: int, per_round: int) -> np.ndarray:
+    """The word each CTA writes: the first word of every round's first row up to
+    the round before last, plus that of the last even round (left in half 0)."""
+    per = -(-n // ctas)
+    out = np.zeros(ctas, dtype=np.uint64)
+    for i in range(ctas):
+        lo, hi = i * per, min(n, i * per + per)
+        if hi <= lo:
+            continue
+        firsts = [int(rows[s]) for s in range(lo, hi, per_round)]
+        R = len(firsts)
+        acc = sum(firsts[:max(0, R - 2)]) + firsts[(R - 1) // 2 * 2]
+        out[i] = acc
+    return (out % (1 << 32)).astype(np.uint32)
+
+
+@pytest.mark.parametrize("kv_rows,stride,row_bytes,n,ctas", [
+    (5000, 1152, 1152, 4096, 152), (5000, 1152, 1152, 1, 1), (70000, 1152, 1152, 131072, 152),
+    (3000, 1152, 576, 2000, 7), (3000, 1168, 1152, 999, 300), (100, 32, 16, 1000, 3)])
+def test_gather_reads_the_listed_rows(kv_rows, stride, row_bytes, n, ctas):
+    g = torch.Generator().manual_seed(n + ctas)
+    kv = torch.zeros(kv_rows, stride, dtype=torch.uint8)
+    kv[:, :4] = torch.arange(kv_rows, dtype=torch.int32).view(-1, 1).view(torch.uint8).view(kv_rows, 4)
+    rows = torch.randint(0, kv_rows, (n,), dtype=torch.int64, generator=g)
+    sink = torch.full((ctas,), -1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvd, rowsd = kv.cuda(), rows.cuda()
+    mla.floor_gather(kvd, rowsd, ctas, sink, status, row_bytes=row_bytes)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    per_round = min((6 * 32 * 1024 // 2) // row_bytes, 128)
+    want = _expected_gather(rows.numpy(), n, ctas, per_round)
+    assert np.array_equal(sink.cpu().numpy().view(np.uint32), want)
+
+
+def test_gather_skips_rows_outside_the_cache():
+    kv = torch.zeros(64, 1152, dtype=torch.uint8, device="cuda")
+    rows = torch.tensor([3, -1, 64, 1 << 40, 5, 63], dtype=torch.int64, device="cuda")
+    sink = torch.zeros(2, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.floor_gather(kv, rows, 2, sink, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0

@@ -1012,6 +1012,21 @@ def ncu_case(args):
             raise RuntimeError("floor read kernel reported a wait timeout")
         log(f"ncu case {args.ncu_case}: {args.calls} reads of {T * ROW_BYTES} B over {pl.num_sms} CTAs + empty pairs")
         return
+    elif args.ncu_case == "floor_gather_k2048":
+        # the gather floor probe on config 3's index list (8 cache copies)
+        import decode_attention_mla_gb300 as mla
+        b = SparseBench("sparse_k2048", 8, args.splits, True, variant=args.variant)
+        idx, ln = b.idx.to(torch.int64), b.len.to(torch.int64)
+        rows = (b.off[:, None] + idx)[(idx >= 0) & (idx < ln[:, None])].contiguous()
+        sink = torch.zeros(b.plan.grid_x, dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for c in range(args.calls):
+            mla.floor_gather(b.kv[c % b.copies], rows, b.plan.grid_x, sink, status)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("floor gather kernel reported a wait timeout")
+        log(f"ncu case {args.ncu_case}: {args.calls} gathers of {rows.numel()} rows over {b.plan.grid_x} CTAs")
+        return
     elif args.ncu_case == "sparse_k2048":
         b = SparseBench("sparse_k2048", min(32, copies_for(2048 * ROW_BYTES)), args.splits, bool(args.pdl),
                         variant=args.variant)
@@ -1040,7 +1055,7 @@ def main():
     ap.add_argument("--details", default=None)
     ap.add_argument("--ncu-case", default=None,
                     help="profiling helper: dense_t<T> | dense_h<H>_t<T> | dense_fp8_t<T> | sparse_k2048 | sparse_b64 | "
-                         "project_h<H> | step_h<H>_t<T> | loop_h<H>_t<T> | floor_t<T>: run --calls eager calls of "
+                         "project_h<H> | step_h<H>_t<T> | loop_h<H>_t<T> | floor_t<T> | floor_gather_k2048: run --calls eager calls of "
                          "that workload and exit (no JSON)")
     ap.add_argument("--calls", type=int, default=20)
     args = ap.parse_args()

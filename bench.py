@@ -661,7 +661,7 @@ def project_timing(H, V, reps=50):
     return {"us": us, "copies": copies, "bytes": wbytes + H * 512 * 4 + H * V * 4}
 
 
-KERNEL_NAMES = {1: "warp-mma", 2: "tcgen05-16", 3: "tcgen05-32", 4: "tcgen05-64"}
+KERNEL_NAMES = {1: "warp-mma", 2: "tcgen05-16", 3: "tcgen05-32", 4: "tcgen05-64", 5: "warp-mma-tcgen05-pv"}
 
 
 def sweep_row(name, bench, us, us_part, reps, P, per="call", tensor_bound=False):
@@ -716,6 +716,14 @@ def sweep_rows(args, P):
     us, _, reps = time_graph_bench(gb, reps=5)
     rows.append(sweep_row("graph_h128", gb, us, None, reps, P, per="decode step per layer (append, partial, "
                           "combine, advance; 64 steps in one graph)", tensor_bound=True))
+    del gb
+    torch.cuda.empty_cache()
+    # the same steps with the append and the advance folded into the two kernels
+    gb = GraphBench(128, 32768, 64, copies_for((32768 + 64) * ROW_BYTES), args.splits, pdl, variant=args.variant,
+                    fused=True)
+    us, _, reps = time_graph_bench(gb, reps=5)
+    rows.append(sweep_row("graph_h128_fused_step", gb, us, None, reps, P, per="decode step per layer "
+                          "(mla_decode_forward_step: two launches; 64 steps in one graph)", tensor_bound=True))
     del gb
     torch.cuda.empty_cache()
     return rows

@@ -12,8 +12,8 @@
 // o = 0, written by the partial kernel, so the merge needs neither the
 // context length nor the slicing).  The 8 warps take contiguous runs of
 // slices; each lane owns 4 consecutive features and loads its run's partials
-// (16 at a time) before the weights are known, so those loads are in flight
-// together with the lse loads.  The max and the sum of exponentials are taken
+// (all of a run of up to 20 at once, else 16 at a time) before the weights
+// are known, so those loads are in flight together with the lse loads.  The max and the sum of exponentials are taken
 // in one pass of (max, sum) pairs.  Each warp adds its run in ascending slice
 // order and the run sums are added in warp order: a fixed association, so
 // the result is reproducible bit for bit.  An all-empty row set gives
@@ -30,11 +30,12 @@ namespace {
 
 constexpr int kWarps = 8;                                        // most warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kBatch = 16;                                       // partials a lane loads at once
+constexpr int kBatch = 16;                                       // partials a lane loads at once (two batches)
+constexpr int kWideBatch = 20;                                   // ... or all of a run of up to 20, at once
 static_assert(MLA_MAX_SPLITS <= kThreads, "one lse per thread of an 8-warp unit");
 static_assert(MLA_MAX_SPLITS <= kWarps * 2 * kBatch, "a warp's run fits two load batches");
 
-template <int W>
+template <int W, int B>
 __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombineParams p, int rows) {
     __shared__ float weight[kThreads];                  // unit u's weights at u * 32 * unit_warps
     __shared__ float red_max[kWarps];
@@ -82,16 +83,16 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     // for slices without entries), so nothing here depends on the context length.
     const int tu = wl * 32 + lane;                     // thread within the unit: 32 * W >= S
     const float ls = (live && tu < S) ? p.lse_part[static_cast<long long>(bh) * S + tu] : -INFINITY;
-    const int run = (S + W - 1) / W;                   // <= 2 * kBatch (the host sizes W that way)
+    const int run = (S + W - 1) / W;                   // <= 2 * B (the host sizes W and B that way)
     const int s0 = wl * run;
     const int s1 = live ? min(S, s0 + run) : s0;
 
     // the first batch of this warp's partials, loaded before the weights are known
     const float4* src = reinterpret_cast<const float4*>(p.o_part + static_cast<long long>(bh) * S * kDLatent) +
                         chunk * (kCombineChunk / 4) + lane;
-    float4 v[kBatch];
+    float4 v[B];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
         const int s = s0 + i;
         v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
     // this warp's run, ascending slice order
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < B; ++i) {
         const int s = s0 + i;
         if (s < s1) {
             const float w = wt[s];
@@ -141,15 +142,15 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
             acc.w += w * v[i].w;
         }
     }
-    if (s0 + kBatch < s1) {
+    if (s0 + B < s1) {
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int s = s0 + kBatch + i;
+        for (int i = 0; i < B; ++i) {
+            const int s = s0 + B + i;
             v[i] = (s < s1) ? src[static_cast<long long>(s) * (kDLatent / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int s = s0 + kBatch + i;
+        for (int i = 0; i < B; ++i) {
+            const int s = s0 + B + i;
             if (s < s1) {
                 const float w = wt[s];
                 acc.x += w * v[i].x;
@@ -179,10 +180,12 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
 }  // namespace
 
 // Warps per (request, head) for S slices: enough threads for one lse each and
-// about 16 slices per warp (one load batch), rounded up to a power of two so
-// that 8 / W units share a CTA of 8 warps.
+// at most 20 slices per warp (one load batch) where 8 warps allow it, rounded
+// up to a power of two so that 8 / W units share a CTA of 8 warps (measured
+// against 16-slice runs: H=128 config step 37.65 -> 36.59 us, T=131072 30.80
+// -> 30.51 us per call).
 int combine_unit_warps(int splits) {
-    const int need = std::max((splits + 31) / 32, std::min((splits + kBatch - 1) / kBatch, kWarps));
+    const int need = std::max((splits + 31) / 32, std::min((splits + kWideBatch - 1) / kWideBatch, kWarps));
     int w = 1;
     while (w < need) w *= 2;
     return w;
@@ -201,7 +204,9 @@ int combine_grid_rows(int rows, int splits) {
 constexpr int kSpreadSmemBytes = 120 * 1024;
 
 cudaError_t combine_prepare() {
-    for (auto fn : {mla_combine_kernel<1>, mla_combine_kernel<2>, mla_combine_kernel<4>, mla_combine_kernel<8>}) {
+    for (auto fn : {mla_combine_kernel<1, kBatch>, mla_combine_kernel<2, kBatch>, mla_combine_kernel<4, kBatch>,
+                    mla_combine_kernel<8, kBatch>, mla_combine_kernel<1, kWideBatch>, mla_combine_kernel<2, kWideBatch>,
+                    mla_combine_kernel<4, kWideBatch>, mla_combine_kernel<8, kWideBatch>}) {
         const cudaError_t e =
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmemBytes);
         if (e != cudaSuccess) return e;
@@ -222,11 +227,22 @@ cudaError_t launch_combine(const CombineParams& p, dim3 grid, int block, bool pd
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const int rows = p.batch * p.heads;
-    switch (combine_unit_warps(p.splits)) {
-        case 1: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<1>, p, rows);
-        case 2: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<2>, p, rows);
-        case 4: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<4>, p, rows);
-        default: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<8>, p, rows);
+    const int w = combine_unit_warps(p.splits);
+    const int run = (p.splits + w - 1) / w;
+    if (run > kBatch && run <= kWideBatch) {
+        // a run of 17-20 slices: one batch of 20 loads instead of two dependent ones
+        switch (w) {
+            case 1: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<1, kWideBatch>, p, rows);
+            case 2: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<2, kWideBatch>, p, rows);
+            case 4: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<4, kWideBatch>, p, rows);
+            default: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<8, kWideBatch>, p, rows);
+        }
+    }
+    switch (w) {
+        case 1: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<1, kBatch>, p, rows);
+        case 2: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<2, kBatch>, p, rows);
+        case 4: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<4, kBatch>, p, rows);
+        default: return cudaLaunchKernelEx(&cfg, mla_combine_kernel<8, kBatch>, p, rows);
     }
 }
 

@@ -246,16 +246,16 @@ def test_plan_flat_split_covers_every_entry_once(batch, topk, sms, heads):
 
 
 def _unit_warps(splits):
-    """Warps that merge one (request, head): one lse per thread, about 16
+    """Warps that merge one (request, head): one lse per thread, at most 20
     slices per warp up to 8 warps, rounded up to a power of two."""
-    need = max(-(-splits // 32), min(-(-splits // 16), 8))
+    need = max(-(-splits // 32), min(-(-splits // 20), 8))
     w = 1
     while w < need:
         w *= 2
     return w
 
 
-@pytest.mark.parametrize("splits", [1, 2, 16, 17, 32, 33, 100, 128, 149, 256])
+@pytest.mark.parametrize("splits", [1, 2, 16, 17, 20, 21, 32, 33, 40, 41, 74, 80, 81, 100, 128, 149, 160, 161, 256])
 @pytest.mark.parametrize("batch", [1, 3, 64])
 def test_combine_grid_follows_the_split_count(splits, batch):
     p = _plan(max_ctx=131072, splits=splits, batch=batch)

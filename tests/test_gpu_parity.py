@@ -60,6 +60,18 @@ def test_dense_t8192_split_sweep(variant):
             assert (np.abs(results[a][1] - results[b][1]) / np.maximum(np.abs(rl), 1)).max() <= 2 * _gpu.LSE_RTOL
 
 
+@pytest.mark.parametrize("splits", [17, 20, 21, 40, 41, 80, 81, 160, 161, 256])
+def test_combine_unit_and_batch_shapes(splits):
+    """Split counts around every change of the combine's unit (1, 2, 4, 8
+    warps) and of its load batch (one batch of up to 20 slices per warp, or
+    two of 16), on the timed workload's shape, against the oracle."""
+    x = workloads.make("dense_t8192")
+    ro, rl = _gpu.oracle_dense(x)
+    out, lse, plan, _ = _gpu.run_dense(x, splits=splits, variant=1)
+    assert plan.splits == splits
+    _gpu.assert_parity(out, lse, ro, rl, f"dense_t8192 S={splits}")
+
+
 @pytest.mark.parametrize("T", [16384, 32768, 65536, 131072])
 def test_dense_context_sweep_workloads(T):
     """The H = 16 context sweep at full size, in the launch configuration the

@@ -13,7 +13,9 @@ kernel (live CUDA-event timing), the end-to-end number through the C ABI with
 host buffers, the oracle timed on the host cores (all threads and one), the SM
 clocks seen during the timed region, a `sweep` of the five workloads and the
 context sweep at H=16 (us per call, the partial kernel alone, fractions of the
-roofline) and a PDL on/off A/B (`pdl_ab`).  ``--impl reference`` times the fp64
+roofline), a PDL on/off A/B (`pdl_ab`) and the `floor` (what a call costs with
+no decode work: empty kernels, a bare bulk read, a bare row gather, beside
+the calls).  ``--impl reference`` times the fp64
 CPU oracle instead.  ``--details PATH`` also writes a longer table (split sweep,
 E4M3 cache, fused step, projection) to PATH.
 
@@ -1056,7 +1058,8 @@ def main():
     ap.add_argument("--pdl", type=int, default=int(os.environ.get("MLA_DECODE_PDL", "1")))
     ap.add_argument("--variant", type=int, default=int(os.environ.get("MLA_DECODE_VARIANT", "0")),
                     help="0 = the planner's choice (warp-MMA for this shape), 1 = warp-MMA kernel, "
-                         "2 / 3 / 4 = tcgen05 kernel with 16 / 32 / 64 heads per CTA")
+                         "2 / 3 / 4 = tcgen05 kernel with 16 / 32 / 64 heads per CTA, 5 = warp-MMA scores "
+                         "with P . V on tcgen05")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep, the PDL A/B and the floor")

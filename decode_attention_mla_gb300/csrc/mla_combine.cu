@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(kThreads) mla_combine_kernel(const CombinePara
 // Warps per (request, head) for S slices: enough threads for one lse each and
 // at most 20 slices per warp (one load batch) where 8 warps allow it, rounded
 // up to a power of two so that 8 / W units share a CTA of 8 warps (measured
-// against 16-slice runs: H=128 config step 37.65 -> 36.59 us, T=131072 30.80
-// -> 30.51 us per call).
+// against 16-slice runs: a dense H=128 decode step at T=32832, 37.65 -> 36.59
+// us; H=16 T=131072, 30.80 -> 30.51 us per call).
 int combine_unit_warps(int splits) {
     const int need = std::max((splits + 31) / 32, std::min((splits + kWideBatch - 1) / kWideBatch, kWarps));
     int w = 1;
